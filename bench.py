@@ -1,0 +1,419 @@
+"""Benchmark of the Muon update hot path on GB300.
+
+One step = one full Muon update (momentum + Nesterov, Frobenius normalisation,
+Newton-Schulz with the path chosen by the measured-cost autotune, shape-scaled
+decoupled-decay update) of the 2560 x 9728 bf16 matrix, through the C ABI, with
+parameters, momentum and gradient resident in HBM.  L2 is flushed (256 MiB
+write) between timed steps, outside the per-step CUDA events.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica of the workload (the matrices
+are independent units; no collective on the data path) and rank 0 prints one
+JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon-step matrices/s and NS TFLOP/s (fraction of GB300 dense BF16 peak)"
+UNIT = "matrices/s"
+WORKLOAD = "single_2560x9728_bf16"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        smax = max(num(r[2]) for r in rows)
+        busy = [s for s in sm if s > 0.5 * smax] or sm
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows)}
+
+
+def _gen_inputs(torch, wl, device):
+    """Seeded generator bytes for every matrix of the workload, moved to the device."""
+    import numpy as np
+    from workloads import gen_matrix, zeros_matrix
+    params, grads, moms, host_grads = [], [], [], []
+    for idx, r, c in wl.matrices():
+        seed = wl.seed(idx)
+        W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
+        G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
+        M = zeros_matrix(r, c, wl.mom_dtype)
+
+        def dev(h):
+            if h.dtype == "f32":
+                return torch.from_numpy(np.ascontiguousarray(h.data)).to(device)
+            return torch.from_numpy(np.ascontiguousarray(h.data).view(np.int16)).to(device).view(torch.bfloat16)
+
+        params.append(dev(W))
+        grads.append(dev(G))
+        moms.append(dev(M))
+        host_grads.append(G)
+    return params, grads, moms, host_grads
+
+
+def run_cpu_baseline(wl, max_seconds=30.0):
+    """The fp64 oracle as it stands, timed on the host cores on a bounded sample."""
+    from oracle import muon_oracle as orc
+    from workloads import gen_matrix, zeros_matrix
+    idx, r, c = next(wl.matrices())
+    seed = wl.seed(idx)
+    W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
+    G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
+    M = zeros_matrix(r, c, wl.mom_dtype)
+    path = "gram" if max(r, c) > min(r, c) else "plain"
+    done, t0 = 0, time.perf_counter()
+    while True:
+        orc.muon_step(W.data, M.data, G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov,
+                      path=path, param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype)
+        done += 1
+        el = time.perf_counter() - t0
+        if el * (done + 1) / done > max_seconds or done >= 3:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} full Muon step(s) of one {r}x{c} {wl.param_dtype} matrix, {path} NS, "
+                      f"numpy fp64 (BLAS threads = host cores)", "seconds": el}
+
+
+def bench_reference(args):
+    """--impl reference: the oracle as it stands on the host cores, same metric."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from oracle import muon_oracle as orc
+    from workloads import WORKLOADS, gen_matrix, zeros_matrix
+    wl = WORKLOADS[WORKLOAD]
+    idx, r, c = next(wl.matrices())
+    seed = wl.seed(idx)
+    W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
+    G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
+    M = zeros_matrix(r, c, wl.mom_dtype)
+
+    def step():
+        orc.muon_step(W.data, M.data, G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov,
+                      path="gram", param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * wl.count / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "matrices": wl.count, "shape": [r, c], "ns_path": "gram 2+2+1"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"one full Muon step of the {r}x{c} matrix per step (numpy fp64)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "epilogue.cuh", "muon_internal.cuh"):
+        with open(os.path.join(ROOT, "newton_schulz_frobenius_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _measured_traffic(kernel_key):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("kernel_hash") == _kernel_hash() and e.get("workload") == WORKLOAD_SEL[0]:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+WORKLOAD_SEL = [WORKLOAD]
+
+
+def _gen_device_inputs(torch, wl, device):
+    """Large stacks: seeded device RNG (same distributions), no host round trip."""
+    g = torch.Generator(device=device).manual_seed(1000 * wl.config_id)
+    pdt = torch.bfloat16 if wl.param_dtype == "bf16" else torch.float32
+    mdt = torch.bfloat16 if wl.mom_dtype == "bf16" else torch.float32
+    params, grads, moms = [], [], []
+    for _, r, c in wl.matrices():
+        params.append((torch.randn((r, c), generator=g, device=device) * wl.weight_std).to(pdt))
+        grads.append((torch.randn((r, c), generator=g, device=device) * wl.grad_std).to(pdt))
+        moms.append(torch.zeros((r, c), device=device, dtype=mdt))
+    return params, grads, moms
+
+
+def bench_gpu(args):
+    import torch
+    world, rank, local = _dist()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    import newton_schulz_frobenius_gb300 as mg
+    from workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    WORKLOAD_SEL[0] = args.workload
+    total_elems = sum(r * c for _, r, c in wl.matrices())
+    if total_elems <= 64 << 20:
+        params, grads, moms, _ = _gen_inputs(torch, wl, device)
+        data = "synthetic: seeded SplitMix64/Box-Muller generator bytes (workloads.py)"
+    else:
+        params, grads, moms = _gen_device_inputs(torch, wl, device)
+        data = "synthetic: seeded torch device RNG, same distributions (workloads.py shapes)"
+    hp = dict(lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    dtype_code = mg.MUON_BF16 if wl.param_dtype == "bf16" else mg.MUON_F32
+
+    # warm-up (the first step autotunes every distinct shape)
+    for _ in range(args.warmup):
+        mg.muon_step(params, grads, moms, **hp)
+    torch.cuda.synchronize()
+    st = mg.muon_sync_status()
+    if st != mg.MUON_OK:
+        raise RuntimeError(f"device status after warm-up: {mg.status_str(st)}")
+
+    shapes = sorted({(min(r, c), max(r, c)) for _, r, c in wl.matrices()})
+    paths = {f"{m}x{n}": ("gram" if mg.muon_last_path(m, n, dtype_code) == mg.MUON_PATH_GRAM else "plain")
+             for m, n in shapes}
+    alg_per_step = nom_per_step = 0.0
+    for _, r, c in wl.matrices():
+        m, n = min(r, c), max(r, c)
+        code = mg.MUON_PATH_GRAM if paths[f"{m}x{n}"] == "gram" else mg.MUON_PATH_PLAIN
+        nom, alg = mg.muon_ns_flops(m, n, code, (2, 2, 1))
+        alg_per_step += alg
+        nom_per_step += nom
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    mg.muon_kernel_timing_read()
+    mg.muon_set_kernel_timing(True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = mg.muon_launch_count()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush, outside the step's events
+        evs[i][0].record()
+        mg.muon_step(params, grads, moms, **hp)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = mg.muon_launch_count() - launches0
+    mg.muon_set_kernel_timing(False)
+    ktimes = mg.muon_kernel_timing_read()
+    clocks = sampler.stop()
+    st = mg.muon_sync_status()
+    if st != mg.MUON_OK:
+        raise RuntimeError(f"device status after timed steps: {mg.status_str(st)}")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(step_ms) / len(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.count / (ms * 1e-3)
+
+    # end to end through the public API: gradients from pinned host memory in,
+    # updated weights back to pinned host memory, every step
+    host_g = [g.cpu().pin_memory() for g in grads]
+    host_w = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
+    e2e_steps = max(3, min(args.steps, 20))
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    torch.cuda.synchronize()
+    for i in range(e2e_steps):
+        flush.zero_()
+        eev[i][0].record()
+        for dg, hg in zip(grads, host_g):
+            dg.copy_(hg, non_blocking=True)
+        mg.muon_step(params, grads, moms, **hp)
+        for hw, p in zip(host_w, params):
+            hw.copy_(p, non_blocking=True)
+        eev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(g.numel() * g.element_size() for g in grads)
+    d2h = sum(p.numel() * p.element_size() for p in params)
+
+    peaks = _peaks()
+    # dominant kernel: the tensor-core product instance with the largest device time
+    groups = {"gemm_tc_apply": ("gemm_tc_apply", "gemm_tc_apply_update"),
+              "gemm_tc_syrk": ("gemm_tc_syrk",), "gemm_tc_square": ("gemm_tc_square",),
+              "gemm_fp32": ("gemm_fp32",)}
+    best, best_ms, best_work, best_n = None, -1.0, 0.0, 0
+    for gname, members in groups.items():
+        tot = sum(ktimes.get(k, (0, 0.0, 0.0))[1] for k in members)
+        if tot > best_ms:
+            best, best_ms = gname, tot
+            best_work = sum(ktimes.get(k, (0, 0.0, 0.0))[2] for k in members)
+            best_n = sum(ktimes.get(k, (0, 0.0, 0.0))[0] for k in members)
+    roofline = None
+    if best_n:
+        achieved = best_work / (best_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roofline = {"kernel": best, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "launches": best_n, "avg_launch_ms": best_ms / best_n,
+                    "traffic": _measured_traffic(best),
+                    "peak_source": f"{peaks['source']} bf16_tflops (burst: kernels timed inside a ~ms step)"}
+    step_total_kernel_ms = sum(v[1] for v in ktimes.values()) / args.steps
+    ns_tflops = alg_per_step * world / (ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.param_dtype == "bf16" else "f32", "data": data,
+        "config": {"workload": args.workload, "matrices": wl.count,
+                   "shapes": [[r, c, k] for r, c, k in wl.shapes], "param_dtype": wl.param_dtype,
+                   "mom_dtype": wl.mom_dtype, "ns_paths": paths, "segments": "2+2+1", "steps_ns": 5,
+                   "lr": wl.lr, "beta": wl.beta, "wd": wl.wd, "nesterov": wl.nesterov,
+                   "l2": "flushed between timed steps (256 MiB device write outside the step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "ns_tflops": {"algorithmic": ns_tflops, "nominal": nom_per_step * world / (ms * 1e-3) / 1e12,
+                      "frac_of_bf16_peak": ns_tflops / world / peaks["bf16_tflops"],
+                      "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
+        "roofline": roofline,
+        "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
+                        "work_per_launch": v[2] / max(v[0], 1),
+                        "rate": (v[2] / (v[1] * 1e-3) / (1e12 if k.startswith("gemm") else 1e9)) if v[1] else None,
+                        "rate_unit": "TFLOP/s" if k.startswith("gemm") else "GB/s"}
+                    for k, v in ktimes.items()},
+        "kernel_ms_per_step": step_total_kernel_ms,
+        "e2e": {"value": world * wl.count / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "what": "gradients H2D from pinned host, muon_step, updated weights D2H to pinned host"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(wl)
+    elif rank == 0 and world == 1:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

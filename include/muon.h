@@ -1,0 +1,190 @@
+/*
+ * muon.h -- C ABI of the GB300 (sm_103a) Muon update library.
+ *
+ * One Muon update of a 2-D weight matrix W with gradient G and momentum M is
+ *
+ *   M' = beta M + G;   U = G + beta M' (Nesterov) or U = M'
+ *   X0 = U / (||U||_F + 1e-7)                       (oriented so rows <= cols)
+ *   O  = NS(X0)                                     (plain or Gram Newton-Schulz)
+ *   W' = W (1 - lr wd) - lr * 0.2 * sqrt(max(rows, cols)) * O
+ *
+ * Sources (page title, section):
+ *   "MuonX: DMuon 调整多卡分工, Gram NS 降低计算量" (CSDN), section 2: momentum
+ *     smooths the gradient, Newton-Schulz orthogonalises it; section 3.2
+ *     "Gram NS": iterate on the Gram matrix XX^T, accumulate the transform,
+ *     apply it to the long matrix only at segment boundaries, 2+2+1 segments.
+ *   "DMuon: Efficient Distributed Muon Training with Near-Adam Overhead"
+ *     (gist.science summary), section 2.2: Gram recursion for m < n, SYRK-style
+ *     symmetric products, batching of same-shape matrices; section 2.3-2.4:
+ *     per-shape measured cost, cached tuned kernel choice.
+ * The pages give neither the momentum rule, the NS polynomial, eps nor the
+ * update; the plain readings above are used (quintic coefficients
+ * (3.4445, -4.7750, 2.0315), 5 steps, sum-form Nesterov, decoupled decay).
+ *
+ * Conventions for every entry point
+ *   - Matrices are caller-owned DEVICE memory, row-major and contiguous.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All GPU work is enqueued on it; calls return once it is enqueued.
+ *   - Host-detectable errors return a negative muon_status and enqueue nothing.
+ *     Device-detected errors (non-finite norm, a bounded wait that gave up) are
+ *     recorded in a per-device status word read by muon_sync_status().
+ *   - No C++ exception crosses the ABI; no call aborts the process.
+ *   - The library keeps a workspace per (device, stream) that only grows; the
+ *     first call of a new shape set may allocate and therefore must not be made
+ *     while the stream is being captured into a CUDA graph.
+ *   - There is no CPU fallback: every step runs in the library's CUDA kernels.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_EINVAL = -1,      /* bad pointer, size, segment list or hyper-parameter */
+    MUON_EDTYPE = -2,      /* dtype not in muon_dtype or not supported for this call */
+    MUON_ENOMEM = -3,      /* workspace allocation failed */
+    MUON_ECUDA = -4,       /* a CUDA runtime/driver call failed (no device, launch error) */
+    MUON_ENONFINITE = -5,  /* device saw a non-finite Frobenius norm */
+    MUON_ETIMEOUT = -6,    /* a kernel's bounded wait gave up */
+    MUON_ENOTSUP = -7      /* no sm_103a device / feature unavailable */
+} muon_status;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+
+typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muon_path;
+
+/*
+ * Newton-Schulz orthogonalisation in place ("MuonX" page, section 3.2; "DMuon"
+ * summary, section 2.2).
+ *   ptr        device pointer to `batch` matrices of m x n, stride m*n elements.
+ *              Read as the NS input U, overwritten with O = NS(U/(||U||_F+eps)).
+ *              Each matrix is normalised on its own.  A matrix with m > n is
+ *              processed as its transpose; the result is written back untransposed.
+ *   dtype      MUON_F32 (fp32 path: fp32 FFMA products) or MUON_BF16 (bf16
+ *              tensor-core products, fp32 accumulation, bf16 intermediates).
+ *   coeffs     (a, b, c) of one NS step X <- aX + (bA + cA^2)X, A = XX^T.
+ *   steps      number of NS steps (>= 1).
+ *   segments   NULL or num_segments == 0: plain NS.  Otherwise Gram NS with
+ *              these segment lengths (each >= 1, sum == steps): per segment
+ *              G = XX^T, then P = aI + bG + cG^2, Q <- P (first) or PQ,
+ *              G <- PGP (not after the last), then X <- QX.
+ * Returns MUON_EINVAL for NULL ptr, m/n/batch < 1, steps < 1 or bad segments.
+ */
+int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype,
+                          const float coeffs[3], int steps, const int* segments,
+                          int num_segments, void* stream);
+
+/*
+ * One Muon step over `count` matrices (the optimizer call the pages' drop-in
+ * API names the participating matrices for: "DMuon" news page, section 3;
+ * "MuonX" page, section 3.3).
+ *   params[i]  device pointer, ms[i] x ns[i] weights, updated in place (param_dtype).
+ *   grads[i]   device pointer, same shape, read only (param_dtype).
+ *   moms[i]    device pointer, same shape, momentum updated in place (mom_dtype).
+ *   lr, beta, wd, nesterov   hyper-parameters of the update above.
+ * Matrices are bucketed by oriented shape; each bucket runs the NS path chosen
+ * by muon_set_ns_config (auto: measured-cost autotune per shape, cached).
+ * param_dtype MUON_F32 selects the fp32 path, MUON_BF16 the tensor-core path;
+ * mom_dtype may be either.  Arrays are host arrays of length `count`.
+ */
+int muon_step(void* const* params, const void* const* grads, void* const* moms,
+              const int64_t* ms, const int64_t* ns, int64_t count,
+              int param_dtype, int mom_dtype, float lr, float beta, float wd,
+              int nesterov, void* stream);
+
+/*
+ * NS configuration used by muon_step (process-wide, mutex-guarded).
+ * coeffs/steps as above; segments/num_segments give the Gram segmentation
+ * (default 2+2+1: "MuonX" page, section 3.2); path is a muon_path.
+ * NULL coeffs keeps the current coefficients.  The default is the quintic
+ * coefficients, 5 steps, 2+2+1, MUON_PATH_AUTO.
+ */
+int muon_set_ns_config(const float coeffs[3], int steps, const int* segments,
+                       int num_segments, int path);
+
+/*
+ * Measured-cost autotune ("DMuon" news page, section 3; "DMuon" summary,
+ * sections 2.3-2.4): for each distinct oriented shape in (ms[i], ns[i]) times
+ * the plain and the Gram path (and the tile choices of the long products) on
+ * synthetic data in the workspace with CUDA events (median of several runs)
+ * and caches the fastest.  Synchronises `stream`.  Never touches caller data.
+ */
+int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream);
+
+/* Persist / reload the tune cache (text file, keyed by device name, SM count,
+ * CUDA runtime version, shape and dtype).  A missing file or a stale or
+ * corrupt entry is ignored; returns the number of entries loaded (>= 0) or a
+ * negative status. */
+int muon_tune_save(const char* path);
+int muon_tune_load(const char* path);
+
+/* Which NS path (MUON_PATH_PLAIN / MUON_PATH_GRAM) muon_step last ran for this
+ * oriented-or-not shape and dtype.  MUON_EINVAL if the shape has not run. */
+int muon_last_path(int64_t m, int64_t n, int dtype, int* path_out);
+
+/* Synchronise `stream`, then read and clear the current device's status word:
+ * MUON_OK, MUON_ENONFINITE or MUON_ETIMEOUT (or MUON_ECUDA if the sync failed). */
+int muon_sync_status(void* stream);
+
+/* Human-readable name of a muon_status value (static string). */
+const char* muon_status_str(int status);
+
+/* Message of the last host-detected error on the calling thread ("" if none);
+ * valid until the thread's next failing call. */
+const char* muon_last_error_message(void);
+
+/*
+ * Product count of one NS update of an m x n matrix (oriented internally):
+ * nominal = sum of 2*M*N*K over the products ("MuonX" page, section 3.2 counts
+ * 1.443 -> 1.134 TFLOPs for 2560 x 9728); algorithmic counts products with a
+ * symmetric result (XX^T and products of polynomials in the same Gram matrix)
+ * as half.  path is MUON_PATH_PLAIN or MUON_PATH_GRAM (segments required).
+ */
+int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_segments,
+                  double* nominal, double* algorithmic);
+
+/* ---- diagnostics (not part of the method) ---------------------------------- */
+
+/* Total kernels this library has launched in this process. */
+int64_t muon_launch_count(void);
+
+/* Enable (1) or disable (0) per-launch CUDA-event timing of the library's
+ * kernels, recorded on the launching stream.  Reading resets the record. */
+int muon_set_kernel_timing(int enable);
+
+/*
+ * Read the per-class timing record: for class k (0 <= k < max_classes)
+ * writes its name into names (max_classes x 32 chars), its launches, total
+ * milliseconds, and its algorithmic work per class (flops for products,
+ * bytes for elementwise kernels).  Synchronises the recorded events.
+ * Returns the number of classes written.
+ */
+int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms,
+                            double* work, int max_classes);
+
+/*
+ * Single product launch for kernel-level tests (bf16 or fp32 path):
+ *   C[b] = alpha * A[b] * op(B[b])  for b < batch, row-major, device pointers.
+ *   A is M x K.  b_kmajor != 0: B is stored N x K and op(B) = B^T;
+ *   b_kmajor == 0: B is stored K x N and op(B) = B.
+ *   symmetric != 0 requires M == N and writes only the lower triangle's
+ *   values, mirrored (C[j][i] = C[i][j]); valid when the exact product is
+ *   symmetric.  poly != 0 (symmetric only, A == B == G) writes
+ *   pa*I + pb*G + pc*(G G) instead of the product.
+ *   C is M x N.  dtype is the storage type of A, B and C.  tile_n selects the
+ *   N extent of the tensor-core tile (0 = default, 128 or 256).
+ */
+int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                    int64_t batch, int dtype, int b_kmajor, int symmetric, int poly,
+                    float alpha, float pa, float pb, float pc, int tile_n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

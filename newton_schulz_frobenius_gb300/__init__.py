@@ -1,0 +1,260 @@
+"""Python binding of the GB300 Muon update library (``include/muon.h``).
+
+Argument marshalling only: every step of the update runs in the library's CUDA
+kernels.  The functions keep the C names; tensors are PyTorch CUDA tensors
+(PyTorch supplies device memory and streams).  Loading fails loudly when the
+shared library has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmuon_gb300.so")
+
+MUON_OK = 0
+MUON_EINVAL = -1
+MUON_EDTYPE = -2
+MUON_ENOMEM = -3
+MUON_ECUDA = -4
+MUON_ENONFINITE = -5
+MUON_ETIMEOUT = -6
+MUON_ENOTSUP = -7
+
+MUON_F32 = 0
+MUON_BF16 = 1
+
+MUON_PATH_AUTO = 0
+MUON_PATH_PLAIN = 1
+MUON_PATH_GRAM = 2
+
+QUINTIC = (3.4445, -4.7750, 2.0315)
+
+#: every entry point include/muon.h declares
+EXPORTS = (
+    "muon_ns_orthogonalize", "muon_step", "muon_set_ns_config", "muon_autotune",
+    "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
+    "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
+    "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
+)
+
+_lib = None
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({last_error_message()})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                          "(nvcc, sm_103a); there is no CPU fallback")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    f3 = ctypes.POINTER(ctypes.c_float)
+    ip = ctypes.POINTER(ctypes.c_int)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    sig = {
+        "muon_ns_orthogonalize": (i32, [vp, i64, i64, i64, i32, f3, i32, ip, i32, vp]),
+        "muon_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), i64p, i64p, i64,
+                            i32, i32, f32, f32, f32, i32, vp]),
+        "muon_set_ns_config": (i32, [f3, i32, ip, i32, i32]),
+        "muon_autotune": (i32, [i64p, i64p, i64, i32, vp]),
+        "muon_tune_save": (i32, [ctypes.c_char_p]),
+        "muon_tune_load": (i32, [ctypes.c_char_p]),
+        "muon_last_path": (i32, [i64, i64, i32, ip]),
+        "muon_sync_status": (i32, [vp]),
+        "muon_status_str": (ctypes.c_char_p, [i32]),
+        "muon_last_error_message": (ctypes.c_char_p, []),
+        "muon_ns_flops": (i32, [i64, i64, i32, ip, i32, dp, dp]),
+        "muon_launch_count": (i64, []),
+        "muon_set_kernel_timing": (i32, [i32]),
+        "muon_kernel_timing_read": (i32, [ctypes.c_char_p, i64p, dp, dp, i32]),
+        "muon_debug_gemm": (i32, [vp, vp, vp, i64, i64, i64, i64, i32, i32, i32, i32,
+                                  f32, f32, f32, f32, i32, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def status_str(status: int) -> str:
+    return lib().muon_status_str(int(status)).decode()
+
+
+def last_error_message() -> str:
+    return lib().muon_last_error_message().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != MUON_OK:
+        raise MuonError(status, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return MUON_F32
+    if t.dtype == torch.bfloat16:
+        return MUON_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ints(vals):
+    vals = list(vals or [])
+    return (ctypes.c_int * max(1, len(vals)))(*vals), len(vals)
+
+
+def _cuda_contig(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+# ---------------------------------------------------------------------------
+# the entry points
+# ---------------------------------------------------------------------------
+
+def muon_ns_orthogonalize(x, coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1), stream=None):
+    """In place: x (m x n or batch x m x n) <- NS(x / ||x||_F).  segments=None: plain NS."""
+    _cuda_contig(x, "x")
+    if x.dim() == 2:
+        batch, m, n = 1, x.shape[0], x.shape[1]
+    elif x.dim() == 3:
+        batch, m, n = x.shape
+    else:
+        raise ValueError("x must be 2-D or 3-D")
+    c = (ctypes.c_float * 3)(*coeffs)
+    segs, nseg = _ints(segments)
+    _check(lib().muon_ns_orthogonalize(x.data_ptr(), m, n, batch, _dtype_code(x), c, steps, segs, nseg,
+                                       _stream_ptr(stream)), "muon_ns_orthogonalize")
+    return x
+
+
+def muon_step(params, grads, moms, lr: float, beta: float, wd: float, nesterov: bool, stream=None):
+    """One Muon step over lists of matrices (updated in place: params, moms)."""
+    k = len(params)
+    if not (len(grads) == k and len(moms) == k):
+        raise ValueError("params, grads and moms must have the same length")
+    if k == 0:
+        return
+    pd = _dtype_code(params[0])
+    md = _dtype_code(moms[0])
+    for i in range(k):
+        p, g, mo = params[i], grads[i], moms[i]
+        for t, nm in ((p, "param"), (g, "grad"), (mo, "mom")):
+            _cuda_contig(t, nm)
+            if t.dim() != 2:
+                raise ValueError(f"{nm} {i} must be 2-D")
+        if p.shape != g.shape or p.shape != mo.shape:
+            raise ValueError(f"shape mismatch at {i}")
+        if _dtype_code(p) != pd or _dtype_code(g) != pd or _dtype_code(mo) != md:
+            raise TypeError(f"dtype mismatch at {i}")
+    VP = ctypes.c_void_p * k
+    I64 = ctypes.c_int64 * k
+    _check(lib().muon_step(VP(*[p.data_ptr() for p in params]), VP(*[g.data_ptr() for g in grads]),
+                           VP(*[m.data_ptr() for m in moms]), I64(*[p.shape[0] for p in params]),
+                           I64(*[p.shape[1] for p in params]), k, pd, md, float(lr), float(beta), float(wd),
+                           1 if nesterov else 0, _stream_ptr(stream)), "muon_step")
+
+
+def muon_set_ns_config(coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1), path: int = MUON_PATH_AUTO):
+    c = (ctypes.c_float * 3)(*coeffs) if coeffs is not None else None
+    segs, nseg = _ints(segments)
+    _check(lib().muon_set_ns_config(c, steps, segs, nseg, path), "muon_set_ns_config")
+
+
+def muon_autotune(shapes, dtype: int = MUON_BF16, stream=None):
+    shapes = list(shapes)
+    k = len(shapes)
+    I64 = ctypes.c_int64 * max(1, k)
+    _check(lib().muon_autotune(I64(*[s[0] for s in shapes]), I64(*[s[1] for s in shapes]), k, dtype,
+                               _stream_ptr(stream)), "muon_autotune")
+
+
+def muon_tune_save(path: str):
+    _check(lib().muon_tune_save(path.encode()), "muon_tune_save")
+
+
+def muon_tune_load(path: str) -> int:
+    r = lib().muon_tune_load(path.encode())
+    if r < 0:
+        raise MuonError(r, "muon_tune_load")
+    return r
+
+
+def muon_last_path(m: int, n: int, dtype: int):
+    out = ctypes.c_int(-1)
+    r = lib().muon_last_path(m, n, dtype, ctypes.byref(out))
+    return out.value if r == MUON_OK else None
+
+
+def muon_sync_status(stream=None) -> int:
+    return lib().muon_sync_status(_stream_ptr(stream))
+
+
+def muon_ns_flops(m: int, n: int, path: int, segments=(2, 2, 1)):
+    segs, nseg = _ints(segments)
+    nom, alg = ctypes.c_double(), ctypes.c_double()
+    _check(lib().muon_ns_flops(m, n, path, segs, nseg, ctypes.byref(nom), ctypes.byref(alg)), "muon_ns_flops")
+    return nom.value, alg.value
+
+
+def muon_launch_count() -> int:
+    return lib().muon_launch_count()
+
+
+def muon_set_kernel_timing(enable: bool):
+    lib().muon_set_kernel_timing(1 if enable else 0)
+
+
+def muon_kernel_timing_read():
+    """{class name: (launches, total_ms, algorithmic work)}; resets the record."""
+    n = 16
+    names = ctypes.create_string_buffer(32 * n)
+    launches = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    work = (ctypes.c_double * n)()
+    k = lib().muon_kernel_timing_read(names, launches, ms, work, n)
+    out = {}
+    for i in range(k):
+        nm = names.raw[32 * i:32 * i + 32].split(b"\0", 1)[0].decode()
+        if launches[i]:
+            out[nm] = (int(launches[i]), float(ms[i]), float(work[i]))
+    return out
+
+
+def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.0, tile_n=0, stream=None):
+    """C[b] = alpha * A[b] op(B[b]) (or the fused polynomial when poly=(a, b, c))."""
+    for t, nm in ((A, "A"), (B, "B"), (C, "C")):
+        _cuda_contig(t, nm)
+    batch = A.shape[0] if A.dim() == 3 else 1
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-2] if b_kmajor else B.shape[-1]
+    pa, pb, pc = poly if poly is not None else (0.0, 0.0, 0.0)
+    _check(lib().muon_debug_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, batch, _dtype_code(A),
+                                 1 if b_kmajor else 0, 1 if symmetric else 0, 1 if poly is not None else 0,
+                                 float(alpha), float(pa), float(pb), float(pc), tile_n, _stream_ptr(stream)),
+           "muon_debug_gemm")
+    return C

@@ -1,0 +1,1069 @@
+// Host runtime of the Muon update library: argument validation, per-device
+// state, workspace, shape bucketing, the Newton-Schulz driver (plain and Gram
+// with segment restarts), the measured-cost autotune with its persistent cache,
+// and the C ABI declared in include/muon.h.
+//
+// Shape-adaptive execution follows the "DMuon" pages: matrices are grouped by
+// shape (news page, section 3; summary, section 2.2 "batching"), each distinct
+// shape is timed once per candidate scheme and the fastest is cached and reused
+// (summary, sections 2.3-2.4).  Gram NS with restarts is the "MuonX" page,
+// section 3.2.
+#include "muon_internal.cuh"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <map>
+#include <mutex>
+#include <sstream>
+#include <string>
+#include <tuple>
+#include <vector>
+
+namespace muon {
+
+// ---------------------------------------------------------------------------
+// logging and errors
+// ---------------------------------------------------------------------------
+
+static int log_level() {
+    static int lvl = [] {
+        const char* e = std::getenv("MUON_LOG");
+        return e ? std::atoi(e) : 0;
+    }();
+    return lvl;
+}
+
+static thread_local std::string t_last_error;
+
+static void logf(int lvl, const char* fmt, ...) {
+    if (log_level() < lvl) return;
+    va_list ap;
+    va_start(ap, fmt);
+    std::fprintf(stderr, "[muon] ");
+    std::vfprintf(stderr, fmt, ap);
+    std::fprintf(stderr, "\n");
+    va_end(ap);
+}
+
+static int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    logf(1, "error %d: %s", status, buf);
+    return status;
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+    return fail(MUON_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MUON_CUDA(call)                                   \
+    do {                                                  \
+        cudaError_t e_ = (call);                          \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// per-device state
+// ---------------------------------------------------------------------------
+
+struct DevCtx {
+    int device = -1;
+    int sms = 0;
+    int major = 0, minor = 0;
+    std::string name;
+    int* status = nullptr;     // device status word
+};
+
+static std::mutex g_mu;                 // guards every global below
+static std::map<int, DevCtx> g_dev;
+
+static int get_dev(DevCtx& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it == g_dev.end()) {
+        cudaDeviceProp p;
+        e = cudaGetDeviceProperties(&p, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        DevCtx c;
+        c.device = dev;
+        c.sms = p.multiProcessorCount;
+        c.major = p.major;
+        c.minor = p.minor;
+        c.name = p.name;
+        if (!(c.major == 10 && c.minor == 3))
+            return fail(MUON_ENOTSUP, "device %d (%s) is sm_%d%d; this library is built for sm_103a", dev,
+                        p.name, c.major, c.minor);
+        e = cudaMalloc(&c.status, 64);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+        e = cudaMemset(c.status, 0, 64);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+        it = g_dev.emplace(dev, c).first;
+    }
+    out = it->second;
+    return MUON_OK;
+}
+
+// ---------------------------------------------------------------------------
+// workspace: one grow-only device buffer and a pinned staging ring for the
+// matrix tables, per (device, stream)
+// ---------------------------------------------------------------------------
+
+constexpr int STAGE_SLOTS = 4;
+
+struct Workspace {
+    char* base = nullptr;
+    size_t bytes = 0;
+    MatEntry* h_stage[STAGE_SLOTS] = {nullptr, nullptr, nullptr, nullptr};
+    cudaEvent_t ev[STAGE_SLOTS] = {nullptr, nullptr, nullptr, nullptr};
+    size_t stage_cap = 0;   // entries per slot
+    int slot = 0;
+};
+
+static std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static int ws_get(int dev, cudaStream_t s, size_t need, Workspace** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.bytes < need) {
+        if (w.base) {
+            cudaError_t e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize(workspace grow)");
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        size_t want = align_up(need + need / 4, 1 << 20);
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&w.base), want);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(MUON_ENOMEM, "workspace allocation of %zu bytes failed: %s", want, cudaGetErrorString(e));
+        }
+        w.bytes = want;
+        logf(2, "workspace grown to %zu bytes on device %d", want, dev);
+    }
+    *out = &w;
+    return MUON_OK;
+}
+
+// Copies `n` table entries to `d_dst` on stream `s` through the pinned ring.
+static int upload_table(Workspace& w, const std::vector<MatEntry>& h, MatEntry* d_dst, cudaStream_t s) {
+    if (h.empty()) return MUON_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (w.stage_cap < h.size()) {
+        for (int i = 0; i < STAGE_SLOTS; ++i) {
+            if (w.ev[i]) cudaEventSynchronize(w.ev[i]);
+            if (w.h_stage[i]) cudaFreeHost(w.h_stage[i]);
+            w.h_stage[i] = nullptr;
+        }
+        size_t cap = std::max<size_t>(h.size(), 256);
+        for (int i = 0; i < STAGE_SLOTS; ++i) {
+            cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&w.h_stage[i]), cap * sizeof(MatEntry));
+            if (e != cudaSuccess) return fail(MUON_ENOMEM, "pinned staging allocation failed");
+            if (!w.ev[i]) {
+                e = cudaEventCreateWithFlags(&w.ev[i], cudaEventDisableTiming);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+            }
+        }
+        w.stage_cap = cap;
+    }
+    const int slot = w.slot;
+    w.slot = (w.slot + 1) % STAGE_SLOTS;
+    cudaError_t e = cudaEventSynchronize(w.ev[slot]);   // the copy made from this slot before has run
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize(stage)");
+    std::memcpy(w.h_stage[slot], h.data(), h.size() * sizeof(MatEntry));
+    e = cudaMemcpyAsync(d_dst, w.h_stage[slot], h.size() * sizeof(MatEntry), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(table)");
+    e = cudaEventRecord(w.ev[slot], s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stage)");
+    return MUON_OK;
+}
+
+// ---------------------------------------------------------------------------
+// launch accounting and optional per-launch event timing
+// ---------------------------------------------------------------------------
+
+static std::atomic<int64_t> g_launches{0};
+static std::atomic<int> g_timing{0};
+
+struct TimedLaunch {
+    int kclass;
+    cudaEvent_t a, b;
+    double work;
+};
+static std::vector<TimedLaunch> g_timed;
+static std::vector<cudaEvent_t> g_event_pool;
+static thread_local int t_open = -1;   // index of the launch being recorded
+
+static const char* kclass_name(int k) {
+    static const char* names[KC_COUNT] = {"prep_momentum_norm", "norm_finalize", "gemm_tc_syrk",
+                                          "gemm_tc_square", "gemm_tc_apply", "gemm_tc_apply_update",
+                                          "gemm_fp32", "other"};
+    return (k >= 0 && k < KC_COUNT) ? names[k] : "other";
+}
+
+static cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+void note_launch_begin(int kclass, cudaStream_t s) {
+    g_launches.fetch_add(1);
+    if (!g_timing.load()) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    TimedLaunch t{kclass, pool_event(), pool_event(), 0.0};
+    cudaEventRecord(t.a, s);
+    g_timed.push_back(t);
+    t_open = (int)g_timed.size() - 1;
+}
+
+void note_launch_end(int kclass, double work, cudaStream_t s) {
+    (void)kclass;
+    if (!g_timing.load() || t_open < 0) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (t_open < (int)g_timed.size()) {
+        cudaEventRecord(g_timed[t_open].b, s);
+        g_timed[t_open].work = work;
+    }
+    t_open = -1;
+}
+
+}  // namespace muon
+
+namespace muon {
+
+// ---------------------------------------------------------------------------
+// NS configuration
+// ---------------------------------------------------------------------------
+
+struct NsConfig {
+    float coeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+    int steps = 5;
+    std::vector<int> segments{2, 2, 1};
+    int path = MUON_PATH_AUTO;
+};
+static NsConfig g_cfg;
+
+static int validate_segments(int steps, const int* segs, int nseg) {
+    if (steps < 1 || steps > 64) return fail(MUON_EINVAL, "steps must be in [1, 64], got %d", steps);
+    if (nseg < 0 || (nseg > 0 && !segs)) return fail(MUON_EINVAL, "bad segment list");
+    if (nseg == 0) return MUON_OK;
+    int sum = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (segs[i] < 1) return fail(MUON_EINVAL, "segment %d has length %d < 1", i, segs[i]);
+        sum += segs[i];
+    }
+    if (sum != steps) return fail(MUON_EINVAL, "segments sum to %d, steps is %d", sum, steps);
+    return MUON_OK;
+}
+
+// A resolved NS plan: the segment lengths actually run.  The plain path is
+// the Gram driver with unit segments (per step: XX^T, P = aI + bA + cA^2,
+// X <- P X), which performs the plain algorithm's products one for one.
+struct NsPlan {
+    float a, b, c;
+    std::vector<int> segs;
+    int path;       // MUON_PATH_PLAIN or MUON_PATH_GRAM
+    int tile_n;     // tensor-core N extent of the long products
+};
+
+static NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_segs, int path, int tile_n) {
+    NsPlan p;
+    p.a = coeffs[0];
+    p.b = coeffs[1];
+    p.c = coeffs[2];
+    p.path = path;
+    p.tile_n = tile_n;
+    if (path == MUON_PATH_GRAM && !gram_segs.empty()) p.segs = gram_segs;
+    else p.segs.assign(steps, 1);
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// products
+// ---------------------------------------------------------------------------
+
+static GemmArgs gemm_base(int dtype, int* status) {
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.dtype = dtype;
+    a.alpha = 1.0f;
+    a.tile_n = 256;
+    a.status = status;
+    a.b_kmajor = 1;
+    return a;
+}
+
+static int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
+    const double mnk = (double)a.M * a.N * a.K * a.batch;
+    const double work = a.symmetric ? mnk : 2.0 * mnk;
+    const int kc = (a.dtype == MUON_BF16) ? kclass : KC_SIMT;
+    note_launch_begin(kc, s);
+    cudaError_t e = (a.dtype == MUON_BF16) ? launch_gemm_tc(a, dc.sms, s) : launch_gemm_simt(a, s);
+    note_launch_end(kc, work, s);
+    if (e != cudaSuccess) return cuda_fail(e, "product launch");
+    return MUON_OK;
+}
+
+static size_t esize(int dtype) { return dtype == MUON_BF16 ? 2 : 4; }
+static int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
+
+// Workspace of one chunk of B matrices of oriented shape m x n.
+struct ChunkLayout {
+    int64_t ldx, ldm;
+    size_t x_bytes, m_bytes;            // one matrix
+    size_t off_X, off_X2, off_G, off_S[3], off_inv, off_part, total;
+    int nparts;
+};
+
+static ChunkLayout chunk_layout(int m, int n, int B, int dtype) {
+    ChunkLayout L;
+    const size_t es = esize(dtype);
+    L.ldx = pad8(n);
+    L.ldm = pad8(m);
+    L.x_bytes = (size_t)m * L.ldx * es;
+    L.m_bytes = (size_t)m * L.ldm * es;
+    L.nparts = prep_num_parts(m, n);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.off_X = take(L.x_bytes * B);
+    L.off_X2 = take(L.x_bytes * B);
+    L.off_G = take(L.m_bytes * B);
+    for (int i = 0; i < 3; ++i) L.off_S[i] = take(L.m_bytes * B);
+    L.off_inv = take(sizeof(float) * B);
+    L.off_part = take(sizeof(float) * (size_t)L.nparts * B);
+    L.total = o;
+    return L;
+}
+
+// Final epilogue of an NS run.
+struct FinalEpi {
+    int kind;               // EPI_UPDATE, EPI_OUT or EPI_STORE (autotune: into the workspace)
+    const MatEntry* mats;   // device table (UPDATE / OUT)
+    int out_dtype;
+    float lr, wd, scale;
+};
+
+// Runs NS on B oriented m x n matrices held (unnormalised when use_inv) in
+// the chunk's X buffer, ending in `fin`.
+static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
+                  int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin) {
+    char* X = base + L.off_X;
+    char* Xn = base + L.off_X2;
+    char* G = base + L.off_G;
+    char* S[3] = {base + L.off_S[0], base + L.off_S[1], base + L.off_S[2]};
+    const float* inv = reinterpret_cast<const float*>(base + L.off_inv);
+    const int64_t strideX = (int64_t)m * L.ldx;
+    const int64_t strideM = (int64_t)m * L.ldm;
+
+    auto sym = [&](const void* A, const void* Bm, void* C) {
+        GemmArgs g = gemm_base(dtype, dc.status);
+        g.A = A; g.lda = L.ldm; g.strideA = strideM;
+        g.B = Bm; g.ldb = L.ldm; g.strideB = strideM;
+        g.M = m; g.N = m; g.K = m; g.batch = B;
+        g.symmetric = 1;
+        g.epi = EPI_STORE;
+        g.C = C; g.ldc = L.ldm; g.strideC = strideM;
+        return g;
+    };
+
+    const int nseg = (int)plan.segs.size();
+    for (int si = 0; si < nseg; ++si) {
+        const int Lseg = plan.segs[si];
+        const bool first = (si == 0);
+        const bool last = (si == nseg - 1);
+
+        // G = X X^T  (lower triangle, mirrored); first segment folds 1/||U||^2
+        {
+            GemmArgs g = gemm_base(dtype, dc.status);
+            g.A = X; g.lda = L.ldx; g.strideA = strideX;
+            g.B = X; g.ldb = L.ldx; g.strideB = strideX;
+            g.M = m; g.N = m; g.K = n; g.batch = B;
+            g.symmetric = 1;
+            g.epi = EPI_STORE;
+            g.C = G; g.ldc = L.ldm; g.strideC = strideM;
+            if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 1; }
+            int r = run_gemm(dc, s, g, KC_SYRK);
+            if (r) return r;
+        }
+
+        bool used[3] = {false, false, false};
+        auto grab = [&]() {
+            for (int i = 0; i < 3; ++i)
+                if (!used[i]) { used[i] = true; return i; }
+            return -1;
+        };
+        int q = -1;
+        for (int j = 1; j <= Lseg; ++j) {
+            // P = aI + bG + cG^2, fused into the G^2 product
+            const int p = grab();
+            {
+                GemmArgs g = sym(G, G, S[p]);
+                g.epi = EPI_POLY;
+                g.Gin = G; g.ldg = L.ldm; g.strideG = strideM;
+                g.pa = plan.a; g.pb = plan.b; g.pc = plan.c;
+                int r = run_gemm(dc, s, g, KC_SQUARE);
+                if (r) return r;
+            }
+            if (j == 1) {
+                q = p;
+            } else {
+                const int qn = grab();     // Q <- P Q
+                int r = run_gemm(dc, s, sym(S[p], S[q], S[qn]), KC_SQUARE);
+                if (r) return r;
+                used[q] = false;
+                q = qn;
+            }
+            if (j < Lseg) {
+                const int t = grab();      // G <- (P G) P
+                int r = run_gemm(dc, s, sym(S[p], G, S[t]), KC_SQUARE);
+                if (r) return r;
+                r = run_gemm(dc, s, sym(S[t], S[p], G), KC_SQUARE);
+                if (r) return r;
+                used[t] = false;
+            }
+            if (p != q) used[p] = false;
+        }
+
+        // X <- Q X: B operand is X itself, read MN-major
+        GemmArgs g = gemm_base(dtype, dc.status);
+        g.A = S[q]; g.lda = L.ldm; g.strideA = strideM;
+        g.B = X; g.ldb = L.ldx; g.strideB = strideX; g.b_kmajor = 0;
+        g.M = m; g.N = n; g.K = m; g.batch = B;
+        g.tile_n = plan.tile_n;
+        if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 0; }
+        int kc = KC_APPLY;
+        if (!last || fin.kind == EPI_STORE) {
+            g.epi = EPI_STORE;
+            g.C = Xn; g.ldc = L.ldx; g.strideC = strideX;
+        } else {
+            g.epi = fin.kind;
+            g.mats = fin.mats;
+            g.out_dtype = fin.out_dtype;
+            g.lr = fin.lr; g.wd = fin.wd; g.scale = fin.scale;
+            if (fin.kind == EPI_UPDATE) kc = KC_APPLY_UPDATE;
+        }
+        int r = run_gemm(dc, s, g, kc);
+        if (r) return r;
+        std::swap(X, Xn);
+    }
+    return MUON_OK;
+}
+
+static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
+                    const MatEntry* d_mats, int in_dtype, int mom_dtype, int x_dtype, bool with_mom, int nesterov,
+                    float beta, bool vec_ok) {
+    PrepArgs p;
+    std::memset(&p, 0, sizeof p);
+    p.mats = d_mats;
+    p.m = m; p.n = n; p.batch = B;
+    p.in_dtype = in_dtype; p.mom_dtype = mom_dtype; p.x_dtype = x_dtype;
+    p.with_momentum = with_mom ? 1 : 0;
+    p.nesterov = nesterov;
+    p.beta = beta;
+    p.X = base + L.off_X; p.ldx = L.ldx; p.strideX = (int64_t)m * L.ldx;
+    p.partials = reinterpret_cast<float*>(base + L.off_part);
+    p.nparts = L.nparts;
+    p.vec_ok = vec_ok ? 1 : 0;
+    const double elems = (double)m * n * B;
+    const double bytes = elems * (esize(in_dtype) + (with_mom ? 2.0 * esize(mom_dtype) : 0.0) + esize(x_dtype));
+    note_launch_begin(KC_PREP, s);
+    cudaError_t e = launch_prep(p, s);
+    note_launch_end(KC_PREP, bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+    note_launch_begin(KC_NORM, s);
+    e = launch_norm_finalize(p.partials, L.nparts, B, 1e-7f, reinterpret_cast<float*>(base + L.off_inv),
+                             dc.status, s);
+    note_launch_end(KC_NORM, (double)L.nparts * B * 4.0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "norm launch");
+    return MUON_OK;
+}
+
+}  // namespace muon
+
+namespace muon {
+
+// ---------------------------------------------------------------------------
+// measured-cost autotune and its cache
+// ---------------------------------------------------------------------------
+
+struct TuneEntry {
+    int path;
+    int tile_n;
+    double ms_per_matrix;
+};
+using TuneKey = std::tuple<std::string, int, int, int64_t, int64_t, int>;   // device, sms, cudart, m, n, dtype
+static std::map<TuneKey, TuneEntry> g_tune;
+static std::map<std::tuple<int64_t, int64_t, int>, int> g_last_path;     // oriented m, n, dtype -> path
+
+static int cudart_version() {
+    int v = 0;
+    cudaRuntimeGetVersion(&v);
+    return v;
+}
+
+static TuneKey tune_key(const DevCtx& dc, int64_t m, int64_t n, int dtype) {
+    return TuneKey{dc.name, dc.sms, cudart_version(), m, n, dtype};
+}
+
+static bool env_flag(const char* name, bool dflt) {
+    const char* e = std::getenv(name);
+    if (!e || !*e) return dflt;
+    return !(e[0] == '0' || e[0] == 'n' || e[0] == 'N' || e[0] == 'f' || e[0] == 'F');
+}
+
+static int save_tune_file(const char* path);
+
+static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int B, const NsConfig& cfg,
+                          TuneEntry* out) {
+    const ChunkLayout L = chunk_layout(m, n, B, dtype);
+    Workspace* w = nullptr;
+    int r = ws_get(dc.device, s, L.total, &w);
+    if (r) return r;
+    char* base = w->base;
+
+    std::vector<std::pair<int, int>> cands;   // (path, tile_n)
+    const int tiles[2] = {256, 128};
+    const int ntiles = (dtype == MUON_BF16) ? 2 : 1;
+    for (int ti = 0; ti < ntiles; ++ti) {
+        cands.push_back({MUON_PATH_PLAIN, tiles[ti]});
+        if (!cfg.segments.empty()) cands.push_back({MUON_PATH_GRAM, tiles[ti]});
+    }
+    cudaEvent_t e0, e1;
+    MUON_CUDA(cudaEventCreate(&e0));
+    MUON_CUDA(cudaEventCreate(&e1));
+    FinalEpi fin{EPI_STORE, nullptr, dtype, 0.f, 0.f, 0.f};
+    const float scale = std::sqrt(3.0f / ((float)m * (float)n));
+    TuneEntry best{MUON_PATH_PLAIN, 256, 1e300};
+    const int reps = 3;
+    for (auto& c : cands) {
+        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, c.first, c.second);
+        std::vector<float> times;
+        for (int rep = 0; rep <= reps; ++rep) {
+            cudaError_t e = launch_fill_synthetic(base + L.off_X, (int64_t)B * m * L.ldx, dtype, scale,
+                                                  0x5eed0000u + (uint32_t)rep, s);
+            if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+            MUON_CUDA(cudaEventRecord(e0, s));
+            r = run_ns(dc, s, base, L, m, n, B, dtype, plan, false, fin);
+            if (r) return r;
+            MUON_CUDA(cudaEventRecord(e1, s));
+            MUON_CUDA(cudaEventSynchronize(e1));
+            float ms = 0.f;
+            MUON_CUDA(cudaEventElapsedTime(&ms, e0, e1));
+            if (rep > 0) times.push_back(ms);   // rep 0 is the warm-up
+        }
+        std::sort(times.begin(), times.end());
+        const double med = times[times.size() / 2] / B;
+        logf(2, "autotune %dx%d dtype %d path %d tile %d: %.4f ms/matrix", m, n, dtype, c.first, c.second, med);
+        if (med < best.ms_per_matrix) best = TuneEntry{c.first, c.second, med};
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    *out = best;
+    return MUON_OK;
+}
+
+// Chooses path and tile for one oriented shape.
+static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int bucket_count,
+                       const NsConfig& cfg, NsPlan* plan) {
+    int path = cfg.path;
+    if (const char* f = std::getenv("MUON_FORCE_PATH")) {
+        if (!std::strcmp(f, "plain")) path = MUON_PATH_PLAIN;
+        else if (!std::strcmp(f, "gram")) path = MUON_PATH_GRAM;
+    }
+    if (path == MUON_PATH_GRAM && cfg.segments.empty()) path = MUON_PATH_PLAIN;
+    const TuneKey key = tune_key(dc, m, n, dtype);
+    TuneEntry ent{-1, 256, 0.0};
+    bool have = false;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_tune.find(key);
+        if (it != g_tune.end()) { ent = it->second; have = true; }
+    }
+    if (path == MUON_PATH_AUTO) {
+        if (!have && env_flag("MUON_AUTOTUNE", true)) {
+            const int B = std::max(1, std::min(bucket_count, 16));
+            int r = autotune_shape(dc, s, m, n, dtype, B, cfg, &ent);
+            if (r) return r;
+            have = true;
+            {
+                std::lock_guard<std::mutex> lk(g_mu);
+                g_tune[key] = ent;
+            }
+            if (const char* p = std::getenv("MUON_TUNE_CACHE")) save_tune_file(p);
+        }
+        if (have) {
+            path = ent.path;
+        } else {
+            // without measurements: Gram needs 9m^2n + 11m^3 products, plain 15m^2n + 5m^3
+            path = (n > m && !cfg.segments.empty()) ? MUON_PATH_GRAM : MUON_PATH_PLAIN;
+        }
+    }
+    const int tile_n = (have && ent.path == path) ? ent.tile_n : 256;
+    *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n);
+    return MUON_OK;
+}
+
+static int save_tune_file(const char* path) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    std::ofstream f(path);
+    if (!f) return fail(MUON_EINVAL, "cannot write tune cache %s", path);
+    f << "muon-tune v1\n";
+    int nwritten = 0;
+    for (auto& kv : g_tune) {
+        std::string dev = std::get<0>(kv.first);
+        std::replace(dev.begin(), dev.end(), '\t', ' ');
+        f << dev << '\t' << std::get<1>(kv.first) << '\t' << std::get<2>(kv.first) << '\t' << std::get<3>(kv.first)
+          << '\t' << std::get<4>(kv.first) << '\t' << std::get<5>(kv.first) << '\t' << kv.second.path << '\t'
+          << kv.second.tile_n << '\t' << kv.second.ms_per_matrix << '\n';
+        ++nwritten;
+    }
+    return nwritten;
+}
+
+static int budget_bytes_chunk(size_t per_matrix, int count) {
+    size_t budget = (size_t)8192 << 20;
+    if (const char* e = std::getenv("MUON_WORKSPACE_MB")) {
+        long v = std::atol(e);
+        if (v > 0) budget = (size_t)v << 20;
+    }
+    size_t c = per_matrix ? budget / per_matrix : (size_t)count;
+    if (c < 1) c = 1;
+    if (c > (size_t)count) c = count;
+    if (c > 65535) c = 65535;
+    return (int)c;
+}
+
+static bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
+
+}  // namespace muon
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+using namespace muon;
+
+extern "C" {
+
+const char* muon_status_str(int status) {
+    switch (status) {
+        case MUON_OK: return "MUON_OK";
+        case MUON_EINVAL: return "MUON_EINVAL: invalid argument";
+        case MUON_EDTYPE: return "MUON_EDTYPE: unsupported dtype";
+        case MUON_ENOMEM: return "MUON_ENOMEM: workspace allocation failed";
+        case MUON_ECUDA: return "MUON_ECUDA: CUDA call failed";
+        case MUON_ENONFINITE: return "MUON_ENONFINITE: non-finite Frobenius norm";
+        case MUON_ETIMEOUT: return "MUON_ETIMEOUT: a bounded device wait gave up";
+        case MUON_ENOTSUP: return "MUON_ENOTSUP: no sm_103a device";
+        default: return "unknown muon status";
+    }
+}
+
+const char* muon_last_error_message(void) { return t_last_error.c_str(); }
+
+int muon_set_ns_config(const float coeffs[3], int steps, const int* segments, int num_segments, int path) {
+    int r = validate_segments(steps, segments, num_segments);
+    if (r) return r;
+    if (path != MUON_PATH_AUTO && path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM)
+        return fail(MUON_EINVAL, "bad path %d", path);
+    if (coeffs && !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
+        return fail(MUON_EINVAL, "non-finite coefficients");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (coeffs) std::memcpy(g_cfg.coeffs, coeffs, sizeof g_cfg.coeffs);
+    g_cfg.steps = steps;
+    g_cfg.segments.assign(segments, segments + num_segments);
+    g_cfg.path = path;
+    return MUON_OK;
+}
+
+int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype, const float coeffs[3],
+                          int steps, const int* segments, int num_segments, void* stream) {
+    if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
+    if (m < 1 || n < 1 || batch < 1) return fail(MUON_EINVAL, "m, n, batch must be >= 1");
+    if (m > (1 << 20) || n > (1 << 20)) return fail(MUON_EINVAL, "matrix side above 2^20");
+    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if (!coeffs || !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
+        return fail(MUON_EINVAL, "coeffs missing or non-finite");
+    int r = validate_segments(steps, segments, num_segments);
+    if (r) return r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    const int trans = m > n;
+    const int om = (int)std::min(m, n), on = (int)std::max(m, n);
+    const int path = num_segments > 0 ? MUON_PATH_GRAM : MUON_PATH_PLAIN;
+    std::vector<int> segs(segments, segments + num_segments);
+    int tile_n = 256;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_tune.find(tune_key(dc, om, on, dtype));
+        if (it != g_tune.end() && it->second.path == path) tile_n = it->second.tile_n;
+    }
+    NsPlan plan = make_plan(coeffs, steps, segs, path, tile_n);
+
+    const size_t es = esize(dtype);
+    const size_t per = chunk_layout(om, on, 1, dtype).total;
+    const int chunk = budget_bytes_chunk(per, (int)std::min<int64_t>(batch, 65535));
+    const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)batch, 256);
+    const ChunkLayout L = chunk_layout(om, on, chunk, dtype);
+    Workspace* w = nullptr;
+    if ((r = ws_get(dc.device, s, table_bytes + L.total, &w))) return r;
+
+    std::vector<MatEntry> h((size_t)batch);
+    for (int64_t b = 0; b < batch; ++b) {
+        char* p = static_cast<char*>(ptr) + (size_t)b * m * n * es;
+        h[b] = MatEntry{p, nullptr, p, trans, 0};
+    }
+    MatEntry* d_table = reinterpret_cast<MatEntry*>(w->base);
+    if ((r = upload_table(*w, h, d_table, s))) return r;
+    char* cbase = w->base + table_bytes;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
+    for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
+        const int B = (int)std::min<int64_t>(chunk, batch - b0);
+        const ChunkLayout LB = chunk_layout(om, on, B, dtype);
+        if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, dtype, false, 0, 0.f, vec_ok)))
+            return r;
+        FinalEpi fin{EPI_OUT, d_table + b0, dtype, 0.f, 0.f, 0.f};
+        if ((r = run_ns(dc, s, cbase, LB, om, on, B, dtype, plan, true, fin))) return r;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_last_path[{om, on, dtype}] = path;
+    }
+    return MUON_OK;
+}
+
+int muon_step(void* const* params, const void* const* grads, void* const* moms, const int64_t* ms,
+              const int64_t* ns, int64_t count, int param_dtype, int mom_dtype, float lr, float beta, float wd,
+              int nesterov, void* stream) {
+    if (count < 0) return fail(MUON_EINVAL, "count < 0");
+    if (count == 0) return MUON_OK;
+    if (!params || !grads || !moms || !ms || !ns) return fail(MUON_EINVAL, "NULL array argument");
+    if (!valid_dtype(param_dtype) || !valid_dtype(mom_dtype))
+        return fail(MUON_EDTYPE, "dtypes %d / %d", param_dtype, mom_dtype);
+    if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(wd))
+        return fail(MUON_EINVAL, "non-finite hyper-parameter");
+    for (int64_t i = 0; i < count; ++i) {
+        if (!params[i] || !grads[i] || !moms[i]) return fail(MUON_EINVAL, "NULL matrix pointer at %lld", (long long)i);
+        if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "matrix %lld has shape %lld x %lld", (long long)i,
+                                                (long long)ms[i], (long long)ns[i]);
+        if (ms[i] > (1 << 20) || ns[i] > (1 << 20)) return fail(MUON_EINVAL, "matrix side above 2^20");
+    }
+    int r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NsConfig cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cfg = g_cfg;
+    }
+
+    // shape buckets in order of first appearance
+    std::vector<std::pair<int, int>> keys;
+    std::map<std::pair<int, int>, std::vector<int64_t>> buckets;
+    for (int64_t i = 0; i < count; ++i) {
+        std::pair<int, int> k{(int)std::min(ms[i], ns[i]), (int)std::max(ms[i], ns[i])};
+        auto it = buckets.find(k);
+        if (it == buckets.end()) {
+            keys.push_back(k);
+            buckets[k] = {i};
+        } else {
+            it->second.push_back(i);
+        }
+    }
+    std::vector<NsPlan> plans(keys.size());
+    std::vector<int> chunks(keys.size());
+    size_t chunk_need = 0;
+    for (size_t k = 0; k < keys.size(); ++k) {
+        const int m = keys[k].first, n = keys[k].second;
+        const int cnt = (int)buckets[keys[k]].size();
+        if ((r = choose_plan(dc, s, m, n, param_dtype, cnt, cfg, &plans[k]))) return r;
+        chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, param_dtype).total, cnt);
+        chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], param_dtype).total);
+    }
+    const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)count, 256);
+    Workspace* w = nullptr;
+    if ((r = ws_get(dc.device, s, table_bytes + chunk_need, &w))) return r;
+
+    std::vector<MatEntry> h;
+    h.reserve((size_t)count);
+    for (auto& k : keys)
+        for (int64_t i : buckets[k])
+            h.push_back(MatEntry{grads[i], moms[i], params[i], ms[i] > ns[i] ? 1 : 0, 0});
+    MatEntry* d_table = reinterpret_cast<MatEntry*>(w->base);
+    if ((r = upload_table(*w, h, d_table, s))) return r;
+    char* cbase = w->base + table_bytes;
+
+    size_t first = 0;
+    for (size_t k = 0; k < keys.size(); ++k) {
+        const int m = keys[k].first, n = keys[k].second;
+        const auto& idx = buckets[keys[k]];
+        bool vec_ok = (m % 8 == 0) && (n % 8 == 0);
+        for (int64_t i : idx)
+            vec_ok = vec_ok && (reinterpret_cast<uintptr_t>(grads[i]) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(moms[i]) % 16 == 0);
+        const float scale = 0.2f * std::sqrt((float)n);
+        for (size_t c0 = 0; c0 < idx.size(); c0 += chunks[k]) {
+            const int B = (int)std::min<size_t>(chunks[k], idx.size() - c0);
+            const ChunkLayout L = chunk_layout(m, n, B, param_dtype);
+            const MatEntry* dm = d_table + first + c0;
+            if ((r = run_prep(dc, s, cbase, L, m, n, B, dm, param_dtype, mom_dtype, param_dtype, true, nesterov,
+                              beta, vec_ok)))
+                return r;
+            FinalEpi fin{EPI_UPDATE, dm, param_dtype, lr, wd, scale};
+            if ((r = run_ns(dc, s, cbase, L, m, n, B, param_dtype, plans[k], true, fin))) return r;
+        }
+        first += idx.size();
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_last_path[{m, n, param_dtype}] = plans[k].path;
+    }
+    return MUON_OK;
+}
+
+int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream) {
+    if (count < 0 || (count > 0 && (!ms || !ns))) return fail(MUON_EINVAL, "bad shape arrays");
+    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    int r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NsConfig cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cfg = g_cfg;
+    }
+    std::map<std::pair<int, int>, int> shapes;
+    for (int64_t i = 0; i < count; ++i) {
+        if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "bad shape at %lld", (long long)i);
+        shapes[{(int)std::min(ms[i], ns[i]), (int)std::max(ms[i], ns[i])}] += 1;
+    }
+    for (auto& kv : shapes) {
+        TuneEntry ent;
+        const int B = std::max(1, std::min(kv.second, 16));
+        if ((r = autotune_shape(dc, s, kv.first.first, kv.first.second, dtype, B, cfg, &ent))) return r;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_tune[tune_key(dc, kv.first.first, kv.first.second, dtype)] = ent;
+    }
+    if (const char* p = std::getenv("MUON_TUNE_CACHE")) save_tune_file(p);
+    return MUON_OK;
+}
+
+int muon_tune_save(const char* path) {
+    if (!path) return fail(MUON_EINVAL, "path is NULL");
+    int r = save_tune_file(path);
+    return r < 0 ? r : MUON_OK;
+}
+
+int muon_tune_load(const char* path) {
+    if (!path) return fail(MUON_EINVAL, "path is NULL");
+    std::ifstream f(path);
+    if (!f) return 0;
+    std::string line;
+    if (!std::getline(f, line) || line != "muon-tune v1") return 0;
+    DevCtx dc;
+    int r = get_dev(dc);
+    if (r) return r;
+    const int cv = cudart_version();
+    int loaded = 0;
+    while (std::getline(f, line)) {
+        std::istringstream ss(line);
+        std::string dev, tok;
+        std::vector<std::string> cols;
+        while (std::getline(ss, tok, '\t')) cols.push_back(tok);
+        if (cols.size() != 9) continue;
+        try {
+            const int sms = std::stoi(cols[1]), cuv = std::stoi(cols[2]);
+            const int64_t m = std::stoll(cols[3]), n = std::stoll(cols[4]);
+            const int dt = std::stoi(cols[5]), path = std::stoi(cols[6]), tile = std::stoi(cols[7]);
+            const double ms = std::stod(cols[8]);
+            if (cols[0] != dc.name || sms != dc.sms || cuv != cv) continue;          // stale: other device/runtime
+            if (m < 1 || n < m || !valid_dtype(dt)) continue;
+            if (path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM) continue;
+            if (tile != 128 && tile != 256) continue;
+            std::lock_guard<std::mutex> lk(g_mu);
+            g_tune[TuneKey{dc.name, sms, cuv, m, n, dt}] = TuneEntry{path, tile, ms};
+            ++loaded;
+        } catch (...) {
+            continue;   // corrupt line
+        }
+    }
+    return loaded;
+}
+
+int muon_last_path(int64_t m, int64_t n, int dtype, int* path_out) {
+    if (!path_out) return fail(MUON_EINVAL, "path_out is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_last_path.find({std::min(m, n), std::max(m, n), dtype});
+    if (it == g_last_path.end()) return MUON_EINVAL;
+    *path_out = it->second;
+    return MUON_OK;
+}
+
+int muon_sync_status(void* stream) {
+    DevCtx dc;
+    int r = get_dev(dc);
+    if (r) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MUON_CUDA(cudaStreamSynchronize(s));
+    int v = 0;
+    MUON_CUDA(cudaMemcpy(&v, dc.status, sizeof v, cudaMemcpyDeviceToHost));
+    if (v) MUON_CUDA(cudaMemset(dc.status, 0, sizeof v));
+    if (v & STATUS_TIMEOUT) return MUON_ETIMEOUT;
+    if (v & STATUS_NONFINITE) return MUON_ENONFINITE;
+    return MUON_OK;
+}
+
+int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_segments, double* nominal,
+                  double* algorithmic) {
+    if (m < 1 || n < 1 || !nominal || !algorithmic) return fail(MUON_EINVAL, "bad arguments");
+    const double M = (double)std::min(m, n), N = (double)std::max(m, n);
+    double nom = 0, alg = 0;
+    auto prod = [&](double a, double b, double k, bool sym) {
+        nom += 2 * a * b * k;
+        alg += sym ? a * b * k : 2 * a * b * k;
+    };
+    if (path == MUON_PATH_PLAIN) {
+        int steps = 0;
+        if (num_segments > 0) {
+            if (!segments) return fail(MUON_EINVAL, "segments NULL");
+            for (int i = 0; i < num_segments; ++i) steps += segments[i];
+        } else {
+            steps = 5;
+        }
+        for (int k = 0; k < steps; ++k) {
+            prod(M, M, N, true);    // A = X X^T
+            prod(M, M, M, true);    // A^2
+            prod(M, N, M, false);   // B X
+        }
+    } else if (path == MUON_PATH_GRAM) {
+        if (num_segments < 1 || !segments) return fail(MUON_EINVAL, "Gram path needs segments");
+        for (int si = 0; si < num_segments; ++si) {
+            const int L = segments[si];
+            if (L < 1) return fail(MUON_EINVAL, "segment < 1");
+            prod(M, M, N, true);    // G = X X^T
+            for (int j = 1; j <= L; ++j) {
+                prod(M, M, M, true);                 // G^2
+                if (j > 1) prod(M, M, M, true);      // P Q
+                if (j < L) {
+                    prod(M, M, M, true);             // P G
+                    prod(M, M, M, true);             // (P G) P
+                }
+            }
+            prod(M, N, M, false);   // Q X
+        }
+    } else {
+        return fail(MUON_EINVAL, "path must be plain or gram");
+    }
+    *nominal = nom;
+    *algorithmic = alg;
+    return MUON_OK;
+}
+
+int64_t muon_launch_count(void) { return g_launches.load(); }
+
+int muon_set_kernel_timing(int enable) {
+    g_timing.store(enable ? 1 : 0);
+    return MUON_OK;
+}
+
+int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms, double* work, int max_classes) {
+    if (max_classes < 0) return fail(MUON_EINVAL, "max_classes < 0");
+    std::vector<TimedLaunch> recs;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        recs.swap(g_timed);
+    }
+    double ms_acc[KC_COUNT] = {0};
+    double work_acc[KC_COUNT] = {0};
+    int64_t cnt[KC_COUNT] = {0};
+    for (auto& t : recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(t.b) == cudaSuccess && cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+            ms_acc[t.kclass] += ms;
+            work_acc[t.kclass] += t.work;
+            cnt[t.kclass] += 1;
+        }
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (auto& t : recs) {
+            g_event_pool.push_back(t.a);
+            g_event_pool.push_back(t.b);
+        }
+    }
+    const int n = std::min<int>(max_classes, KC_COUNT);
+    for (int k = 0; k < n; ++k) {
+        if (names) {
+            std::strncpy(names + 32 * k, kclass_name(k), 31);
+            names[32 * k + 31] = 0;
+        }
+        if (launches) launches[k] = cnt[k];
+        if (total_ms) total_ms[k] = ms_acc[k];
+        if (work) work[k] = work_acc[k];
+    }
+    return n;
+}
+
+int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t batch,
+                    int dtype, int b_kmajor, int symmetric, int poly, float alpha, float pa, float pb, float pc,
+                    int tile_n, void* stream) {
+    if (!A || !B || !C) return fail(MUON_EINVAL, "NULL operand");
+    if (M < 1 || N < 1 || K < 1 || batch < 1) return fail(MUON_EINVAL, "bad sizes");
+    if (M > (1 << 20) || N > (1 << 20) || K > (1 << 20)) return fail(MUON_EINVAL, "size above 2^20");
+    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if ((symmetric || poly) && M != N) return fail(MUON_EINVAL, "symmetric product needs M == N");
+    if (poly && (!symmetric || K != M)) return fail(MUON_EINVAL, "poly needs a symmetric square product");
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256) return fail(MUON_EINVAL, "tile_n must be 0, 128 or 256");
+    if (dtype == MUON_BF16) {
+        const int64_t ldb = b_kmajor ? K : N;
+        if ((K % 8) || (ldb % 8) || (reinterpret_cast<uintptr_t>(A) % 16) || (reinterpret_cast<uintptr_t>(B) % 16))
+            return fail(MUON_EINVAL, "bf16 operands need 16-byte aligned rows");
+    }
+    int r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    GemmArgs g = gemm_base(dtype, dc.status);
+    g.A = A; g.lda = K; g.strideA = M * K;
+    g.B = B; g.b_kmajor = b_kmajor ? 1 : 0;
+    g.ldb = b_kmajor ? K : N; g.strideB = N * K;
+    g.M = (int)M; g.N = (int)N; g.K = (int)K; g.batch = (int)batch;
+    g.symmetric = symmetric ? 1 : 0;
+    g.alpha = alpha;
+    g.C = C; g.ldc = N; g.strideC = M * N;
+    g.tile_n = tile_n ? tile_n : 256;
+    if (poly) {
+        g.epi = EPI_POLY;
+        g.Gin = A; g.ldg = K; g.strideG = M * K;
+        g.pa = pa; g.pb = pb; g.pc = pc;
+    }
+    return run_gemm(dc, reinterpret_cast<cudaStream_t>(stream), g, KC_OTHER);
+}
+
+}  // extern "C"

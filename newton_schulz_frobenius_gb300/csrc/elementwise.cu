@@ -1,0 +1,215 @@
+// Elementwise kernels of the Muon update: momentum (+Nesterov), orientation
+// into the workspace, Frobenius partial sums, and the norm finalisation.
+//
+// Momentum smooths the gradient before Newton-Schulz ("MuonX" page, section 2);
+// the Frobenius normalisation places every singular value at or below 1 before
+// the iteration.  The scale 1/(||U||_F + eps) is not applied here: it is folded
+// into the first XX^T (as its square) and the first Q X of the NS path, so U is
+// read and written exactly once.
+//
+// Layout: one CTA handles a 64 x 64 tile of the ORIENTED matrix (m <= n).  For
+// a tall caller matrix (trans = 1) the CTA reads the matching transposed tile of
+// the caller's rows (coalesced), writes momentum back in the caller's layout,
+// and transposes through shared memory so the workspace write is coalesced too.
+#include "muon_internal.cuh"
+#include "epilogue.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int PT = 64;          // tile edge
+constexpr int PTHREADS = 256;   // 64 rows x 4 segments of 16 elements
+
+__device__ __forceinline__ void load16(const void* p, int dtype, int64_t off, int valid, bool vec,
+                                       float (&v)[16]) {
+    if (vec && valid == 16) {
+        if (dtype == MUON_BF16) {
+            const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p) + off);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 u = __ldg(q + h);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+                    float2 f = __bfloat1622float2(b2);
+                    v[h * 8 + 2 * k] = f.x;
+                    v[h * 8 + 2 * k + 1] = f.y;
+                }
+            }
+        } else {
+            const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + off);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float4 f = __ldg(q + h);
+                v[4 * h] = f.x; v[4 * h + 1] = f.y; v[4 * h + 2] = f.z; v[4 * h + 3] = f.w;
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = (j < valid) ? ld_elem(p, off + j, dtype) : 0.f;
+}
+
+__device__ __forceinline__ void store16(void* p, int dtype, int64_t off, int valid, bool vec,
+                                        const float (&v)[16]) {
+    if (vec && valid == 16) {
+        store_row_run<16>(p, off, v, dtype);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (j < valid) st_elem(p, off + j, v[j], dtype);
+}
+
+__global__ void __launch_bounds__(PTHREADS)
+prep_kernel(const __grid_constant__ PrepArgs a) {
+    __shared__ float tile[PT][PT + 1];
+    __shared__ float red[PTHREADS / 32];
+
+    const int b = blockIdx.y;
+    const int tiles_c = (a.n + PT - 1) / PT;
+    const int tr = blockIdx.x / tiles_c;
+    const int tc = blockIdx.x % tiles_c;
+    const MatEntry e = a.mats[b];
+    const int lr = threadIdx.x >> 2;          // row within the tile
+    const int seg = (threadIdx.x & 3) * 16;   // first of 16 columns
+    const bool vec = a.vec_ok != 0;
+
+    // Raw (caller) coordinates of this thread's 16 elements.
+    int raw_r, raw_c0, raw_rows, raw_cols;
+    if (!e.trans) {
+        raw_rows = a.m; raw_cols = a.n;
+        raw_r = tr * PT + lr; raw_c0 = tc * PT + seg;
+    } else {
+        raw_rows = a.n; raw_cols = a.m;
+        raw_r = tc * PT + lr; raw_c0 = tr * PT + seg;
+    }
+    int valid = 0;
+    if (raw_r < raw_rows) valid = max(0, min(16, raw_cols - raw_c0));
+    const int64_t off = (int64_t)raw_r * raw_cols + raw_c0;
+
+    float u[16];
+    float ss = 0.f;
+    if (valid > 0) {
+        float g[16];
+        load16(e.grad, a.in_dtype, off, valid, vec, g);
+        if (a.with_momentum) {
+            float mo[16];
+            load16(e.mom, a.mom_dtype, off, valid, vec, mo);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float mn = fmaf(a.beta, mo[j], g[j]);          // M' = beta M + G
+                mo[j] = mn;
+                u[j] = a.nesterov ? fmaf(a.beta, mn, g[j]) : mn;     // U = G + beta M'
+            }
+            // momentum is stored in its own dtype; U continues from the fp32 M'
+            store16(e.mom, a.mom_dtype, off, valid, vec, mo);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = g[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < valid) ss = fmaf(u[j], u[j], ss);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) u[j] = 0.f;
+    }
+
+    const int64_t xb = (int64_t)b * a.strideX;
+    const bool xvec = (a.ldx % 8) == 0;
+    if (!e.trans) {
+        if (valid > 0) store16(a.X, a.x_dtype, xb + (int64_t)raw_r * a.ldx + raw_c0, valid, xvec, u);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tile[lr][seg + j] = u[j];
+        __syncthreads();
+        // oriented row = tr*64 + lr2, columns tc*64 + seg2 .. +16  <- tile[col][row]
+        const int orow = tr * PT + lr;
+        const int ocol0 = tc * PT + seg;
+        int ovalid = 0;
+        if (orow < a.m) ovalid = max(0, min(16, a.n - ocol0));
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = tile[seg + j][lr];
+        if (ovalid > 0) store16(a.X, a.x_dtype, xb + (int64_t)orow * a.ldx + ocol0, ovalid, xvec, x);
+    }
+
+    // Block sum of squares -> one partial per tile.
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < PTHREADS / 32; ++w) t += red[w];
+        a.partials[(int64_t)b * a.nparts + blockIdx.x] = t;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+norm_finalize_kernel(const float* __restrict__ partials, int nparts, float eps,
+                     float* __restrict__ inv, int* status) {
+    __shared__ double red[8];
+    const int b = blockIdx.x;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < nparts; i += 256) s += (double)partials[(int64_t)b * nparts + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 8; ++w) t += red[w];
+        if (!isfinite(t)) atomicOr(status, STATUS_NONFINITE);
+        inv[b] = (float)(1.0 / (sqrt(t) + (double)eps));
+    }
+}
+
+__device__ __forceinline__ uint32_t hash32(uint32_t x) {
+    x ^= x >> 16; x *= 0x7feb352du;
+    x ^= x >> 15; x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+
+__global__ void fill_synthetic_kernel(void* X, int64_t count, int dtype, float scale, uint32_t seed) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t h = hash32((uint32_t)i * 2654435761u ^ seed ^ (uint32_t)(i >> 32));
+        float v = ((float)(h >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
+        st_elem(X, i, v, dtype);
+    }
+}
+
+}  // namespace
+
+int prep_num_parts(int m, int n) {
+    return ((m + PT - 1) / PT) * ((n + PT - 1) / PT);
+}
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+    dim3 grid(prep_num_parts(a.m, a.n), a.batch);
+    prep_kernel<<<grid, PTHREADS, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
+                                 float* inv, int* status, cudaStream_t s) {
+    norm_finalize_kernel<<<batch, 256, 0, s>>>(partials, nparts, eps, inv, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale, uint32_t seed,
+                                  cudaStream_t s) {
+    int64_t nb = (count + 255) / 256;
+    int blocks = (int)(nb < 4096 ? nb : 4096);
+    if (blocks < 1) blocks = 1;
+    fill_synthetic_kernel<<<blocks, 256, 0, s>>>(X, count, dtype, scale, seed);
+    return cudaGetLastError();
+}
+
+}  // namespace muon

@@ -1,0 +1,501 @@
+// bf16 products of the Newton-Schulz path on the 5th-generation tensor cores.
+//
+// Every product of the Muon update is a dense contraction: the Gram matrix
+// XX^T, the square products of polynomials in G (G^2, PG, (PG)P, PQ), and the
+// long apply QX ("MuonX" page, section 3.2 counts them: 6 long and 11 square
+// for 2+2+1 Gram NS).  XX^T and the square products have symmetric results;
+// the "DMuon" summary (section 2.2) computes only one triangle of them, and so
+// does this kernel: symmetric launches enumerate lower-triangle tiles only and
+// mirror on store.  Because every square operand is symmetric, both operands of
+// every product except QX can be read K-major straight from row-major storage;
+// QX reads X as an MN-major operand.
+//
+// Structure (one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: 3-D tensor maps (k, row, batch), 128-byte swizzle,
+//               STAGES-deep ring of (A, B) tiles guarded by full/empty mbarriers
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//               (M = 128, N = BN, K = 16 per instruction, fp32 accumulator)
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, fused epilogue from
+//               epilogue.cuh, global stores
+// The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
+// of tile t overlaps the main loop of tile t+1.  Every mbarrier wait is bounded:
+// after WAIT_LIMIT_NS it sets an abort flag and the status word, waits (again
+// bounded) for its own copies and products in flight, frees TMEM and returns.
+#include "muon_internal.cuh"
+#include "epilogue.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace muon {
+
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;            // bf16 elements = 128 bytes: one swizzle row
+constexpr int NTHREADS = 192;
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+// Bounded wait on phase `parity`.  Gives up when another role has aborted or
+// after WAIT_LIMIT_NS, in which case it raises the abort flag and the status.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicOr(status, STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) return;
+    }
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i gets its lane's 32 values.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    // The wait names every destination register so no use is scheduled before it.
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+          "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+          "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+          "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+        :
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: start, leading/stride byte offsets, the
+// fixed descriptor version of this MMA generation (bit 46) and 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
+// K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct TileSched {
+    int tiles_m, tiles_n, per_batch, total, sym;
+
+    __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn) const {
+        b = t / per_batch;
+        const int l = t - b * per_batch;
+        if (sym) {
+            int r = (int)((sqrtf(8.0f * (float)l + 1.0f) - 1.0f) * 0.5f);
+            while (r * (r + 1) / 2 > l) --r;
+            while ((r + 1) * (r + 2) / 2 <= l) ++r;
+            tm = r;
+            tn = l - r * (r + 1) / 2;
+        } else {
+            tm = l % tiles_m;
+            tn = l / tiles_m;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int BN, bool B_KMAJOR>
+__global__ void __launch_bounds__(NTHREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ GemmArgs args, const TileSched sched) {
+    using C = Cfg<BN>;
+    constexpr int S = C::STAGES;
+    constexpr uint32_t IDESC = idesc_bf16(BM, BN, !B_KMAJOR);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * S;
+    const uint32_t accf0 = empty0 + 8 * S;
+    const uint32_t acce0 = accf0 + 16;
+    const uint32_t drain_bar = acce0 + 16;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accf0, 1);
+        mbar_init(accf0 + 8, 1);
+        mbar_init(acce0, 4);
+        mbar_init(acce0 + 8, 4);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = (args.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int issued[S];
+#pragma unroll
+            for (int s = 0; s < S; ++s) issued[s] = -1;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+                int b, tm, tn;
+                sched.decode(t, b, tm, tn);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, C::STAGE_BYTES);
+                    tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * BK, tm * BM, b);
+                    if (B_KMAJOR) {
+                        tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * BK, tn * BN, b);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q)
+                            tma_load_3d(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmB, fb,
+                                        tn * BN + q * 64, kb * BK, b);
+                    }
+                    issued[stage] = (int)phase;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // wait (bounded) for this CTA's copies still in flight
+#pragma unroll
+                for (int s = 0; s < S; ++s)
+                    if (issued[s] >= 0) wait_drain(full0 + 8 * s, (uint32_t)issued[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t aphase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+                if (!wait_bounded(acce0 + 8 * acc, aphase ^ 1u, abort_flag, args.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sdesc(a_base + kk * 32, 16, 1024);
+                        const uint64_t bd = B_KMAJOR ? sdesc(b_base + kk * 32, 16, 1024)
+                                                     : sdesc(b_base + kk * 2048, BK * 128, 1024);
+                        tc_mma_bf16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty0 + 8 * stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(accf0 + 8 * acc);
+                acc ^= 1;
+                if (acc == 0) aphase ^= 1u;
+            }
+            if (!ok) {
+                // wait (bounded) for the products this thread issued
+                tc_commit(drain_bar);
+                wait_drain(drain_bar, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t aphase = 0;
+        for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+            int b, tm, tn;
+            sched.decode(t, b, tm, tn);
+            // every lane observes the barrier itself; the warp proceeds only together
+            const bool ok = wait_bounded(accf0 + 8 * acc, aphase, abort_flag, args.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int row = tm * BM + q * 32 + lane;
+            const int warp_row_max = tm * BM + q * 32 + 31;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int col0 = tn * BN + ch * 32;
+                if (col0 >= args.N) break;
+                if (args.symmetric && col0 > warp_row_max) continue;
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
+                epi_row_chunk<32>(args, b, row, col0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map over `batch` matrices of `rows` x `inner` (row pitch ld,
+// matrix pitch stride, in elements), box box_inner x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t batch, uint64_t ld,
+              uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (batch <= 1) stride = ld * rows;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {ld * 2, stride * 2};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool B_KMAJOR>
+cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
+    using C = Cfg<BN>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, B_KMAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda, (uint64_t)a.strideA,
+                  BK, BM))
+        return cudaErrorInvalidValue;
+    bool okB = B_KMAJOR ? make_map(&mB, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch, (uint64_t)a.ldb,
+                                   (uint64_t)a.strideB, BK, BN)
+                        : make_map(&mB, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch, (uint64_t)a.ldb,
+                                   (uint64_t)a.strideB, 64, BK);
+    if (!okB) return cudaErrorInvalidValue;
+
+    TileSched sc;
+    sc.tiles_m = (a.M + BM - 1) / BM;
+    sc.tiles_n = (a.N + BN - 1) / BN;
+    sc.sym = a.symmetric;
+    sc.per_batch = a.symmetric ? sc.tiles_m * (sc.tiles_m + 1) / 2 : sc.tiles_m * sc.tiles_n;
+    sc.total = sc.per_batch * a.batch;
+    const int grid = sc.total < num_sms ? sc.total : num_sms;
+    gemm_tc_kernel<BN, B_KMAJOR><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mA, mB, a, sc);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
+    if (a.dtype != MUON_BF16) return cudaErrorInvalidValue;
+    if (a.M < 1 || a.N < 1 || a.K < 1 || a.batch < 1) return cudaErrorInvalidValue;
+    if (a.symmetric && a.M != a.N) return cudaErrorInvalidValue;
+    // TMA: 16-byte aligned bases and pitches
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    if (!al16(a.A) || !al16(a.B) || (a.lda % 8) || (a.ldb % 8) || (a.strideA % 8) || (a.strideB % 8))
+        return cudaErrorInvalidValue;
+    if ((int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + 127) / 128) > (int64_t)1 << 30)
+        return cudaErrorInvalidValue;
+    const int bn = a.symmetric ? 128 : (a.tile_n == 128 ? 128 : 256);
+    if (bn == 128) {
+        return a.b_kmajor ? tc::launch_impl<128, true>(a, num_sms, s) : tc::launch_impl<128, false>(a, num_sms, s);
+    }
+    return a.b_kmajor ? tc::launch_impl<256, true>(a, num_sms, s) : tc::launch_impl<256, false>(a, num_sms, s);
+}
+
+}  // namespace muon

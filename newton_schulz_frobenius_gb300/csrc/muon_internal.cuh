@@ -1,0 +1,102 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/muon.h"
+
+namespace muon {
+
+// Bits of the per-device status word (read by muon_sync_status).
+enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
+
+// A bounded wait gives up after this long (nanoseconds of %globaltimer); no
+// legitimate wait inside one of the library's kernels comes near it.
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+// One matrix of a pointer-table launch (momentum kernel, fused update, output).
+// Oriented shape is m x n (m <= n); trans = 1 means the caller's matrix is
+// n x m and the oriented matrix is its transpose.
+struct MatEntry {
+    const void* grad;   // caller gradient (param dtype) or NS input
+    void* mom;          // caller momentum (mom dtype), may be null
+    void* w;            // caller weights (update) or NS output
+    int trans;
+    int pad;
+};
+
+enum EpiKind : int {
+    EPI_STORE = 0,   // C = alpha * acc
+    EPI_POLY = 1,    // C = pa*I + pb*Gin + pc*alpha*acc   (symmetric only)
+    EPI_UPDATE = 2,  // W = W (1 - lr wd) - lr * scale * alpha * acc   (via mats)
+    EPI_OUT = 3      // O = alpha * acc written to the caller's buffer (via mats)
+};
+
+// One (batched) product C[b] = epilogue(A[b] * op(B[b])).
+// A is M x K row-major (K contiguous).  b_kmajor: B stored N x K (op = ^T);
+// otherwise B stored K x N (op = identity).  dtype is the storage type of
+// A, B, C and Gin (MUON_BF16 or MUON_F32).
+struct GemmArgs {
+    const void* A; int64_t lda; int64_t strideA;
+    const void* B; int64_t ldb; int64_t strideB;
+    int b_kmajor;
+    int M, N, K, batch;
+    int symmetric;          // M == N, lower-triangle tiles only, mirrored store
+    int dtype;
+    int epi;
+    float alpha;            // scalar factor
+    const float* alpha_vec; // optional per-batch factor (device), may be null
+    int alpha_sq;           // use alpha_vec[b]^2
+    void* C; int64_t ldc; int64_t strideC;
+    const void* Gin; int64_t ldg; int64_t strideG;
+    float pa, pb, pc;
+    const MatEntry* mats;   // device table indexed by b (EPI_UPDATE / EPI_OUT)
+    int out_dtype;          // storage type of the caller's W / O
+    float lr, wd, scale;
+    int tile_n;             // tensor-core tile N extent (128 or 256)
+    int* status;            // device status word
+};
+
+// Launchers (return the CUDA error of the launch).
+cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
+
+// Momentum (+Nesterov) or plain copy, orientation and Frobenius partial sums.
+struct PrepArgs {
+    const MatEntry* mats;   // device table, one entry per batch index
+    int m, n, batch;        // oriented shape
+    int in_dtype;           // dtype of grad (or NS input)
+    int mom_dtype;
+    int x_dtype;            // workspace X dtype
+    int with_momentum;      // 0: U = input (NS only)
+    int nesterov;
+    float beta;
+    void* X; int64_t ldx; int64_t strideX;
+    float* partials;        // [batch][nparts]
+    int nparts;
+    int vec_ok;             // caller rows are 16-byte aligned for vector access
+};
+int prep_num_parts(int m, int n);
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+
+// inv[b] = 1 / (sqrt(sum(partials[b][:])) + eps); flags a non-finite sum.
+cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
+                                 float* inv, int* status, cudaStream_t s);
+
+// Fills `count` elements of a workspace buffer with bounded pseudo-random values
+// (autotune input only; never touches caller data).
+cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale,
+                                  uint32_t seed, cudaStream_t s);
+
+// Kernel-class bookkeeping for launch counting and optional event timing.
+enum KernelClass : int {
+    KC_PREP = 0, KC_NORM = 1, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
+    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_COUNT = 8
+};
+void note_launch_begin(int kclass, cudaStream_t s);
+void note_launch_end(int kclass, double work, cudaStream_t s);
+
+}  // namespace muon

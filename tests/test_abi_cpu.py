@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and its host-only logic (validation, FLOP accounting, status
+strings, tune-cache parsing) behaves as documented.  No call here reaches a
+CUDA device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import muon_oracle as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mg():
+    from newton_schulz_frobenius_gb300 import _build
+    _build.build()
+    import newton_schulz_frobenius_gb300 as pkg
+    pkg.lib()
+    return pkg
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declarations_match_binding(mg):
+    assert _declared() == sorted(mg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(mg):
+    L = mg.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_no_fallback_when_library_missing(monkeypatch):
+    import newton_schulz_frobenius_gb300 as pkg
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg, "LIB_PATH", "/nonexistent/libmuon_gb300.so")
+    with pytest.raises(ImportError):
+        pkg.lib()
+
+
+def test_status_strings(mg):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert mg.status_str(code).startswith("MUON_")
+    assert "unknown" in mg.status_str(12345)
+
+
+@pytest.mark.parametrize("m,n", [(2560, 9728), (128, 512), (256, 256), (4096, 14336), (8192, 2048), (37, 200)])
+def test_flop_accounting_matches_oracle_product_log(mg, m, n):
+    om, on = min(m, n), max(m, n)
+    for path, code, segs in (("plain", mg.MUON_PATH_PLAIN, ()), ("gram", mg.MUON_PATH_GRAM, (2, 2, 1)),
+                             ("gram", mg.MUON_PATH_GRAM, (2, 3)), ("gram", mg.MUON_PATH_GRAM, (1, 1, 1, 1, 1))):
+        nom, alg = mg.muon_ns_flops(m, n, code, segs)
+        log = orc.ns_product_log(om, on, path, segments=segs if segs else (2, 2, 1))
+        assert nom == log.nominal_flops()
+        assert alg == log.algorithmic_flops()
+
+
+def test_flop_accounting_pages_numbers(mg):
+    nom_p, _ = mg.muon_ns_flops(2560, 9728, mg.MUON_PATH_PLAIN, ())
+    nom_g, _ = mg.muon_ns_flops(2560, 9728, mg.MUON_PATH_GRAM, (2, 2, 1))
+    assert round(nom_p / 1e12, 3) == 1.443 and round(nom_g / 1e12, 3) == 1.134
+
+
+def test_flops_rejects_bad_arguments(mg):
+    L = mg.lib()
+    d = ctypes.c_double()
+    assert L.muon_ns_flops(0, 5, 1, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
+    assert L.muon_ns_flops(5, 5, 2, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
+    assert L.muon_ns_flops(5, 5, 7, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
+
+
+def test_set_ns_config_validation(mg):
+    L = mg.lib()
+    c = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    bad = (ctypes.c_int * 3)(2, 2, 2)
+    assert L.muon_set_ns_config(c, 5, bad, 3, 0) == mg.MUON_EINVAL        # sums to 6
+    zero = (ctypes.c_int * 2)(5, 0)
+    assert L.muon_set_ns_config(c, 5, zero, 2, 0) == mg.MUON_EINVAL       # empty segment
+    assert L.muon_set_ns_config(c, 0, None, 0, 0) == mg.MUON_EINVAL       # no steps
+    assert L.muon_set_ns_config(c, 5, None, 0, 9) == mg.MUON_EINVAL       # bad path
+    nanc = (ctypes.c_float * 3)(float("nan"), 0, 0)
+    assert L.muon_set_ns_config(nanc, 5, None, 0, 0) == mg.MUON_EINVAL
+    good = (ctypes.c_int * 3)(2, 2, 1)
+    assert L.muon_set_ns_config(c, 5, good, 3, 0) == mg.MUON_OK
+    assert "segments" in mg.last_error_message() or mg.last_error_message() != ""
+
+
+def test_step_and_orthogonalize_validation_before_any_device_use(mg):
+    L = mg.lib()
+    vp = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    assert L.muon_step(None, None, None, None, None, 0, 1, 1, 0.02, 0.95, 0.1, 0, None) == mg.MUON_OK
+    assert L.muon_step(None, None, None, None, None, -1, 1, 1, 0.02, 0.95, 0.1, 0, None) == mg.MUON_EINVAL
+    ptrs = (vp * 1)(None)
+    ms = (i64 * 1)(4)
+    ns = (i64 * 1)(8)
+    assert L.muon_step(ptrs, ptrs, ptrs, ms, ns, 1, 1, 1, 0.02, 0.95, 0.1, 0, None) == mg.MUON_EINVAL
+    assert L.muon_step(ptrs, ptrs, ptrs, ms, ns, 1, 7, 1, 0.02, 0.95, 0.1, 0, None) == mg.MUON_EDTYPE
+    fake = (vp * 1)(0x1000)
+    zero = (i64 * 1)(0)
+    assert L.muon_step(fake, fake, fake, zero, ns, 1, 1, 1, 0.02, 0.95, 0.1, 0, None) == mg.MUON_EINVAL
+    assert L.muon_step(fake, fake, fake, ms, ns, 1, 1, 1, float("inf"), 0.95, 0.1, 0, None) == mg.MUON_EINVAL
+    c = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    segs = (ctypes.c_int * 3)(2, 2, 1)
+    assert L.muon_ns_orthogonalize(None, 4, 8, 1, 1, c, 5, segs, 3, None) == mg.MUON_EINVAL
+    assert L.muon_ns_orthogonalize(0x1000, 0, 8, 1, 1, c, 5, segs, 3, None) == mg.MUON_EINVAL
+    assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 5, c, 5, segs, 3, None) == mg.MUON_EDTYPE
+    assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 1, c, 4, segs, 3, None) == mg.MUON_EINVAL
+    assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 1, None, 5, segs, 3, None) == mg.MUON_EINVAL
+
+
+def test_debug_gemm_validation(mg):
+    L = mg.lib()
+    assert L.muon_debug_gemm(None, None, None, 4, 4, 4, 1, 1, 1, 0, 0, 1.0, 0, 0, 0, 0, None) == mg.MUON_EINVAL
+    p = 0x1000
+    assert L.muon_debug_gemm(p, p, p, 4, 8, 4, 1, 1, 1, 1, 0, 1.0, 0, 0, 0, 0, None) == mg.MUON_EINVAL
+    assert L.muon_debug_gemm(p, p, p, 8, 8, 8, 1, 1, 1, 1, 0, 1.0, 0, 0, 0, 100, None) == mg.MUON_EINVAL
+    assert L.muon_debug_gemm(p, p, p, 8, 8, 12, 1, 1, 1, 0, 0, 1.0, 0, 0, 0, 0, None) == mg.MUON_EINVAL
+
+
+def test_last_path_unknown_shape(mg):
+    assert mg.muon_last_path(3, 7, mg.MUON_BF16) is None
+
+
+def test_tune_load_missing_or_foreign_file(mg, tmp_path):
+    assert mg.muon_tune_load(str(tmp_path / "missing.tsv")) == 0
+    p = tmp_path / "junk.tsv"
+    p.write_text("not a tune cache\n1\t2\t3\n")
+    assert mg.muon_tune_load(str(p)) == 0
+
+
+def test_kernel_timing_read_empty(mg):
+    mg.muon_set_kernel_timing(False)
+    assert mg.muon_kernel_timing_read() == {}
+    assert mg.muon_launch_count() >= 0

@@ -1,0 +1,109 @@
+"""Kernel-level tests of the product kernels through muon_debug_gemm, against a
+plain PyTorch reference of the same product (fp64 on the GPU from the same
+stored operands).  bf16 runs on the tcgen05 tensor-core kernel, fp32 on the
+FFMA kernel.  Shapes span several tiles and ragged tails."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as pkg
+    return pkg
+
+
+def _rand(shape, dtype, seed, scale=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32) * scale).to(dtype)
+
+
+def _check(C, ref, dtype):
+    C64 = C.double()
+    err = (C64 - ref).norm() / ref.norm()
+    tol = 1e-2 if dtype == torch.bfloat16 else 1e-5
+    assert err.item() < tol, err.item()
+    # elementwise: within a few output ulps of the reference scale
+    scale = ref.abs().max().item()
+    atol = (2.0 ** -6 if dtype == torch.bfloat16 else 1e-5) * scale
+    assert (C64 - ref).abs().max().item() <= atol
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,N,K,batch,tile", [
+    (128, 128, 64, 1, 0), (256, 512, 320, 2, 256), (256, 512, 320, 2, 128),
+    (200, 264, 136, 3, 0), (384, 1000, 72, 1, 128), (1, 8, 8, 1, 0)])
+def test_product_k_major(mg, dtype, M, N, K, batch, tile):
+    A = _rand((batch, M, K), dtype, 1)
+    B = _rand((batch, N, K), dtype, 2)
+    C = torch.zeros((batch, M, N), dtype=dtype, device="cuda")
+    mg.muon_debug_gemm(A, B, C, b_kmajor=True, alpha=0.5, tile_n=tile)
+    torch.cuda.synchronize()
+    assert mg.muon_sync_status() == mg.MUON_OK
+    ref = 0.5 * torch.matmul(A.double(), B.double().transpose(1, 2))
+    _check(C, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,N,K,batch,tile", [
+    (128, 256, 128, 1, 256), (200, 304, 136, 2, 256), (200, 304, 136, 2, 128),
+    (512, 1000, 512, 1, 0), (64, 64, 64, 1, 128)])
+def test_product_mn_major(mg, dtype, M, N, K, batch, tile):
+    A = _rand((batch, M, K), dtype, 3)
+    B = _rand((batch, K, N), dtype, 4)
+    C = torch.zeros((batch, M, N), dtype=dtype, device="cuda")
+    mg.muon_debug_gemm(A, B, C, b_kmajor=False, tile_n=tile)
+    torch.cuda.synchronize()
+    ref = torch.matmul(A.double(), B.double())
+    _check(C, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("m,k,batch", [(128, 64, 1), (260, 1000, 2), (512, 384, 1), (37, 200, 3)])
+def test_symmetric_gram(mg, dtype, m, k, batch):
+    if dtype == torch.bfloat16 and k % 8:
+        pytest.skip("tensor-map rows need 16-byte pitch")
+    X = _rand((batch, m, k), dtype, 5)
+    C = torch.full((batch, m, m), float("nan"), dtype=dtype, device="cuda")
+    mg.muon_debug_gemm(X, X, C, b_kmajor=True, symmetric=True, alpha=1.0 / k)
+    torch.cuda.synchronize()
+    assert torch.equal(C, C.transpose(1, 2))          # mirrored, every element written
+    ref = torch.matmul(X.double(), X.double().transpose(1, 2)) / k
+    _check(C, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("m", [128, 384, 200])
+def test_fused_polynomial(mg, dtype, m):
+    X = _rand((1, m, 2 * m), torch.float64, 6)
+    G64 = torch.matmul(X, X.transpose(1, 2))
+    G64 = G64 / torch.linalg.matrix_norm(G64, ord=2, keepdim=True)
+    G = G64.to(dtype).contiguous()
+    P = torch.zeros_like(G)
+    a, b, c = 3.4445, -4.7750, 2.0315
+    mg.muon_debug_gemm(G, G, P, b_kmajor=True, symmetric=True, poly=(a, b, c))
+    torch.cuda.synchronize()
+    Gd = G.double()
+    ref = a * torch.eye(m, device="cuda", dtype=torch.float64) + b * Gd + c * torch.matmul(Gd, Gd)
+    assert torch.equal(P, P.transpose(1, 2))
+    _check(P, ref, dtype)
+
+
+def test_large_gram_and_apply_bf16(mg):
+    """The two long products at the 2560 x 9728 size (several waves of tiles)."""
+    m, n = 2560, 9728
+    X = _rand((1, m, n), torch.bfloat16, 7, scale=1.0 / np.sqrt(n))
+    G = torch.zeros((1, m, m), dtype=torch.bfloat16, device="cuda")
+    mg.muon_debug_gemm(X, X, G, b_kmajor=True, symmetric=True)
+    Q = _rand((1, m, m), torch.bfloat16, 8, scale=1.0 / np.sqrt(m))
+    Y = torch.zeros((1, m, n), dtype=torch.bfloat16, device="cuda")
+    mg.muon_debug_gemm(Q, X, Y, b_kmajor=False)
+    torch.cuda.synchronize()
+    Xd = X.double()
+    _check(G, torch.matmul(Xd, Xd.transpose(1, 2)), torch.bfloat16)
+    _check(Y, torch.matmul(Q.double(), Xd), torch.bfloat16)

@@ -1,0 +1,203 @@
+"""CUDA path vs the fp64 CPU oracle on identical seeded bytes.
+
+Bars (relative Frobenius error of the ortho output; singular values sorted):
+fp32 path 1e-4, bf16 path 2e-2, max singular-value deviation 0.05.  For
+muon_step the updated weights are compared as
+||W'_gpu - W'_exact|| / ||W'_exact - W|| <= tol + q, q being the oracle's own
+storage-rounding term, and momentum within one storage ulp of round(beta M + G).
+Sizes span several tiles and ragged tails; edge cases cover vectors, tiny and
+unaligned shapes, mixed orientation in one bucket, zero and non-finite input.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import muon_oracle as orc
+from tests.gpu_util import SIGMA_TOL, TOL, rel_fro, sigma_dev, to_device, to_f64
+from workloads import gen_matrix, zeros_matrix
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as pkg
+    yield pkg
+    pkg.muon_set_ns_config(pkg.QUINTIC, 5, (2, 2, 1), pkg.MUON_PATH_AUTO)
+
+
+def _ortho_case(mg, rows, cols, batch, dtype, segments, seed, std=1.0):
+    mats = [gen_matrix(seed + b, 0, rows, cols, std, dtype) for b in range(batch)]
+    x = torch.stack([to_device(h, torch) for h in mats]).contiguous()
+    mg.muon_ns_orthogonalize(x, mg.QUINTIC, 5, segments)
+    assert mg.muon_sync_status() == mg.MUON_OK
+    path = "gram" if segments else "plain"
+    worst_f, worst_s = 0.0, 0.0
+    for b, h in enumerate(mats):
+        O_ref = orc.orthogonalize(orc.to_f64(h.data, dtype), path, segments=segments or (2, 2, 1))
+        O = to_f64(x[b])
+        worst_f = max(worst_f, rel_fro(O, O_ref))
+        worst_s = max(worst_s, sigma_dev(O, O_ref))
+    return worst_f, worst_s
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(256, 1024, 1), (200, 37, 2), (96, 300, 1), (64, 160, 3)])
+@pytest.mark.parametrize("segments", [None, (2, 2, 1)])
+def test_orthogonalize_fp32(mg, rows, cols, batch, segments):
+    f, s = _ortho_case(mg, rows, cols, batch, "f32", segments, 100)
+    assert f <= TOL["f32"], f
+    assert s <= SIGMA_TOL
+
+
+@pytest.mark.parametrize("rows,cols,batch", [
+    (256, 1024, 1), (128, 512, 4), (256, 256, 2), (300, 1000, 1), (1000, 296, 1), (8, 16, 2),
+    (2, 3, 1), (1, 64, 1), (37, 200, 2), (130, 130, 1)])
+@pytest.mark.parametrize("segments", [None, (2, 2, 1), (2, 3)])
+def test_orthogonalize_bf16(mg, rows, cols, batch, segments):
+    f, s = _ortho_case(mg, rows, cols, batch, "bf16", segments, 200, std=0.03)
+    assert f <= TOL["bf16"], f
+    assert s <= SIGMA_TOL, s
+
+
+def _step_case(mg, shapes, dtype, mom_dtype, path_code, nesterov, seed0, grad_std, steps=1):
+    """Runs `steps` muon_step calls (fresh gradient each) and compares each step."""
+    Ws = [gen_matrix(seed0 + i, 1, r, c, 0.02, dtype) for i, (r, c) in enumerate(shapes)]
+    Ms = [zeros_matrix(r, c, mom_dtype) for (r, c) in shapes]
+    w = [to_device(h, torch) for h in Ws]
+    mo = [to_device(h, torch) for h in Ms]
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), path_code)
+    results = []
+    for st in range(steps):
+        Gs = [gen_matrix(seed0 + i, 0 if st == 0 else 2, r, c, grad_std, dtype) for i, (r, c) in enumerate(shapes)]
+        g = [to_device(h, torch) for h in Gs]
+        W_host = [to_f64(t) for t in w]
+        M_host = [to_f64(t) for t in mo]
+        mg.muon_step(w, g, mo, lr=0.02, beta=0.95, wd=0.1, nesterov=nesterov)
+        assert mg.muon_sync_status() == mg.MUON_OK
+        for i, (r, c) in enumerate(shapes):
+            path = mg.muon_last_path(r, c, mg.MUON_BF16 if dtype == "bf16" else mg.MUON_F32)
+            pname = "gram" if path == mg.MUON_PATH_GRAM else "plain"
+            # the library receives fp32 hyper-parameters; the oracle gets the same values
+            ref = orc.muon_step(_store(W_host[i], dtype), _store(M_host[i], mom_dtype), Gs[i].data,
+                                lr=F32(0.02), beta=F32(0.95), wd=F32(0.1), nesterov=nesterov, path=pname,
+                                param_dtype=dtype, mom_dtype=mom_dtype)
+            d = ref["W_exact"] - ref["W_old"]
+            err = np.linalg.norm(to_f64(w[i]) - ref["W_exact"]) / np.linalg.norm(d)
+            q = np.linalg.norm(ref["W_new"] - ref["W_exact"]) / np.linalg.norm(d)
+            m_gpu = to_f64(mo[i])
+            ulp = _ulp(ref["M_new"], mom_dtype)
+            m_ok = bool(np.all(np.abs(m_gpu - ref["M_new"]) <= ulp))
+            results.append((err, q, m_ok, pname))
+    return results
+
+
+def F32(x):
+    return float(np.float32(x))
+
+
+def _store(x64, dtype):
+    if dtype == "f32":
+        return x64.astype(np.float32)
+    return orc.bf16_bits_from_f64(orc.round_bf16(x64))
+
+
+def _ulp(x, dtype):
+    bits = 8 if dtype == "bf16" else 24
+    ax = np.maximum(np.abs(x), 1e-30)
+    return np.ldexp(1.0, (np.floor(np.log2(ax)).astype(int) - (bits - 1)))
+
+
+@pytest.mark.parametrize("path", ["plain", "gram"])
+def test_step_single_256x1024_f32(mg, path):
+    code = mg.MUON_PATH_PLAIN if path == "plain" else mg.MUON_PATH_GRAM
+    for err, q, m_ok, pname in _step_case(mg, [(256, 1024)], "f32", "f32", code, False, 1000, 1.0, steps=2):
+        assert pname == path
+        assert err <= TOL["f32"] + q, (err, q)
+        assert m_ok
+
+
+@pytest.mark.parametrize("path", ["plain", "gram"])
+def test_step_bf16_mixed_shapes_two_steps(mg, path):
+    code = mg.MUON_PATH_PLAIN if path == "plain" else mg.MUON_PATH_GRAM
+    shapes = [(192, 640), (640, 192), (192, 640), (96, 96), (37, 200), (1, 40)]
+    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", code, True, 3000, 0.02, steps=2):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+
+
+def test_step_bf16_params_f32_momentum(mg):
+    shapes = [(256, 896), (896, 256)]
+    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "f32", mg.MUON_PATH_AUTO, False, 5000, 0.0316, steps=2):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+
+
+def test_zero_gradient_only_decays(mg):
+    W = gen_matrix(7000, 1, 128, 384, 0.02, "bf16")
+    w = to_device(W, torch)
+    g = torch.zeros_like(w)
+    mo = torch.zeros_like(w)
+    mg.muon_step([w], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+    assert mg.muon_sync_status() == mg.MUON_OK
+    expect = orc.round_bf16(orc.to_f64(W.data, "bf16") * (1 - 0.002))
+    got = to_f64(w)
+    assert np.max(np.abs(got - expect) / np.maximum(np.abs(expect), 1e-30)) <= 2.0 ** -8
+
+
+def test_nonfinite_gradient_is_reported(mg):
+    w = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros_like(w)
+    g[3, 5] = float("inf")
+    mo = torch.zeros_like(w)
+    mg.muon_step([w], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+    assert mg.muon_sync_status() == mg.MUON_ENONFINITE
+    assert mg.muon_sync_status() == mg.MUON_OK        # the word is cleared on read
+
+
+def test_launch_count_matches_plan(mg):
+    w = torch.randn((128, 512), device="cuda").to(torch.bfloat16)
+    g, mo = torch.randn_like(w) * 0.01, torch.zeros_like(w)
+    for path, expect in ((mg.MUON_PATH_GRAM, 2 + 3 + 5 + 2 + 4 + 3), (mg.MUON_PATH_PLAIN, 2 + 5 * 3)):
+        mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), path)
+        before = mg.muon_launch_count()
+        mg.muon_step([w], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+        assert mg.muon_launch_count() - before == expect
+    assert mg.muon_sync_status() == mg.MUON_OK
+
+
+def test_kernel_timing_record(mg):
+    w = torch.randn((256, 1024), device="cuda").to(torch.bfloat16)
+    g, mo = torch.randn_like(w) * 0.01, torch.zeros_like(w)
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_GRAM)
+    mg.muon_kernel_timing_read()
+    mg.muon_set_kernel_timing(True)
+    mg.muon_step([w], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+    rec = mg.muon_kernel_timing_read()
+    mg.muon_set_kernel_timing(False)
+    assert rec["gemm_tc_syrk"][0] == 3 and rec["gemm_tc_apply"][0] == 2 and rec["gemm_tc_apply_update"][0] == 1
+    nom, alg = mg.muon_ns_flops(256, 1024, mg.MUON_PATH_GRAM, (2, 2, 1))
+    tot = sum(v[2] for k, v in rec.items() if k.startswith("gemm"))
+    assert abs(tot - alg) / alg < 1e-12
+    assert all(v[1] > 0 for v in rec.values())
+
+
+def test_autotune_and_cache_round_trip(mg, tmp_path):
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_AUTO)
+    mg.muon_autotune([(256, 768), (768, 256), (128, 128)], mg.MUON_BF16)
+    p = tmp_path / "tune.tsv"
+    mg.muon_tune_save(str(p))
+    assert mg.muon_tune_load(str(p)) >= 2
+    w = torch.randn((768, 256), device="cuda").to(torch.bfloat16)
+    g, mo = torch.randn_like(w) * 0.01, torch.zeros_like(w)
+    mg.muon_step([w], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+    assert mg.muon_last_path(256, 768, mg.MUON_BF16) in (mg.MUON_PATH_PLAIN, mg.MUON_PATH_GRAM)
+    assert mg.muon_sync_status() == mg.MUON_OK
+    text = p.read_text().splitlines()
+    assert text[0] == "muon-tune v1" and len(text) >= 3
+    # a corrupt line is skipped, the rest loads
+    p.write_text("\n".join(text + ["garbage\tline"]) + "\n")
+    assert mg.muon_tune_load(str(p)) == len(text) - 1
