@@ -176,8 +176,11 @@ int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms,
  *   values, mirrored (C[j][i] = C[i][j]); valid when the exact product is
  *   symmetric.  poly != 0 (symmetric only, A == B == G) writes
  *   pa*I + pb*G + pc*(G G) instead of the product.
- *   C is M x N.  dtype is the storage type of A, B and C.  tile_n selects the
- *   N extent of the tensor-core tile (0 = default, 128 or 256).
+ *   C is M x N.  dtype is the storage type of A, B and C: MUON_BF16 (bf16
+ *   tensor cores), MUON_F32 (fp32 FFMA), or 2 = fp32 storage multiplied on the
+ *   TF32 tensor path (the kind the bf16 NS path uses for its Gram-space
+ *   products; B must be K-major).  tile_n selects the N extent of the
+ *   tensor-core tile (0 = default, 128 or 256).
  */
 int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                     int64_t batch, int dtype, int b_kmajor, int symmetric, int poly,

@@ -245,15 +245,21 @@ def muon_kernel_timing_read():
     return out
 
 
-def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.0, tile_n=0, stream=None):
-    """C[b] = alpha * A[b] op(B[b]) (or the fused polynomial when poly=(a, b, c))."""
+MUON_DEBUG_TF32 = 2
+
+
+def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.0, tile_n=0, stream=None,
+                    tf32=False):
+    """C[b] = alpha * A[b] op(B[b]) (or the fused polynomial when poly=(a, b, c)).
+    tf32=True multiplies fp32 tensors on the TF32 tensor-core path."""
     for t, nm in ((A, "A"), (B, "B"), (C, "C")):
         _cuda_contig(t, nm)
     batch = A.shape[0] if A.dim() == 3 else 1
     M, K = A.shape[-2], A.shape[-1]
     N = B.shape[-2] if b_kmajor else B.shape[-1]
     pa, pb, pc = poly if poly is not None else (0.0, 0.0, 0.0)
-    _check(lib().muon_debug_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, batch, _dtype_code(A),
+    code = MUON_DEBUG_TF32 if tf32 else _dtype_code(A)
+    _check(lib().muon_debug_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, batch, code,
                                  1 if b_kmajor else 0, 1 if symmetric else 0, 1 if poly is not None else 0,
                                  float(alpha), float(pa), float(pb), float(pc), tile_n, _stream_ptr(stream)),
            "muon_debug_gemm")

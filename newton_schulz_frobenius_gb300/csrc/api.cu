@@ -307,6 +307,7 @@ static GemmArgs gemm_base(int dtype, int* status) {
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
     a.dtype = dtype;
+    a.c_dtype = dtype == MUON_BF16 ? MUON_BF16 : MUON_F32;
     a.alpha = 1.0f;
     a.tile_n = 256;
     a.status = status;
@@ -317,9 +318,10 @@ static GemmArgs gemm_base(int dtype, int* status) {
 static int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
     const double mnk = (double)a.M * a.N * a.K * a.batch;
     const double work = a.symmetric ? mnk : 2.0 * mnk;
-    const int kc = (a.dtype == MUON_BF16) ? kclass : KC_SIMT;
+    const bool tc = (a.dtype == MUON_BF16 || a.dtype == DT_TF32);
+    const int kc = tc ? kclass : KC_SIMT;
     note_launch_begin(kc, s);
-    cudaError_t e = (a.dtype == MUON_BF16) ? launch_gemm_tc(a, dc.sms, s) : launch_gemm_simt(a, s);
+    cudaError_t e = tc ? launch_gemm_tc(a, dc.sms, s) : launch_gemm_simt(a, s);
     note_launch_end(kc, work, s);
     if (e != cudaSuccess) return cuda_fail(e, "product launch");
     return MUON_OK;
@@ -336,13 +338,15 @@ struct ChunkLayout {
     int nparts;
 };
 
+// X is stored in the path's dtype; the m x m Gram-space matrices are fp32 on
+// both paths (TF32-rounded on the bf16 path).
 static ChunkLayout chunk_layout(int m, int n, int B, int dtype) {
     ChunkLayout L;
     const size_t es = esize(dtype);
     L.ldx = pad8(n);
     L.ldm = pad8(m);
     L.x_bytes = (size_t)m * L.ldx * es;
-    L.m_bytes = (size_t)m * L.ldm * es;
+    L.m_bytes = (size_t)m * L.ldm * 4;
     L.nparts = prep_num_parts(m, n);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -370,6 +374,13 @@ struct FinalEpi {
 
 // Runs NS on B oriented m x n matrices held (unnormalised when use_inv) in
 // the chunk's X buffer, ending in `fin`.
+//
+// Precision of the bf16 path: X and the long products XX^T, QX are bf16 with
+// fp32 accumulation; the m x m Gram-space matrices G, P, PG, Q are kept as
+// TF32-rounded fp32 and multiplied on the TF32 tensor path; the transform that
+// is applied to X at a segment end is rounded to bf16.  With every Gram-space
+// matrix in bf16 instead, square and small inputs of the Gram path exceed a 2%
+// relative error against the exact iteration; with TF32 they stay near 1%.
 static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
                   int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin) {
     char* X = base + L.off_X;
@@ -380,14 +391,24 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
     const int64_t strideX = (int64_t)m * L.ldx;
     const int64_t strideM = (int64_t)m * L.ldm;
 
-    auto sym = [&](const void* A, const void* Bm, void* C) {
-        GemmArgs g = gemm_base(dtype, dc.status);
+    const bool bf = (dtype == MUON_BF16);
+    const int sq_dtype = bf ? DT_TF32 : MUON_F32;     // Gram-space operands
+    auto gram_out = [&](GemmArgs& g, bool feeds_apply) {
+        // Gram-space result: TF32-rounded fp32, or bf16 when it is the
+        // transform the long apply consumes (bf16 path only)
+        if (!bf) return;
+        if (feeds_apply) { g.c_dtype = MUON_BF16; g.round_tf32 = 0; }
+        else { g.c_dtype = MUON_F32; g.round_tf32 = 1; }
+    };
+    auto sym = [&](const void* A, const void* Bm, void* C, bool feeds_apply) {
+        GemmArgs g = gemm_base(sq_dtype, dc.status);
         g.A = A; g.lda = L.ldm; g.strideA = strideM;
         g.B = Bm; g.ldb = L.ldm; g.strideB = strideM;
         g.M = m; g.N = m; g.K = m; g.batch = B;
         g.symmetric = 1;
         g.epi = EPI_STORE;
         g.C = C; g.ldc = L.ldm; g.strideC = strideM;
+        gram_out(g, feeds_apply);
         return g;
     };
 
@@ -406,6 +427,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
             g.symmetric = 1;
             g.epi = EPI_STORE;
             g.C = G; g.ldc = L.ldm; g.strideC = strideM;
+            gram_out(g, false);
             if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 1; }
             int r = run_gemm(dc, s, g, KC_SYRK);
             if (r) return r;
@@ -422,7 +444,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
             // P = aI + bG + cG^2, fused into the G^2 product
             const int p = grab();
             {
-                GemmArgs g = sym(G, G, S[p]);
+                GemmArgs g = sym(G, G, S[p], Lseg == 1);
                 g.epi = EPI_POLY;
                 g.Gin = G; g.ldg = L.ldm; g.strideG = strideM;
                 g.pa = plan.a; g.pb = plan.b; g.pc = plan.c;
@@ -433,16 +455,16 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
                 q = p;
             } else {
                 const int qn = grab();     // Q <- P Q
-                int r = run_gemm(dc, s, sym(S[p], S[q], S[qn]), KC_SQUARE);
+                int r = run_gemm(dc, s, sym(S[p], S[q], S[qn], j == Lseg), KC_SQUARE);
                 if (r) return r;
                 used[q] = false;
                 q = qn;
             }
             if (j < Lseg) {
                 const int t = grab();      // G <- (P G) P
-                int r = run_gemm(dc, s, sym(S[p], G, S[t]), KC_SQUARE);
+                int r = run_gemm(dc, s, sym(S[p], G, S[t], false), KC_SQUARE);
                 if (r) return r;
-                r = run_gemm(dc, s, sym(S[t], S[p], G), KC_SQUARE);
+                r = run_gemm(dc, s, sym(S[t], S[p], G, false), KC_SQUARE);
                 if (r) return r;
                 used[t] = false;
             }
@@ -1037,14 +1059,16 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
     if (!A || !B || !C) return fail(MUON_EINVAL, "NULL operand");
     if (M < 1 || N < 1 || K < 1 || batch < 1) return fail(MUON_EINVAL, "bad sizes");
     if (M > (1 << 20) || N > (1 << 20) || K > (1 << 20)) return fail(MUON_EINVAL, "size above 2^20");
-    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if (!valid_dtype(dtype) && dtype != DT_TF32) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if (dtype == DT_TF32 && !b_kmajor) return fail(MUON_EINVAL, "TF32 products need a K-major B");
     if ((symmetric || poly) && M != N) return fail(MUON_EINVAL, "symmetric product needs M == N");
     if (poly && (!symmetric || K != M)) return fail(MUON_EINVAL, "poly needs a symmetric square product");
     if (tile_n != 0 && tile_n != 128 && tile_n != 256) return fail(MUON_EINVAL, "tile_n must be 0, 128 or 256");
-    if (dtype == MUON_BF16) {
+    if (dtype == MUON_BF16 || dtype == DT_TF32) {
         const int64_t ldb = b_kmajor ? K : N;
-        if ((K % 8) || (ldb % 8) || (reinterpret_cast<uintptr_t>(A) % 16) || (reinterpret_cast<uintptr_t>(B) % 16))
-            return fail(MUON_EINVAL, "bf16 operands need 16-byte aligned rows");
+        const int64_t epr = dtype == DT_TF32 ? 4 : 8;
+        if ((K % epr) || (ldb % epr) || (reinterpret_cast<uintptr_t>(A) % 16) || (reinterpret_cast<uintptr_t>(B) % 16))
+            return fail(MUON_EINVAL, "tensor-core operands need 16-byte aligned rows");
     }
     int r;
     DevCtx dc;

@@ -24,6 +24,14 @@ __device__ __forceinline__ void st_elem(void* p, int64_t i, float v, int dtype) 
     else reinterpret_cast<float*>(p)[i] = v;
 }
 
+// Nearest TF32 value (10 explicit mantissa bits), ties to even, on the fp32
+// bit pattern; finite inputs only (the NS path keeps its values bounded).
+__device__ __forceinline__ float round_tf32(float v) {
+    uint32_t u = __float_as_uint(v);
+    u = (u + 0xFFFu + ((u >> 13) & 1u)) & ~0x1FFFu;
+    return __uint_as_float(u);
+}
+
 __device__ __forceinline__ float epi_alpha(const GemmArgs& a, int b) {
     float s = a.alpha;
     if (a.alpha_vec) {
@@ -79,6 +87,7 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
 
     if (a.epi == EPI_STORE || a.epi == EPI_POLY) {
         const int64_t cbase = (int64_t)b * a.strideC;
+        const int cd = a.c_dtype;
         if (a.epi == EPI_POLY) {
             const int64_t gbase = (int64_t)b * a.strideG + (int64_t)r * a.ldg + c0;
 #pragma unroll
@@ -92,21 +101,25 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
 #pragma unroll
             for (int j = 0; j < W; ++j) v[j] *= s;
         }
+        if (a.round_tf32) {
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = round_tf32(v[j]);
+        }
         if (a.symmetric) {
 #pragma unroll
             for (int j = 0; j < W; ++j) {
                 const int c = c0 + j;
                 if (j < nvalid && c <= r) {
-                    st_elem(a.C, cbase + (int64_t)r * a.ldc + c, v[j], a.dtype);
-                    if (c < r) st_elem(a.C, cbase + (int64_t)c * a.ldc + r, v[j], a.dtype);
+                    st_elem(a.C, cbase + (int64_t)r * a.ldc + c, v[j], cd);
+                    if (c < r) st_elem(a.C, cbase + (int64_t)c * a.ldc + r, v[j], cd);
                 }
             }
         } else if (nvalid == W) {
-            store_row_run<W>(a.C, cbase + (int64_t)r * a.ldc + c0, v, a.dtype);
+            store_row_run<W>(a.C, cbase + (int64_t)r * a.ldc + c0, v, cd);
         } else {
 #pragma unroll
             for (int j = 0; j < W; ++j)
-                if (j < nvalid) st_elem(a.C, cbase + (int64_t)r * a.ldc + c0 + j, v[j], a.dtype);
+                if (j < nvalid) st_elem(a.C, cbase + (int64_t)r * a.ldc + c0 + j, v[j], cd);
         }
         return;
     }
@@ -159,6 +172,103 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
             }
         }
     }
+}
+
+}  // namespace muon
+
+namespace muon {
+
+// Tensor-core epilogue for one warp and one 32 x 32 chunk: lane l holds row
+// r0 + l, columns c0 .. c0+31 (one tcgen05.ld).  The chunk is staged through
+// shared memory (stage: 32 x 33 floats owned by this warp) so that every
+// global access is a 32-lane run along a row of its matrix:
+//   row phase     lane l handles column c0 + l of rows r0 .. r0+31
+//                 (row-major stores, the polynomial's G reads, the caller's
+//                 W / O in their own orientation)
+//   column phase  lane l handles row r0 + l of columns c0 .. c0+31
+//                 (the mirrored half of a symmetric product, and the caller's
+//                 W / O of a transposed (tall) matrix)
+__device__ __forceinline__ void epi_chunk_staged(const GemmArgs& a, int b, int r0, int c0, const float (&v)[32],
+                                                 float (*stage)[33]) {
+    const int lane = threadIdx.x & 31;
+    const float s = epi_alpha(a, b);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[lane][j] = s * v[j];
+    __syncwarp();
+
+    const int col = c0 + lane;
+    const bool col_ok = col < a.N;
+    const int epi = a.epi;
+    if (epi == EPI_STORE || epi == EPI_POLY) {
+        const int64_t cbase = (int64_t)b * a.strideC;
+        const int cd = a.c_dtype;
+        for (int i = 0; i < 32; ++i) {
+            const int row = r0 + i;
+            if (row >= a.M) break;
+            if (!col_ok) continue;
+            float val = stage[i][lane];
+            if (epi == EPI_POLY) {
+                const float g = ld_elem(a.Gin, (int64_t)b * a.strideG + (int64_t)row * a.ldg + col, a.dtype);
+                val = a.pc * val + a.pb * g + (row == col ? a.pa : 0.f);
+            }
+            if (a.round_tf32) val = round_tf32(val);
+            stage[i][lane] = val;
+            if (!a.symmetric || col <= row) st_elem(a.C, cbase + (int64_t)row * a.ldc + col, val, cd);
+        }
+        if (a.symmetric) {
+            __syncwarp();
+            const int r = r0 + lane;
+            if (r < a.M) {
+                for (int j = 0; j < 32; ++j) {
+                    const int c = c0 + j;
+                    if (c >= r || c >= a.N) break;   // only strictly below the diagonal
+                    st_elem(a.C, cbase + (int64_t)c * a.ldc + r, stage[lane][j], cd);
+                }
+            }
+        }
+        __syncwarp();
+        return;
+    }
+
+    const MatEntry e = a.mats[b];
+    const int od = a.out_dtype;
+    const float keep = 1.0f - a.lr * a.wd;
+    const float step = a.lr * a.scale;
+    if (!e.trans) {
+        // caller matrix is m x n, row-major: row phase
+        for (int i = 0; i < 32; ++i) {
+            const int row = r0 + i;
+            if (row >= a.M) break;
+            if (!col_ok) continue;
+            const int64_t off = (int64_t)row * a.N + col;
+            const float o = stage[i][lane];
+            if (epi == EPI_OUT) {
+                st_elem(e.w, off, o, od);
+            } else {
+                const float w = ld_elem(e.w, off, od);
+                st_elem(e.w, off, fmaf(-step, o, keep * w), od);
+            }
+        }
+    } else {
+        // caller matrix is n x m (tall): element (row, col) of the oriented
+        // matrix lives at col * m + row; column phase keeps lanes on a run
+        const int r = r0 + lane;
+        if (r < a.M) {
+            for (int j = 0; j < 32; ++j) {
+                const int c = c0 + j;
+                if (c >= a.N) break;
+                const int64_t off = (int64_t)c * a.M + r;
+                const float o = stage[lane][j];
+                if (epi == EPI_OUT) {
+                    st_elem(e.w, off, o, od);
+                } else {
+                    const float w = ld_elem(e.w, off, od);
+                    st_elem(e.w, off, fmaf(-step, o, keep * w), od);
+                }
+            }
+        }
+    }
+    __syncwarp();
 }
 
 }  // namespace muon

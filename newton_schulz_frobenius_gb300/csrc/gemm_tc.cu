@@ -17,6 +17,9 @@
 //               (M = 128, N = BN, K = 16 per instruction, fp32 accumulator)
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, fused epilogue from
 //               epilogue.cuh, global stores
+// Operand kinds: bf16 (kind::f16, K = 16 per instruction) for the long
+// products, TF32 on fp32 storage (kind::tf32, K = 8) for the m x m Gram-space
+// products; either way one k-block is 128 bytes of every operand row.
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
 // of tile t overlaps the main loop of tile t+1.  Every mbarrier wait is bounded:
 // after WAIT_LIMIT_NS it sets an abort flag and the status word, waits (again
@@ -33,7 +36,8 @@ namespace muon {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BK = 64;            // bf16 elements = 128 bytes: one swizzle row
+constexpr int BK = 64;            // bf16 elements per k-block = 128 bytes: one swizzle row
+constexpr int BK_BYTES = 128;
 constexpr int NTHREADS = 192;
 
 template <int BN>
@@ -44,7 +48,8 @@ struct Cfg {
     static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+    static constexpr int EPI_STAGE_BYTES = 4 * 32 * 33 * 4;   // one 32 x 33 fp32 chunk per epilogue warp
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
 };
 
 // ---------------------------------------------------------------------------
@@ -156,6 +161,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
@@ -207,6 +222,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::tf32: fp32 accumulator, TF32 A and B (format
+// code 2), both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 struct TileSched {
     int tiles_m, tiles_n, per_batch, total, sym;
 
@@ -230,19 +251,22 @@ struct TileSched {
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int BN, bool B_KMAJOR>
+template <int BN, bool B_KMAJOR, bool TF32>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ GemmArgs args, const TileSched sched) {
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
-    constexpr uint32_t IDESC = idesc_bf16(BM, BN, !B_KMAJOR);
+    static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
+    constexpr uint32_t IDESC = TF32 ? idesc_tf32(BM, BN) : idesc_bf16(BM, BN, !B_KMAJOR);
+    constexpr int KE = TF32 ? 32 : 64;    // elements per 128-byte k-block
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
+    float* epi_stage = reinterpret_cast<float*>(sB + S * C::B_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_stage) + C::EPI_STAGE_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -280,7 +304,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int kblocks = (args.K + BK - 1) / BK;
+    const int kblocks = (args.K + KE - 1) / KE;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -301,9 +325,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, C::STAGE_BYTES);
-                    tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * BK, tm * BM, b);
+                    tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
                     if (B_KMAJOR) {
-                        tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * BK, tn * BN, b);
+                        tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN, b);
                     } else {
 #pragma unroll
                         for (int q = 0; q < BN / 64; ++q)
@@ -350,10 +374,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
+                        // one instruction consumes 32 bytes of K (16 bf16 or 8 TF32)
                         const uint64_t ad = sdesc(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_KMAJOR ? sdesc(b_base + kk * 32, 16, 1024)
                                                      : sdesc(b_base + kk * 2048, BK * 128, 1024);
-                        tc_mma_bf16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if (TF32) tc_mma_tf32(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                        else tc_mma_bf16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8 * stage);
                     if (++stage == S) {
@@ -376,6 +402,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;   // TMEM lane quarter this warp may access
+        float (*stage)[33] = reinterpret_cast<float (*)[33]>(epi_stage + (warp - 2) * 32 * 33);
         int acc = 0;
         uint32_t aphase = 0;
         for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
@@ -385,8 +412,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const bool ok = wait_bounded(accf0 + 8 * acc, aphase, abort_flag, args.status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int row = tm * BM + q * 32 + lane;
-            const int warp_row_max = tm * BM + q * 32 + 31;
+            const int row0 = tm * BM + q * 32;
+            const int warp_row_max = row0 + 31;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 const int col0 = tn * BN + ch * 32;
@@ -394,7 +421,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (args.symmetric && col0 > warp_row_max) continue;
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-                epi_row_chunk<32>(args, b, row, col0, v);
+                epi_chunk_staged(args, b, row0, col0, v, stage);
             }
             tc_fence_before();
             __syncwarp();
@@ -430,42 +457,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D bf16 tensor map over `batch` matrices of `rows` x `inner` (row pitch ld,
-// matrix pitch stride, in elements), box box_inner x box_rows x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t batch, uint64_t ld,
-              uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
+// 3-D tensor map (bf16 or fp32 elements) over `batch` matrices of `rows` x
+// `inner` (row pitch ld, matrix pitch stride, in elements), box box_inner x
+// box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t rows, uint64_t batch,
+              uint64_t ld, uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     if (batch <= 1) stride = ld * rows;
+    const uint64_t eb = f32 ? 4 : 2;
     cuuint64_t dims[3] = {inner, rows, batch};
-    cuuint64_t strides[2] = {ld * 2, stride * 2};
+    cuuint64_t strides[2] = {ld * eb, stride * eb};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_KMAJOR>
+template <int BN, bool B_KMAJOR, bool TF32>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     using C = Cfg<BN>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, B_KMAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, B_KMAJOR, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap mA, mB;
-    if (!make_map(&mA, a.A, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda, (uint64_t)a.strideA,
-                  BK, BM))
+    constexpr uint32_t KE = TF32 ? 32 : 64;   // elements per 128-byte k-block
+    if (!make_map(&mA, a.A, TF32, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda,
+                  (uint64_t)a.strideA, KE, BM))
         return cudaErrorInvalidValue;
-    bool okB = B_KMAJOR ? make_map(&mB, a.B, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch, (uint64_t)a.ldb,
-                                   (uint64_t)a.strideB, BK, BN)
-                        : make_map(&mB, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch, (uint64_t)a.ldb,
-                                   (uint64_t)a.strideB, 64, BK);
+    bool okB = B_KMAJOR ? make_map(&mB, a.B, TF32, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
+                                   (uint64_t)a.ldb, (uint64_t)a.strideB, KE, BN)
+                        : make_map(&mB, a.B, TF32, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch,
+                                   (uint64_t)a.ldb, (uint64_t)a.strideB, 64, BK);
     if (!okB) return cudaErrorInvalidValue;
 
     TileSched sc;
@@ -475,27 +505,36 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     sc.per_batch = a.symmetric ? sc.tiles_m * (sc.tiles_m + 1) / 2 : sc.tiles_m * sc.tiles_n;
     sc.total = sc.per_batch * a.batch;
     const int grid = sc.total < num_sms ? sc.total : num_sms;
-    gemm_tc_kernel<BN, B_KMAJOR><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mA, mB, a, sc);
+    gemm_tc_kernel<BN, B_KMAJOR, TF32><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mA, mB, a, sc);
     return cudaGetLastError();
 }
 
 }  // namespace tc
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
-    if (a.dtype != MUON_BF16) return cudaErrorInvalidValue;
+    const bool tf32 = (a.dtype == DT_TF32);
+    if (a.dtype != MUON_BF16 && !tf32) return cudaErrorInvalidValue;
+    if (tf32 && !a.b_kmajor) return cudaErrorInvalidValue;
     if (a.M < 1 || a.N < 1 || a.K < 1 || a.batch < 1) return cudaErrorInvalidValue;
     if (a.symmetric && a.M != a.N) return cudaErrorInvalidValue;
     // TMA: 16-byte aligned bases and pitches
+    const int64_t epr = tf32 ? 4 : 8;   // elements per 16 bytes
     auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    if (!al16(a.A) || !al16(a.B) || (a.lda % 8) || (a.ldb % 8) || (a.strideA % 8) || (a.strideB % 8))
+    if (!al16(a.A) || !al16(a.B) || (a.lda % epr) || (a.ldb % epr) || (a.strideA % epr) || (a.strideB % epr))
         return cudaErrorInvalidValue;
     if ((int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + 127) / 128) > (int64_t)1 << 30)
         return cudaErrorInvalidValue;
     const int bn = a.symmetric ? 128 : (a.tile_n == 128 ? 128 : 256);
-    if (bn == 128) {
-        return a.b_kmajor ? tc::launch_impl<128, true>(a, num_sms, s) : tc::launch_impl<128, false>(a, num_sms, s);
+    if (tf32) {
+        return bn == 128 ? tc::launch_impl<128, true, true>(a, num_sms, s)
+                         : tc::launch_impl<256, true, true>(a, num_sms, s);
     }
-    return a.b_kmajor ? tc::launch_impl<256, true>(a, num_sms, s) : tc::launch_impl<256, false>(a, num_sms, s);
+    if (bn == 128) {
+        return a.b_kmajor ? tc::launch_impl<128, true, false>(a, num_sms, s)
+                          : tc::launch_impl<128, false, false>(a, num_sms, s);
+    }
+    return a.b_kmajor ? tc::launch_impl<256, true, false>(a, num_sms, s)
+                      : tc::launch_impl<256, false, false>(a, num_sms, s);
 }
 
 }  // namespace muon

@@ -10,6 +10,11 @@
 
 namespace muon {
 
+// Internal storage/arithmetic code next to MUON_F32 and MUON_BF16: fp32
+// storage whose values are consumed by the tensor cores as TF32 (10-bit
+// mantissa).  The bf16 path keeps its m x m Gram-space matrices in this form.
+constexpr int DT_TF32 = 2;
+
 // Bits of the per-device status word (read by muon_sync_status).
 enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
 
@@ -37,8 +42,10 @@ enum EpiKind : int {
 
 // One (batched) product C[b] = epilogue(A[b] * op(B[b])).
 // A is M x K row-major (K contiguous).  b_kmajor: B stored N x K (op = ^T);
-// otherwise B stored K x N (op = identity).  dtype is the storage type of
-// A, B, C and Gin (MUON_BF16 or MUON_F32).
+// otherwise B stored K x N (op = identity).  dtype is the operand type of A, B
+// and Gin (MUON_BF16, MUON_F32 on the FFMA path, or DT_TF32); c_dtype is the
+// storage type of C (MUON_BF16 or MUON_F32); round_tf32 rounds fp32 results to
+// the nearest TF32 value (ties to even) before they are stored.
 struct GemmArgs {
     const void* A; int64_t lda; int64_t strideA;
     const void* B; int64_t ldb; int64_t strideB;
@@ -46,6 +53,8 @@ struct GemmArgs {
     int M, N, K, batch;
     int symmetric;          // M == N, lower-triangle tiles only, mirrored store
     int dtype;
+    int c_dtype;
+    int round_tf32;
     int epi;
     float alpha;            // scalar factor
     const float* alpha_vec; // optional per-batch factor (device), may be null

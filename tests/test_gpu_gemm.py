@@ -107,3 +107,52 @@ def test_large_gram_and_apply_bf16(mg):
     Xd = X.double()
     _check(G, torch.matmul(Xd, Xd.transpose(1, 2)), torch.bfloat16)
     _check(Y, torch.matmul(Q.double(), Xd), torch.bfloat16)
+
+
+def _tf32_rne(t):
+    u = t.view(torch.int32)
+    u = (u + 0xFFF + ((u >> 13) & 1)) & ~0x1FFF
+    return u.view(torch.float32)
+
+
+def _tf32_trunc(t):
+    """fp32 values with the 13 low mantissa bits cleared (the TF32 operand)."""
+    return (t.view(torch.int32) & ~0x1FFF).view(torch.float32)
+
+
+@pytest.mark.parametrize("M,N,K,batch,sym", [
+    (128, 128, 32, 1, False), (256, 384, 200, 2, False), (200, 200, 200, 1, True), (384, 384, 520, 2, True)])
+def test_product_tf32(mg, M, N, K, batch, sym):
+    A = _rand((batch, M, K), torch.float32, 9)
+    B = A if sym else _rand((batch, N, K), torch.float32, 10)
+    C = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    mg.muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=sym, tf32=True)
+    torch.cuda.synchronize()
+    exact = torch.matmul(A.double(), B.double().transpose(1, 2))
+    err = ((C.double() - exact).norm() / exact.norm()).item()
+    assert err < 2e-3, err                      # TF32 operands: 10-bit mantissa
+    if sym:
+        assert torch.equal(C, C.transpose(1, 2))
+    # the product of the TF32 operands (low mantissa bits dropped or rounded
+    # off, whichever the hardware does) accumulated in fp32 matches closely
+    errs = []
+    for conv in (_tf32_trunc, _tf32_rne):
+        At, Bt = conv(A.contiguous()).double(), conv(B.contiguous()).double()
+        near = torch.matmul(At, Bt.transpose(1, 2))
+        errs.append(((C.double() - near).norm() / near.norm()).item())
+    assert min(errs) < 1e-5, errs
+
+
+def test_poly_tf32(mg):
+    m = 256
+    X = _rand((1, m, 3 * m), torch.float64, 11)
+    G = torch.matmul(X, X.transpose(1, 2))
+    G = (G / torch.linalg.matrix_norm(G, ord=2, keepdim=True)).float().contiguous()
+    P = torch.zeros_like(G)
+    a, b, c = 3.4445, -4.7750, 2.0315
+    mg.muon_debug_gemm(G, G, P, b_kmajor=True, symmetric=True, poly=(a, b, c), tf32=True)
+    torch.cuda.synchronize()
+    Gd = G.double()
+    ref = a * torch.eye(m, device="cuda", dtype=torch.float64) + b * Gd + c * torch.matmul(Gd, Gd)
+    err = ((P.double() - ref).norm() / ref.norm()).item()
+    assert err < 2e-3, err
