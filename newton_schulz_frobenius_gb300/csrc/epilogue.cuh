@@ -78,48 +78,91 @@ __device__ __forceinline__ void store_row_run(void* base, int64_t off, const flo
     }
 }
 
+// Loads W contiguous values (all < N, row < M) into v, with 16-byte vector
+// loads when the address allows it.
+template <int W>
+__device__ __forceinline__ void load_row_run(const void* base, int64_t off, float (&v)[W], int dtype) {
+    if (dtype == MUON_BF16) {
+        const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(base) + off;
+        if ((W % 8) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < W; j += 8) {
+                const uint4 u = *reinterpret_cast<const uint4*>(p + j);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[k]));
+                    v[j + 2 * k] = f.x;
+                    v[j + 2 * k + 1] = f.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = __bfloat162float(p[j]);
+        }
+    } else {
+        const float* p = reinterpret_cast<const float*>(base) + off;
+        if ((W % 4) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < W; j += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(p + j);
+                v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = p[j];
+        }
+    }
+}
+
+// One thread, one row r, columns c0 .. c0+W-1.  Every global load of a chunk
+// is issued before its first store (the caller's W is both read and written,
+// so a load placed after a store to it could not be moved ahead of it).
+// Row runs use 16-byte vector accesses; the mirrored half of a symmetric
+// product and the caller's matrix of a tall (transposed) bucket are written
+// column by column, which is coalesced across the 32 lanes of a warp because
+// the lanes of a tensor-core epilogue warp own 32 consecutive rows.
 template <int W>
 __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, int c0, float (&v)[W]) {
     if (r >= a.M) return;
     const float s = epi_alpha(a, b);
     const int nvalid = min(W, a.N - c0);
     if (nvalid <= 0) return;
+#pragma unroll
+    for (int j = 0; j < W; ++j) v[j] *= s;
 
     if (a.epi == EPI_STORE || a.epi == EPI_POLY) {
         const int64_t cbase = (int64_t)b * a.strideC;
         const int cd = a.c_dtype;
         if (a.epi == EPI_POLY) {
-            const int64_t gbase = (int64_t)b * a.strideG + (int64_t)r * a.ldg + c0;
+            float g[W];
+            const int64_t goff = (int64_t)b * a.strideG + (int64_t)r * a.ldg + c0;
+            if (nvalid == W) {
+                load_row_run<W>(a.Gin, goff, g, a.dtype);
+            } else {
 #pragma unroll
-            for (int j = 0; j < W; ++j) {
-                if (j < nvalid) {
-                    float g = ld_elem(a.Gin, gbase + j, a.dtype);
-                    v[j] = a.pc * (s * v[j]) + a.pb * g + ((c0 + j) == r ? a.pa : 0.f);
-                }
+                for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(a.Gin, goff + j, a.dtype) : 0.f;
             }
-        } else {
 #pragma unroll
-            for (int j = 0; j < W; ++j) v[j] *= s;
+            for (int j = 0; j < W; ++j) v[j] = a.pc * v[j] + a.pb * g[j] + ((c0 + j) == r ? a.pa : 0.f);
         }
         if (a.round_tf32) {
 #pragma unroll
             for (int j = 0; j < W; ++j) v[j] = round_tf32(v[j]);
         }
-        if (a.symmetric) {
-#pragma unroll
-            for (int j = 0; j < W; ++j) {
-                const int c = c0 + j;
-                if (j < nvalid && c <= r) {
-                    st_elem(a.C, cbase + (int64_t)r * a.ldc + c, v[j], cd);
-                    if (c < r) st_elem(a.C, cbase + (int64_t)c * a.ldc + r, v[j], cd);
-                }
-            }
-        } else if (nvalid == W) {
-            store_row_run<W>(a.C, cbase + (int64_t)r * a.ldc + c0, v, cd);
+        const int64_t roff = cbase + (int64_t)r * a.ldc + c0;
+        const bool full_row = (nvalid == W) && (!a.symmetric || c0 + W - 1 <= r);
+        if (full_row) {
+            store_row_run<W>(a.C, roff, v, cd);
         } else {
 #pragma unroll
             for (int j = 0; j < W; ++j)
-                if (j < nvalid) st_elem(a.C, cbase + (int64_t)r * a.ldc + c0 + j, v[j], cd);
+                if (j < nvalid && (!a.symmetric || c0 + j <= r)) st_elem(a.C, roff + j, v[j], cd);
+        }
+        if (a.symmetric) {
+#pragma unroll
+            for (int j = 0; j < W; ++j)
+                if (j < nvalid && c0 + j < r) st_elem(a.C, cbase + (int64_t)(c0 + j) * a.ldc + r, v[j], cd);
         }
         return;
     }
@@ -127,148 +170,42 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
     // EPI_UPDATE / EPI_OUT: caller matrices through the table.
     const MatEntry e = a.mats[b];
     const int od = a.out_dtype;
-    if (a.epi == EPI_OUT) {
-        if (!e.trans) {
-#pragma unroll
-            for (int j = 0; j < W; ++j) v[j] *= s;
-            if (nvalid == W) {
-                store_row_run<W>(e.w, (int64_t)r * a.N + c0, v, od);
-            } else {
-#pragma unroll
-                for (int j = 0; j < W; ++j)
-                    if (j < nvalid) st_elem(e.w, (int64_t)r * a.N + c0 + j, v[j], od);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < W; ++j)
-                if (j < nvalid) st_elem(e.w, (int64_t)(c0 + j) * a.M + r, s * v[j], od);
-        }
-        return;
-    }
-    // EPI_UPDATE: W' = W (1 - lr wd) - lr * scale * O
-    const float keep = 1.0f - a.lr * a.wd;
-    const float step = a.lr * a.scale * s;
-    if (!e.trans) {
-        const int64_t off = (int64_t)r * a.N + c0;
-        float w[W];
-#pragma unroll
-        for (int j = 0; j < W; ++j) w[j] = (j < nvalid) ? ld_elem(e.w, off + j, od) : 0.f;
-#pragma unroll
-        for (int j = 0; j < W; ++j) w[j] = fmaf(-step, v[j], keep * w[j]);
-        if (nvalid == W) {
-            store_row_run<W>(e.w, off, w, od);
-        } else {
-#pragma unroll
-            for (int j = 0; j < W; ++j)
-                if (j < nvalid) st_elem(e.w, off + j, w[j], od);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < W; ++j) {
-            if (j < nvalid) {
-                const int64_t off = (int64_t)(c0 + j) * a.M + r;
-                const float w = ld_elem(e.w, off, od);
-                st_elem(e.w, off, fmaf(-step, v[j], keep * w), od);
-            }
-        }
-    }
-}
-
-}  // namespace muon
-
-namespace muon {
-
-// Tensor-core epilogue for one warp and one 32 x 32 chunk: lane l holds row
-// r0 + l, columns c0 .. c0+31 (one tcgen05.ld).  The chunk is staged through
-// shared memory (stage: 32 x 33 floats owned by this warp) so that every
-// global access is a 32-lane run along a row of its matrix:
-//   row phase     lane l handles column c0 + l of rows r0 .. r0+31
-//                 (row-major stores, the polynomial's G reads, the caller's
-//                 W / O in their own orientation)
-//   column phase  lane l handles row r0 + l of columns c0 .. c0+31
-//                 (the mirrored half of a symmetric product, and the caller's
-//                 W / O of a transposed (tall) matrix)
-__device__ __forceinline__ void epi_chunk_staged(const GemmArgs& a, int b, int r0, int c0, const float (&v)[32],
-                                                 float (*stage)[33]) {
-    const int lane = threadIdx.x & 31;
-    const float s = epi_alpha(a, b);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) stage[lane][j] = s * v[j];
-    __syncwarp();
-
-    const int col = c0 + lane;
-    const bool col_ok = col < a.N;
-    const int epi = a.epi;
-    if (epi == EPI_STORE || epi == EPI_POLY) {
-        const int64_t cbase = (int64_t)b * a.strideC;
-        const int cd = a.c_dtype;
-        for (int i = 0; i < 32; ++i) {
-            const int row = r0 + i;
-            if (row >= a.M) break;
-            if (!col_ok) continue;
-            float val = stage[i][lane];
-            if (epi == EPI_POLY) {
-                const float g = ld_elem(a.Gin, (int64_t)b * a.strideG + (int64_t)row * a.ldg + col, a.dtype);
-                val = a.pc * val + a.pb * g + (row == col ? a.pa : 0.f);
-            }
-            if (a.round_tf32) val = round_tf32(val);
-            stage[i][lane] = val;
-            if (!a.symmetric || col <= row) st_elem(a.C, cbase + (int64_t)row * a.ldc + col, val, cd);
-        }
-        if (a.symmetric) {
-            __syncwarp();
-            const int r = r0 + lane;
-            if (r < a.M) {
-                for (int j = 0; j < 32; ++j) {
-                    const int c = c0 + j;
-                    if (c >= r || c >= a.N) break;   // only strictly below the diagonal
-                    st_elem(a.C, cbase + (int64_t)c * a.ldc + r, stage[lane][j], cd);
-                }
-            }
-        }
-        __syncwarp();
-        return;
-    }
-
-    const MatEntry e = a.mats[b];
-    const int od = a.out_dtype;
     const float keep = 1.0f - a.lr * a.wd;
     const float step = a.lr * a.scale;
     if (!e.trans) {
-        // caller matrix is m x n, row-major: row phase
-        for (int i = 0; i < 32; ++i) {
-            const int row = r0 + i;
-            if (row >= a.M) break;
-            if (!col_ok) continue;
-            const int64_t off = (int64_t)row * a.N + col;
-            const float o = stage[i][lane];
-            if (epi == EPI_OUT) {
-                st_elem(e.w, off, o, od);
+        const int64_t off = (int64_t)r * a.N + c0;
+        if (a.epi == EPI_UPDATE) {
+            float w[W];
+            if (nvalid == W) {
+                load_row_run<W>(e.w, off, w, od);
             } else {
-                const float w = ld_elem(e.w, off, od);
-                st_elem(e.w, off, fmaf(-step, o, keep * w), od);
+#pragma unroll
+                for (int j = 0; j < W; ++j) w[j] = (j < nvalid) ? ld_elem(e.w, off + j, od) : 0.f;
             }
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * w[j]);
+        }
+        if (nvalid == W) {
+            store_row_run<W>(e.w, off, v, od);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j)
+                if (j < nvalid) st_elem(e.w, off + j, v[j], od);
         }
     } else {
-        // caller matrix is n x m (tall): element (row, col) of the oriented
-        // matrix lives at col * m + row; column phase keeps lanes on a run
-        const int r = r0 + lane;
-        if (r < a.M) {
-            for (int j = 0; j < 32; ++j) {
-                const int c = c0 + j;
-                if (c >= a.N) break;
-                const int64_t off = (int64_t)c * a.M + r;
-                const float o = stage[lane][j];
-                if (epi == EPI_OUT) {
-                    st_elem(e.w, off, o, od);
-                } else {
-                    const float w = ld_elem(e.w, off, od);
-                    st_elem(e.w, off, fmaf(-step, o, keep * w), od);
-                }
-            }
+        // caller matrix is n x m: oriented (r, c) lives at c * m + r
+        if (a.epi == EPI_UPDATE) {
+            float w[W];
+#pragma unroll
+            for (int j = 0; j < W; ++j) w[j] = (j < nvalid) ? ld_elem(e.w, (int64_t)(c0 + j) * a.M + r, od) : 0.f;
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * w[j]);
         }
+#pragma unroll
+        for (int j = 0; j < W; ++j)
+            if (j < nvalid) st_elem(e.w, (int64_t)(c0 + j) * a.M + r, v[j], od);
     }
-    __syncwarp();
 }
 
 }  // namespace muon
+

@@ -48,8 +48,7 @@ struct Cfg {
     static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int EPI_STAGE_BYTES = 4 * 32 * 33 * 4;   // one 32 x 33 fp32 chunk per epilogue warp
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
 };
 
 // ---------------------------------------------------------------------------
@@ -265,8 +264,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::A_BYTES;
-    float* epi_stage = reinterpret_cast<float*>(sB + S * C::B_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_stage) + C::EPI_STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -402,7 +400,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;   // TMEM lane quarter this warp may access
-        float (*stage)[33] = reinterpret_cast<float (*)[33]>(epi_stage + (warp - 2) * 32 * 33);
         int acc = 0;
         uint32_t aphase = 0;
         for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
@@ -421,7 +418,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (args.symmetric && col0 > warp_row_max) continue;
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-                epi_chunk_staged(args, b, row0, col0, v, stage);
+                epi_row_chunk<32>(args, b, row0 + lane, col0, v);
             }
             tc_fence_before();
             __syncwarp();
