@@ -80,6 +80,34 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
                           int num_segments, void* stream);
 
 /*
+ * muon_ns_orthogonalize for callers that must not allocate device memory.
+ * The pages have no counterpart: this entry point exists for code that runs
+ * where device memory belongs to someone else's allocator (a framework's
+ * caching pool, a fixed per-job memory budget) or where allocation after
+ * start-up is forbidden (a real-time training loop).  It computes the same
+ * result with the same arguments and conventions as muon_ns_orthogonalize,
+ * but inside one fixed 64 MiB array compiled into the library (every GPU that
+ * loads the library holds it until the process exits) and it calls no
+ * cudaMalloc, cudaFree, cudaMallocHost or other allocating routine.
+ *   - The status word, the matrix table and the NS buffers of the whole batch
+ *     must fit in the 64 MiB: one 1024 x 4096 bf16 matrix, 31 of 256 x 1024
+ *     bf16, 127 of 128 x 512 bf16 (2048 x 2048 does not fit).  A call that
+ *     does not fit returns
+ *     MUON_EINVAL (see muon_last_error_message) and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call reuses the same array, which keeps the last call's contents;
+ *     calls that overlap on the GPU (two streams, or two host threads) race.
+ *   - Device-detected errors go to a status word inside the array, not to the
+ *     one muon_sync_status reads; a non-finite input gives a non-finite output.
+ *   - With muon_set_kernel_timing(1) the timing records create CUDA events.
+ */
+int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype,
+                                  const float coeffs[3], int steps, const int* segments,
+                                  int num_segments, void* stream);
+
+/*
  * One Muon step over `count` matrices (the optimizer call the pages' drop-in
  * API names the participating matrices for: "DMuon" news page, section 3;
  * "MuonX" page, section 3.3).

@@ -33,7 +33,7 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 
 #: every entry point include/muon.h declares
 EXPORTS = (
-    "muon_ns_orthogonalize", "muon_step", "muon_set_ns_config", "muon_autotune",
+    "muon_ns_orthogonalize", "muon_ns_orthogonalize_noalloc", "muon_step", "muon_set_ns_config", "muon_autotune",
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
     dp = ctypes.POINTER(ctypes.c_double)
     sig = {
         "muon_ns_orthogonalize": (i32, [vp, i64, i64, i64, i32, f3, i32, ip, i32, vp]),
+        "muon_ns_orthogonalize_noalloc": (i32, [vp, i64, i64, i64, i32, f3, i32, ip, i32, vp]),
         "muon_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), i64p, i64p, i64,
                             i32, i32, f32, f32, f32, i32, vp]),
         "muon_set_ns_config": (i32, [f3, i32, ip, i32, i32]),
@@ -149,6 +150,23 @@ def muon_ns_orthogonalize(x, coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1),
     segs, nseg = _ints(segments)
     _check(lib().muon_ns_orthogonalize(x.data_ptr(), m, n, batch, _dtype_code(x), c, steps, segs, nseg,
                                        _stream_ptr(stream)), "muon_ns_orthogonalize")
+    return x
+
+
+def muon_ns_orthogonalize_noalloc(x, coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1), stream=None):
+    """Same as muon_ns_orthogonalize, inside the library's fixed 64 MiB scratch
+    array: no device memory is allocated (for callers that may not allocate)."""
+    _cuda_contig(x, "x")
+    if x.dim() == 2:
+        batch, m, n = 1, x.shape[0], x.shape[1]
+    elif x.dim() == 3:
+        batch, m, n = x.shape
+    else:
+        raise ValueError("x must be 2-D or 3-D")
+    c = (ctypes.c_float * 3)(*coeffs)
+    segs, nseg = _ints(segments)
+    _check(lib().muon_ns_orthogonalize_noalloc(x.data_ptr(), m, n, batch, _dtype_code(x), c, steps, segs, nseg,
+                                               _stream_ptr(stream)), "muon_ns_orthogonalize_noalloc")
     return x
 
 
