@@ -15,8 +15,10 @@
 //               STAGES-deep ring of (A, B) tiles guarded by full/empty mbarriers
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //               (M = 128, N = BN, K = 16 per instruction, fp32 accumulator)
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, fused epilogue from
-//               epilogue.cuh, global stores
+//   warps 2-9   epilogue: two warps per TMEM lane quarter, each draining half
+//               of the tile's columns with tcgen05.ld 32 at a time, fused
+//               epilogue from epilogue.cuh; while the main loop of a tile runs
+//               they prefetch into L2 the caller data their epilogue will read
 // Operand kinds: bf16 (kind::f16, K = 16 per instruction) for the long
 // products, TF32 on fp32 storage (kind::tf32, K = 8) for the m x m Gram-space
 // products; either way one k-block is 128 bytes of every operand row.
@@ -38,7 +40,8 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;            // bf16 elements per k-block = 128 bytes: one swizzle row
 constexpr int BK_BYTES = 128;
-constexpr int NTHREADS = 192;
+constexpr int NEPI = 8;                        // epilogue warps
+constexpr int NTHREADS = 64 + 32 * NEPI;
 
 template <int BN>
 struct Cfg {
@@ -119,6 +122,10 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer() - t0 > WAIT_LIMIT_NS) return;
     }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -284,8 +291,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         mbar_init(accf0, 1);
         mbar_init(accf0 + 8, 1);
-        mbar_init(acce0, 4);
-        mbar_init(acce0 + 8, 4);
+        mbar_init(acce0, NEPI);
+        mbar_init(acce0 + 8, NEPI);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -398,13 +405,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        // ---------------- epilogue (warps 2..9) ----------------
+        const int q = warp & 3;                    // TMEM lane quarter this warp may access
+        const int half = (warp - 2) / 4;           // which half of the tile's columns
+        constexpr int HALF_COLS = BN / 2;
         int acc = 0;
         uint32_t aphase = 0;
         for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
             int b, tm, tn;
             sched.decode(t, b, tm, tn);
+            if (args.epi == EPI_UPDATE) {
+                // the update reads the caller's W: start pulling this tile's
+                // part into L2 while the products are still accumulating
+                const MatEntry e = args.mats[b];
+                const int r = tm * BM + q * 32 + lane;
+                const int cbeg = tn * BN + half * HALF_COLS;
+                const int ob = args.out_dtype == MUON_BF16 ? 2 : 4;
+                const char* wb = reinterpret_cast<const char*>(e.w);
+                if (!e.trans) {
+                    if (r < args.M)
+                        for (int c = cbeg; c < min(cbeg + HALF_COLS, args.N); c += 128 / ob)
+                            prefetch_l2(wb + ((int64_t)r * args.N + c) * ob);
+                } else {
+                    for (int c = cbeg + lane; c < min(cbeg + HALF_COLS, args.N); c += 32)
+                        prefetch_l2(wb + ((int64_t)c * args.M + tm * BM + q * 32) * ob);
+                }
+            }
             // every lane observes the barrier itself; the warp proceeds only together
             const bool ok = wait_bounded(accf0 + 8 * acc, aphase, abort_flag, args.status);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -412,7 +438,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int row0 = tm * BM + q * 32;
             const int warp_row_max = row0 + 31;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = half * (HALF_COLS / 32); ch < (half + 1) * (HALF_COLS / 32); ++ch) {
                 const int col0 = tn * BN + ch * 32;
                 if (col0 >= args.N) break;
                 if (args.symmetric && col0 > warp_row_max) continue;
