@@ -43,6 +43,21 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def combine_over_ranks(local_ms, dist, device):
+    """Slowest rank's step time (the job's step time); local value when not distributed."""
+    if dist is None:
+        return float(local_ms)
+    import torch
+    t = torch.tensor([float(local_ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(matrices_per_rank, world, step_ms):
+    """Whole-job matrices/s: every rank runs its own replica of the workload."""
+    return world * matrices_per_rank / (step_ms * 1e-3)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -283,35 +298,38 @@ def bench_gpu(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    mg.muon_kernel_timing_read()
-    mg.muon_set_kernel_timing(True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = mg.muon_launch_count()
-    for i in range(args.steps):
-        flush.zero_()                      # L2 flush, outside the step's events
-        evs[i][0].record()
-        mg.muon_step(params, grads, moms, **hp)
-        evs[i][1].record()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    launches = mg.muon_launch_count() - launches0
-    mg.muon_set_kernel_timing(False)
-    ktimes = mg.muon_kernel_timing_read()
+
+    def timed_pass(kernel_timing):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        mg.muon_kernel_timing_read()
+        mg.muon_set_kernel_timing(kernel_timing)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        l0 = mg.muon_launch_count()
+        for i in range(args.steps):
+            flush.zero_()                      # L2 flush, outside the step's events
+            evs[i][0].record()
+            mg.muon_step(params, grads, moms, **hp)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        mg.muon_set_kernel_timing(False)
+        return [a.elapsed_time(b) for a, b in evs], mg.muon_launch_count() - l0, mg.muon_kernel_timing_read()
+
+    # pass 1: the step as a user runs it (no per-launch instrumentation) -> value
+    step_ms, launches, _ = timed_pass(False)
+    # pass 2: same steps with per-launch CUDA events on the launching stream
+    # -> per-kernel times and the roofline of the dominant kernel
+    step_ms_instr, _, ktimes = timed_pass(True)
     clocks = sampler.stop()
     st = mg.muon_sync_status()
     if st != mg.MUON_OK:
         raise RuntimeError(f"device status after timed steps: {mg.status_str(st)}")
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(step_ms) / len(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.count / (ms * 1e-3)
+    ms = combine_over_ranks(sum(step_ms) / len(step_ms), dist, device)
+    value = job_throughput(wl.count, world, ms)
 
     # end to end through the public API: gradients from pinned host memory in,
     # updated weights back to pinned host memory, every step
@@ -330,11 +348,7 @@ def bench_gpu(args):
             hw.copy_(p, non_blocking=True)
         eev[i][1].record()
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = combine_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / e2e_steps, dist, device)
     h2d = sum(g.numel() * g.element_size() for g in grads)
     d2h = sum(p.numel() * p.element_size() for p in params)
 
@@ -342,7 +356,7 @@ def bench_gpu(args):
     # dominant kernel: the tensor-core product instance with the largest device time
     groups = {"gemm_tc_apply": ("gemm_tc_apply", "gemm_tc_apply_update"),
               "gemm_tc_syrk": ("gemm_tc_syrk",), "gemm_tc_square": ("gemm_tc_square",),
-              "gemm_fp32": ("gemm_fp32",)}
+              "gemm_fp32": ("gemm_fp32",), "small_ns_fused": ("small_ns_fused",)}
     best, best_ms, best_work, best_n = None, -1.0, 0.0, 0
     for gname, members in groups.items():
         tot = sum(ktimes.get(k, (0, 0.0, 0.0))[1] for k in members)
@@ -377,11 +391,13 @@ def bench_gpu(args):
         "roofline": roofline,
         "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
                         "work_per_launch": v[2] / max(v[0], 1),
-                        "rate": (v[2] / (v[1] * 1e-3) / (1e12 if k.startswith("gemm") else 1e9)) if v[1] else None,
-                        "rate_unit": "TFLOP/s" if k.startswith("gemm") else "GB/s"}
+                        "rate": (v[2] / (v[1] * 1e-3) / (1e12 if k.startswith(("gemm", "small")) else 1e9))
+                        if v[1] else None,
+                        "rate_unit": "TFLOP/s" if k.startswith(("gemm", "small")) else "GB/s"}
                     for k, v in ktimes.items()},
         "kernel_ms_per_step": step_total_kernel_ms,
-        "e2e": {"value": world * wl.count / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "ms_per_step_instrumented": sum(step_ms_instr) / len(step_ms_instr),
+        "e2e": {"value": job_throughput(wl.count, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "what": "gradients H2D from pinned host, muon_step, updated weights D2H to pinned host"},
         "gpu_launches": launches,

@@ -212,7 +212,7 @@ static thread_local int t_open = -1;   // index of the launch being recorded
 static const char* kclass_name(int k) {
     static const char* names[KC_COUNT] = {"prep_momentum_norm", "norm_finalize", "gemm_tc_syrk",
                                           "gemm_tc_square", "gemm_tc_apply", "gemm_tc_apply_update",
-                                          "gemm_fp32", "other"};
+                                          "gemm_fp32", "other", "small_ns_fused"};
     return (k >= 0 && k < KC_COUNT) ? names[k] : "other";
 }
 
@@ -285,10 +285,29 @@ struct NsPlan {
     std::vector<int> segs;
     int path;       // MUON_PATH_PLAIN or MUON_PATH_GRAM
     int tile_n;     // tensor-core N extent of the long products
+    int sym_tile_n; // tensor-core N extent of the symmetric products (128 or 256)
+    int gram_tf32;  // bf16 path: Gram-space matrices kept in TF32 (else bf16)
+    int fused;      // run the whole update of each matrix in one CTA (small_ns.cu)
 };
 
-static NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_segs, int path, int tile_n) {
+// Precision of the bf16 path's m x m Gram-space matrices (G, P, PG, Q).
+// A bit-faithful CPU simulation of the iteration against the exact one gives,
+// for the Gram path with bf16 Gram space, 0.8-1.2% relative error on every
+// shape with m >= 128 and n >= 2m, but 1.5-4% on square and near-square shapes
+// and 2.3% for m = 37; with TF32 Gram space all of them stay at or below 1.5%.
+// The plain path's error is set by the bf16 X (0.8-1.9% either way), so it
+// keeps bf16.  TF32 costs twice the operand bytes and half the tensor rate on
+// the m^3 products, so it is used only where bf16 is not accurate enough.
+static int gram_space_tf32(int path, int m, int n) {
+    return (path == MUON_PATH_GRAM && (m < 128 || n < 2 * m)) ? 1 : 0;
+}
+
+static NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_segs, int path, int tile_n,
+                        int m, int n, int sym_tile_n = 128) {
     NsPlan p;
+    p.sym_tile_n = sym_tile_n;
+    p.gram_tf32 = gram_space_tf32(path, m, n);
+    p.fused = 0;
     p.a = coeffs[0];
     p.b = coeffs[1];
     p.c = coeffs[2];
@@ -376,11 +395,9 @@ struct FinalEpi {
 // the chunk's X buffer, ending in `fin`.
 //
 // Precision of the bf16 path: X and the long products XX^T, QX are bf16 with
-// fp32 accumulation; the m x m Gram-space matrices G, P, PG, Q are kept as
-// TF32-rounded fp32 and multiplied on the TF32 tensor path; the transform that
-// is applied to X at a segment end is rounded to bf16.  With every Gram-space
-// matrix in bf16 instead, square and small inputs of the Gram path exceed a 2%
-// relative error against the exact iteration; with TF32 they stay near 1%.
+// fp32 accumulation; the m x m Gram-space matrices G, P, PG, Q are bf16, or,
+// where gram_space_tf32() asks for it, TF32-rounded fp32 multiplied on the
+// TF32 tensor path, with the transform applied to X rounded to bf16.
 static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
                   int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin) {
     char* X = base + L.off_X;
@@ -392,11 +409,12 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
     const int64_t strideM = (int64_t)m * L.ldm;
 
     const bool bf = (dtype == MUON_BF16);
-    const int sq_dtype = bf ? DT_TF32 : MUON_F32;     // Gram-space operands
+    const bool tf = bf && plan.gram_tf32;
+    const int sq_dtype = bf ? (tf ? DT_TF32 : MUON_BF16) : MUON_F32;   // Gram-space operands
     auto gram_out = [&](GemmArgs& g, bool feeds_apply) {
-        // Gram-space result: TF32-rounded fp32, or bf16 when it is the
-        // transform the long apply consumes (bf16 path only)
-        if (!bf) return;
+        // TF32 Gram space: TF32-rounded fp32, or bf16 when it is the
+        // transform the long apply consumes; otherwise the path's own dtype
+        if (!tf) return;
         if (feeds_apply) { g.c_dtype = MUON_BF16; g.round_tf32 = 0; }
         else { g.c_dtype = MUON_F32; g.round_tf32 = 1; }
     };
@@ -408,6 +426,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
         g.symmetric = 1;
         g.epi = EPI_STORE;
         g.C = C; g.ldc = L.ldm; g.strideC = strideM;
+        g.tile_n = plan.sym_tile_n;
         gram_out(g, feeds_apply);
         return g;
     };
@@ -427,6 +446,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
             g.symmetric = 1;
             g.epi = EPI_STORE;
             g.C = G; g.ldc = L.ldm; g.strideC = strideM;
+            g.tile_n = plan.sym_tile_n;
             gram_out(g, false);
             if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 1; }
             int r = run_gemm(dc, s, g, KC_SYRK);
@@ -537,6 +557,8 @@ struct TuneEntry {
     int path;
     int tile_n;
     double ms_per_matrix;
+    int fused;
+    int sym_tile_n;
 };
 using TuneKey = std::tuple<std::string, int, int, int64_t, int64_t, int>;   // device, sms, cudart, m, n, dtype
 static std::map<TuneKey, TuneEntry> g_tune;
@@ -560,30 +582,88 @@ static bool env_flag(const char* name, bool dflt) {
 
 static int save_tune_file(const char* path);
 
+// Whether the one-CTA-per-matrix kernel can run this plan (bf16, m <= 128,
+// n <= 512, segments of length <= 2, bf16 Gram space).  MUON_SMALL=0 turns it off.
+static bool small_eligible(const NsPlan& p, int m, int n, int dtype) {
+    if (dtype != MUON_BF16 || p.gram_tf32 || !env_flag("MUON_SMALL", true)) return false;
+    return small_ns_fits(m, n, (int)p.segs.size(), p.segs.data());
+}
+
+__global__ void table_fill_kernel(MatEntry* t, char* base, int64_t stride_bytes, int trans, int batch) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) {
+        char* p = base + (int64_t)b * stride_bytes;
+        t[b] = MatEntry{p, nullptr, p, trans, 0};
+    }
+}
+
+static SmallArgs small_args(const NsPlan& p, const MatEntry* mats, int B, int m, int n, int mode, int param_dtype,
+                            int mom_dtype, int nesterov, float beta, float lr, float wd, bool vec_ok, int* status) {
+    SmallArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.mats = mats;
+    a.batch = B; a.m = m; a.n = n;
+    a.mode = mode;
+    a.param_dtype = param_dtype; a.mom_dtype = mom_dtype;
+    a.nesterov = nesterov;
+    a.beta = beta; a.lr = lr; a.wd = wd;
+    a.scale = 0.2f * std::sqrt((float)n);
+    a.a = p.a; a.b = p.b; a.c = p.c;
+    a.nseg = (int)p.segs.size();
+    for (int i = 0; i < a.nseg && i < 16; ++i) a.segs[i] = p.segs[i];
+    a.vec_ok = vec_ok ? 1 : 0;
+    a.status = status;
+    return a;
+}
+
+// Algorithmic FLOPs of one NS update under this plan (symmetric results half).
+static double plan_alg_flops(const NsPlan& p, int m, int n) {
+    const double M = m, N = n;
+    double f = 0.0;
+    for (int L : p.segs) {
+        f += M * M * N;                 // X X^T
+        f += L * M * M * M;             // one G^2 per iteration
+        f += (L - 1) * 3.0 * M * M * M; // P Q, P G and (P G) P for every further iteration
+        f += 2.0 * M * M * N;           // Q X
+    }
+    return f;
+}
+
+static int run_small(const DevCtx& dc, cudaStream_t s, const SmallArgs& a, double alg_flops) {
+    note_launch_begin(KC_SMALL, s);
+    cudaError_t e = launch_small_ns(a, dc.sms, s);
+    note_launch_end(KC_SMALL, alg_flops, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fused small-matrix launch");
+    return MUON_OK;
+}
+
 static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int B, const NsConfig& cfg,
                           TuneEntry* out) {
     const ChunkLayout L = chunk_layout(m, n, B, dtype);
+    const size_t table_off = align_up(L.total, 256);
     Workspace* w = nullptr;
-    int r = ws_get(dc.device, s, L.total, &w);
+    int r = ws_get(dc.device, s, table_off + align_up(sizeof(MatEntry) * (size_t)B, 256), &w);
     if (r) return r;
     char* base = w->base;
 
-    std::vector<std::pair<int, int>> cands;   // (path, tile_n)
+    struct Cand { int path, tile_n, sym_tile_n; };
+    std::vector<Cand> cands;
     const int tiles[2] = {256, 128};
     const int ntiles = (dtype == MUON_BF16) ? 2 : 1;
-    for (int ti = 0; ti < ntiles; ++ti) {
-        cands.push_back({MUON_PATH_PLAIN, tiles[ti]});
-        if (!cfg.segments.empty()) cands.push_back({MUON_PATH_GRAM, tiles[ti]});
-    }
+    for (int ti = 0; ti < ntiles; ++ti)
+        for (int si = 0; si < ntiles; ++si) {
+            cands.push_back({MUON_PATH_PLAIN, tiles[ti], tiles[1 - si]});
+            if (!cfg.segments.empty()) cands.push_back({MUON_PATH_GRAM, tiles[ti], tiles[1 - si]});
+        }
     cudaEvent_t e0, e1;
     MUON_CUDA(cudaEventCreate(&e0));
     MUON_CUDA(cudaEventCreate(&e1));
     FinalEpi fin{EPI_STORE, nullptr, dtype, 0.f, 0.f, 0.f};
     const float scale = std::sqrt(3.0f / ((float)m * (float)n));
-    TuneEntry best{MUON_PATH_PLAIN, 256, 1e300};
+    TuneEntry best{MUON_PATH_PLAIN, 256, 1e300, 0, 128};
     const int reps = 3;
     for (auto& c : cands) {
-        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, c.first, c.second);
+        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, c.path, c.tile_n, m, n, c.sym_tile_n);
         std::vector<float> times;
         for (int rep = 0; rep <= reps; ++rep) {
             cudaError_t e = launch_fill_synthetic(base + L.off_X, (int64_t)B * m * L.ldx, dtype, scale,
@@ -600,8 +680,37 @@ static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dt
         }
         std::sort(times.begin(), times.end());
         const double med = times[times.size() / 2] / B;
-        logf(2, "autotune %dx%d dtype %d path %d tile %d: %.4f ms/matrix", m, n, dtype, c.first, c.second, med);
-        if (med < best.ms_per_matrix) best = TuneEntry{c.first, c.second, med};
+        logf(2, "autotune %dx%d dtype %d path %d tile %d sym tile %d: %.4f ms/matrix", m, n, dtype, c.path,
+             c.tile_n, c.sym_tile_n, med);
+        if (med < best.ms_per_matrix) best = TuneEntry{c.path, c.tile_n, med, 0, c.sym_tile_n};
+    }
+    // the one-CTA-per-matrix kernel, on B synthetic matrices stored contiguously
+    for (int path : {MUON_PATH_PLAIN, MUON_PATH_GRAM}) {
+        if (path == MUON_PATH_GRAM && cfg.segments.empty()) continue;
+        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, 256, m, n);
+        if (!small_eligible(plan, m, n, dtype)) continue;
+        MatEntry* table = reinterpret_cast<MatEntry*>(base + table_off);
+        char* mats = base + L.off_X2;
+        table_fill_kernel<<<(B + 127) / 128, 128, 0, s>>>(table, mats, (int64_t)m * n * 2, 0, B);
+        MUON_CUDA(cudaGetLastError());
+        const SmallArgs sa = small_args(plan, table, B, m, n, 1, MUON_BF16, MUON_BF16, 0, 0.f, 0.f, 0.f,
+                                        (m % 8 == 0) && (n % 8 == 0), dc.status);
+        std::vector<float> times;
+        for (int rep = 0; rep <= reps; ++rep) {
+            cudaError_t e = launch_fill_synthetic(mats, (int64_t)B * m * n, dtype, scale, 0x5eed0000u + (uint32_t)rep, s);
+            if (e != cudaSuccess) return cuda_fail(e, "fill launch");
+            MUON_CUDA(cudaEventRecord(e0, s));
+            if ((r = run_small(dc, s, sa, 0.0))) return r;
+            MUON_CUDA(cudaEventRecord(e1, s));
+            MUON_CUDA(cudaEventSynchronize(e1));
+            float ms = 0.f;
+            MUON_CUDA(cudaEventElapsedTime(&ms, e0, e1));
+            if (rep > 0) times.push_back(ms);
+        }
+        std::sort(times.begin(), times.end());
+        const double med = times[times.size() / 2] / B;
+        logf(2, "autotune %dx%d fused path %d: %.4f ms/matrix", m, n, path, med);
+        if (med < best.ms_per_matrix) best = TuneEntry{path, 256, med, 1, 128};
     }
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
@@ -619,7 +728,7 @@ static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype
     }
     if (path == MUON_PATH_GRAM && cfg.segments.empty()) path = MUON_PATH_PLAIN;
     const TuneKey key = tune_key(dc, m, n, dtype);
-    TuneEntry ent{-1, 256, 0.0};
+    TuneEntry ent{-1, 256, 0.0, 0, 128};
     bool have = false;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -646,7 +755,11 @@ static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype
         }
     }
     const int tile_n = (have && ent.path == path) ? ent.tile_n : 256;
-    *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n);
+    const int sym_tile_n = (have && ent.path == path) ? ent.sym_tile_n : 128;
+    *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n, m, n, sym_tile_n);
+    // the fused small-matrix kernel: as measured, else whenever it applies
+    const bool measured = have && ent.path == path;
+    plan->fused = small_eligible(*plan, m, n, dtype) && (measured ? ent.fused != 0 : true);
     return MUON_OK;
 }
 
@@ -654,14 +767,15 @@ static int save_tune_file(const char* path) {
     std::lock_guard<std::mutex> lk(g_mu);
     std::ofstream f(path);
     if (!f) return fail(MUON_EINVAL, "cannot write tune cache %s", path);
-    f << "muon-tune v1\n";
+    f << "muon-tune v3\n";
     int nwritten = 0;
     for (auto& kv : g_tune) {
         std::string dev = std::get<0>(kv.first);
         std::replace(dev.begin(), dev.end(), '\t', ' ');
         f << dev << '\t' << std::get<1>(kv.first) << '\t' << std::get<2>(kv.first) << '\t' << std::get<3>(kv.first)
           << '\t' << std::get<4>(kv.first) << '\t' << std::get<5>(kv.first) << '\t' << kv.second.path << '\t'
-          << kv.second.tile_n << '\t' << kv.second.ms_per_matrix << '\n';
+          << kv.second.tile_n << '\t' << kv.second.ms_per_matrix << '\t' << kv.second.fused << '\t'
+          << kv.second.sym_tile_n << '\n';
         ++nwritten;
     }
     return nwritten;
@@ -747,9 +861,28 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
         auto it = g_tune.find(tune_key(dc, om, on, dtype));
         if (it != g_tune.end() && it->second.path == path) tile_n = it->second.tile_n;
     }
-    NsPlan plan = make_plan(coeffs, steps, segs, path, tile_n);
+    NsPlan plan = make_plan(coeffs, steps, segs, path, tile_n, om, on);
 
     const size_t es = esize(dtype);
+    if (small_eligible(plan, om, on, dtype) && batch <= (1 << 20)) {
+        const size_t tb = align_up(sizeof(MatEntry) * (size_t)batch, 256);
+        Workspace* w = nullptr;
+        if ((r = ws_get(dc.device, s, tb, &w))) return r;
+        std::vector<MatEntry> h((size_t)batch);
+        for (int64_t b = 0; b < batch; ++b) {
+            char* p = static_cast<char*>(ptr) + (size_t)b * m * n * es;
+            h[b] = MatEntry{p, nullptr, p, trans, 0};
+        }
+        MatEntry* d_table = reinterpret_cast<MatEntry*>(w->base);
+        if ((r = upload_table(*w, h, d_table, s))) return r;
+        const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
+        const SmallArgs sa = small_args(plan, d_table, (int)batch, om, on, 1, dtype, dtype, 0, 0.f, 0.f, 0.f, vec_ok,
+                                        dc.status);
+        if ((r = run_small(dc, s, sa, plan_alg_flops(plan, om, on) * (double)batch))) return r;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_last_path[{om, on, dtype}] = path;
+        return MUON_OK;
+    }
     const size_t per = chunk_layout(om, on, 1, dtype).total;
     const int chunk = budget_bytes_chunk(per, (int)std::min<int64_t>(batch, 65535));
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)batch, 256);
@@ -827,6 +960,10 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
         const int m = keys[k].first, n = keys[k].second;
         const int cnt = (int)buckets[keys[k]].size();
         if ((r = choose_plan(dc, s, m, n, param_dtype, cnt, cfg, &plans[k]))) return r;
+        if (plans[k].fused) {
+            chunks[k] = cnt;            // one launch, no workspace beyond the table
+            continue;
+        }
         chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, param_dtype).total, cnt);
         chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], param_dtype).total);
     }
@@ -852,6 +989,15 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
             vec_ok = vec_ok && (reinterpret_cast<uintptr_t>(grads[i]) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(moms[i]) % 16 == 0);
         const float scale = 0.2f * std::sqrt((float)n);
+        if (plans[k].fused) {
+            const SmallArgs sa = small_args(plans[k], d_table + first, (int)idx.size(), m, n, 0, param_dtype,
+                                            mom_dtype, nesterov, beta, lr, wd, vec_ok, dc.status);
+            if ((r = run_small(dc, s, sa, plan_alg_flops(plans[k], m, n) * (double)idx.size()))) return r;
+            first += idx.size();
+            std::lock_guard<std::mutex> lk(g_mu);
+            g_last_path[{m, n, param_dtype}] = plans[k].path;
+            continue;
+        }
         for (size_t c0 = 0; c0 < idx.size(); c0 += chunks[k]) {
             const int B = (int)std::min<size_t>(chunks[k], idx.size() - c0);
             const ChunkLayout L = chunk_layout(m, n, B, param_dtype);
@@ -908,7 +1054,7 @@ int muon_tune_load(const char* path) {
     std::ifstream f(path);
     if (!f) return 0;
     std::string line;
-    if (!std::getline(f, line) || line != "muon-tune v1") return 0;
+    if (!std::getline(f, line) || line != "muon-tune v3") return 0;
     DevCtx dc;
     int r = get_dev(dc);
     if (r) return r;
@@ -919,18 +1065,22 @@ int muon_tune_load(const char* path) {
         std::string dev, tok;
         std::vector<std::string> cols;
         while (std::getline(ss, tok, '\t')) cols.push_back(tok);
-        if (cols.size() != 9) continue;
+        if (cols.size() != 11) continue;
         try {
             const int sms = std::stoi(cols[1]), cuv = std::stoi(cols[2]);
             const int64_t m = std::stoll(cols[3]), n = std::stoll(cols[4]);
             const int dt = std::stoi(cols[5]), path = std::stoi(cols[6]), tile = std::stoi(cols[7]);
             const double ms = std::stod(cols[8]);
+            const int fused = std::stoi(cols[9]);
+            const int sym_tile = std::stoi(cols[10]);
+            if (fused != 0 && fused != 1) continue;
+            if (sym_tile != 128 && sym_tile != 256) continue;
             if (cols[0] != dc.name || sms != dc.sms || cuv != cv) continue;          // stale: other device/runtime
             if (m < 1 || n < m || !valid_dtype(dt)) continue;
             if (path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM) continue;
             if (tile != 128 && tile != 256) continue;
             std::lock_guard<std::mutex> lk(g_mu);
-            g_tune[TuneKey{dc.name, sms, cuv, m, n, dt}] = TuneEntry{path, tile, ms};
+            g_tune[TuneKey{dc.name, sms, cuv, m, n, dt}] = TuneEntry{path, tile, ms, fused, sym_tile};
             ++loaded;
         } catch (...) {
             continue;   // corrupt line
@@ -1081,7 +1231,7 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
     g.symmetric = symmetric ? 1 : 0;
     g.alpha = alpha;
     g.C = C; g.ldc = N; g.strideC = M * N;
-    g.tile_n = tile_n ? tile_n : 256;
+    g.tile_n = tile_n;   // 0: the launcher's default for the product kind
     if (poly) {
         g.epi = EPI_POLY;
         g.Gin = A; g.ldg = K; g.strideG = M * K;
@@ -1203,7 +1353,7 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
 
     const int path = num_segments > 0 ? MUON_PATH_GRAM : MUON_PATH_PLAIN;
     std::vector<int> segs(segments, segments + num_segments);
-    NsPlan plan = make_plan(coeffs, steps, segs, path, 256);
+    NsPlan plan = make_plan(coeffs, steps, segs, path, 256, om, on);
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
     if ((r = run_prep(dc, s, cbase, L, om, on, (int)batch, d_table, dtype, dtype, dtype, false, 0, 0.f, vec_ok)))
         return r;

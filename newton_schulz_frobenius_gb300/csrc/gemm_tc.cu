@@ -48,7 +48,7 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = (BN == 256) ? 4 : 7;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
@@ -234,13 +234,24 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Tile order within one matrix.  sym == 0: all tiles, row blocks fastest.
+// sym == 1: square 128 x 128 tiles with tn <= tm (lower triangle).
+// sym == 2: 128 x 256 tiles that meet the lower triangle, tn <= tm / 2; row
+// blocks 2p and 2p+1 both hold p + 1 tiles, so p(p+1) tiles precede block 2p.
 struct TileSched {
     int tiles_m, tiles_n, per_batch, total, sym;
 
     __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn) const {
         b = t / per_batch;
         const int l = t - b * per_batch;
-        if (sym) {
+        if (sym == 2) {
+            int p = (int)((sqrtf(4.0f * (float)l + 1.0f) - 1.0f) * 0.5f);
+            while (p * (p + 1) > l) --p;
+            while ((p + 1) * (p + 2) <= l) ++p;
+            const int off = l - p * (p + 1);
+            tm = 2 * p + (off >= p + 1 ? 1 : 0);
+            tn = off >= p + 1 ? off - (p + 1) : off;
+        } else if (sym) {
             int r = (int)((sqrtf(8.0f * (float)l + 1.0f) - 1.0f) * 0.5f);
             while (r * (r + 1) / 2 > l) --r;
             while ((r + 1) * (r + 2) / 2 <= l) ++r;
@@ -524,8 +535,13 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     TileSched sc;
     sc.tiles_m = (a.M + BM - 1) / BM;
     sc.tiles_n = (a.N + BN - 1) / BN;
-    sc.sym = a.symmetric;
-    sc.per_batch = a.symmetric ? sc.tiles_m * (sc.tiles_m + 1) / 2 : sc.tiles_m * sc.tiles_n;
+    sc.sym = a.symmetric ? (BN == 256 ? 2 : 1) : 0;
+    if (sc.sym == 2) {
+        sc.per_batch = 0;
+        for (int tm = 0; tm < sc.tiles_m; ++tm) sc.per_batch += tm / 2 + 1;
+    } else {
+        sc.per_batch = a.symmetric ? sc.tiles_m * (sc.tiles_m + 1) / 2 : sc.tiles_m * sc.tiles_n;
+    }
     sc.total = sc.per_batch * a.batch;
     const int grid = sc.total < num_sms ? sc.total : num_sms;
     gemm_tc_kernel<BN, B_KMAJOR, TF32><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mA, mB, a, sc);
@@ -547,7 +563,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
         return cudaErrorInvalidValue;
     if ((int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + 127) / 128) > (int64_t)1 << 30)
         return cudaErrorInvalidValue;
-    const int bn = a.symmetric ? 128 : (a.tile_n == 128 ? 128 : 256);
+    // symmetric products default to 128 x 128 tiles, the others to 128 x 256
+    const int bn = a.symmetric ? (a.tile_n == 256 ? 256 : 128) : (a.tile_n == 128 ? 128 : 256);
     if (tf32) {
         return bn == 128 ? tc::launch_impl<128, true, true>(a, num_sms, s)
                          : tc::launch_impl<256, true, true>(a, num_sms, s);

@@ -91,6 +91,25 @@ struct PrepArgs {
 int prep_num_parts(int m, int n);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
+// Whole update of small matrices (oriented m <= 128, m <= n <= 512, bf16,
+// segments of length 1 or 2), one CTA per matrix: see small_ns.cu.
+struct SmallArgs {
+    const MatEntry* mats;   // device table, one entry per matrix
+    int batch, m, n;        // oriented shape
+    int mode;               // 0: Muon step (momentum + fused update), 1: write O
+    int param_dtype;        // MUON_BF16
+    int mom_dtype;
+    int nesterov;
+    float beta, lr, wd, scale;
+    float a, b, c;
+    int nseg;
+    int segs[16];
+    int vec_ok;             // caller rows 16-byte aligned, 8-element multiples
+    int* status;
+};
+bool small_ns_fits(int m, int n, int nseg, const int* segs);
+cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s);
+
 // inv[b] = 1 / (sqrt(sum(partials[b][:])) + eps); flags a non-finite sum.
 cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
                                  float* inv, int* status, cudaStream_t s);
@@ -103,7 +122,7 @@ cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale
 // Kernel-class bookkeeping for launch counting and optional event timing.
 enum KernelClass : int {
     KC_PREP = 0, KC_NORM = 1, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
-    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_COUNT = 8
+    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_COUNT = 9
 };
 void note_launch_begin(int kclass, cudaStream_t s);
 void note_launch_end(int kclass, double work, cudaStream_t s);

@@ -63,30 +63,33 @@ def test_product_mn_major(mg, dtype, M, N, K, batch, tile):
     _check(C, ref, dtype)
 
 
+@pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("m,k,batch", [(128, 64, 1), (260, 1000, 2), (512, 384, 1), (37, 200, 3)])
-def test_symmetric_gram(mg, dtype, m, k, batch):
+@pytest.mark.parametrize("m,k,batch", [(128, 64, 1), (260, 1000, 2), (512, 384, 1), (37, 200, 3), (896, 136, 1)])
+def test_symmetric_gram(mg, dtype, m, k, batch, tile):
+    """Lower-triangle tiles of 128 x 128 or 128 x 256, mirrored on store."""
     if dtype == torch.bfloat16 and k % 8:
         pytest.skip("tensor-map rows need 16-byte pitch")
     X = _rand((batch, m, k), dtype, 5)
     C = torch.full((batch, m, m), float("nan"), dtype=dtype, device="cuda")
-    mg.muon_debug_gemm(X, X, C, b_kmajor=True, symmetric=True, alpha=1.0 / k)
+    mg.muon_debug_gemm(X, X, C, b_kmajor=True, symmetric=True, alpha=1.0 / k, tile_n=tile)
     torch.cuda.synchronize()
     assert torch.equal(C, C.transpose(1, 2))          # mirrored, every element written
     ref = torch.matmul(X.double(), X.double().transpose(1, 2)) / k
     _check(C, ref, dtype)
 
 
+@pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("m", [128, 384, 200])
-def test_fused_polynomial(mg, dtype, m):
+def test_fused_polynomial(mg, dtype, m, tile):
     X = _rand((1, m, 2 * m), torch.float64, 6)
     G64 = torch.matmul(X, X.transpose(1, 2))
     G64 = G64 / torch.linalg.matrix_norm(G64, ord=2, keepdim=True)
     G = G64.to(dtype).contiguous()
     P = torch.zeros_like(G)
     a, b, c = 3.4445, -4.7750, 2.0315
-    mg.muon_debug_gemm(G, G, P, b_kmajor=True, symmetric=True, poly=(a, b, c))
+    mg.muon_debug_gemm(G, G, P, b_kmajor=True, symmetric=True, poly=(a, b, c), tile_n=tile)
     torch.cuda.synchronize()
     Gd = G.double()
     ref = a * torch.eye(m, device="cuda", dtype=torch.float64) + b * Gd + c * torch.matmul(Gd, Gd)

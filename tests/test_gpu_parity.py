@@ -53,11 +53,15 @@ def test_orthogonalize_fp32(mg, rows, cols, batch, segments):
     assert s <= SIGMA_TOL
 
 
+@pytest.mark.parametrize("small", ["1", "0"])
 @pytest.mark.parametrize("rows,cols,batch", [
     (256, 1024, 1), (128, 512, 4), (256, 256, 2), (300, 1000, 1), (1000, 296, 1), (8, 16, 2),
-    (2, 3, 1), (1, 64, 1), (37, 200, 2), (130, 130, 1)])
+    (2, 3, 1), (1, 64, 1), (37, 200, 2), (130, 130, 1), (512, 128, 3), (96, 300, 2)])
 @pytest.mark.parametrize("segments", [None, (2, 2, 1), (2, 3)])
-def test_orthogonalize_bf16(mg, rows, cols, batch, segments):
+def test_orthogonalize_bf16(mg, monkeypatch, rows, cols, batch, segments, small):
+    """small=1: shapes that fit run the one-CTA-per-matrix kernel; small=0: the
+    general product path for every shape."""
+    monkeypatch.setenv("MUON_SMALL", small)
     f, s = _ortho_case(mg, rows, cols, batch, "bf16", segments, 200, std=0.03)
     assert f <= TOL["bf16"], f
     assert s <= SIGMA_TOL, s
@@ -158,7 +162,8 @@ def test_nonfinite_gradient_is_reported(mg):
     assert mg.muon_sync_status() == mg.MUON_OK        # the word is cleared on read
 
 
-def test_launch_count_matches_plan(mg):
+def test_launch_count_matches_plan(mg, monkeypatch):
+    monkeypatch.setenv("MUON_SMALL", "0")
     w = torch.randn((128, 512), device="cuda").to(torch.bfloat16)
     g, mo = torch.randn_like(w) * 0.01, torch.zeros_like(w)
     for path, expect in ((mg.MUON_PATH_GRAM, 2 + 3 + 5 + 2 + 4 + 3), (mg.MUON_PATH_PLAIN, 2 + 5 * 3)):
@@ -197,7 +202,41 @@ def test_autotune_and_cache_round_trip(mg, tmp_path):
     assert mg.muon_last_path(256, 768, mg.MUON_BF16) in (mg.MUON_PATH_PLAIN, mg.MUON_PATH_GRAM)
     assert mg.muon_sync_status() == mg.MUON_OK
     text = p.read_text().splitlines()
-    assert text[0] == "muon-tune v1" and len(text) >= 3
+    assert text[0] == "muon-tune v3" and len(text) >= 3
     # a corrupt line is skipped, the rest loads
     p.write_text("\n".join(text + ["garbage\tline"]) + "\n")
     assert mg.muon_tune_load(str(p)) == len(text) - 1
+
+
+@pytest.mark.parametrize("path", ["plain", "gram"])
+@pytest.mark.parametrize("mom_dtype", ["bf16", "f32"])
+def test_small_bucket_fused_step(mg, monkeypatch, path, mom_dtype):
+    """A bucket of small matrices (mixed orientation) runs as one fused launch
+    and matches the oracle on two consecutive steps."""
+    monkeypatch.setenv("MUON_SMALL", "1")
+    code = mg.MUON_PATH_PLAIN if path == "plain" else mg.MUON_PATH_GRAM
+    shapes = [(128, 512), (512, 128), (128, 512), (128, 384)]
+    before = mg.muon_launch_count()
+    res = _step_case(mg, shapes, "bf16", mom_dtype, code, True, 8000, 0.0316, steps=2)
+    # two buckets (128x512 and 128x384), two steps, one launch each
+    assert mg.muon_launch_count() - before == 4
+    for err, q, m_ok, pname in res:
+        assert pname == path
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+
+
+def test_small_fused_zero_and_tiny(mg, monkeypatch):
+    monkeypatch.setenv("MUON_SMALL", "1")
+    for shape in ((1, 8), (3, 5), (64, 64)):
+        for err, q, m_ok, _ in _step_case(mg, [shape], "bf16", "bf16", mg.MUON_PATH_PLAIN, False, 9000, 0.02):
+            assert err <= TOL["bf16"] + q, (shape, err, q)
+            assert m_ok
+    w = gen_matrix(9100, 1, 96, 200, 0.02, "bf16")
+    wt = to_device(w, torch)
+    g = torch.zeros_like(wt)
+    mo = torch.zeros_like(wt)
+    mg.muon_step([wt], [g], [mo], lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+    assert mg.muon_sync_status() == mg.MUON_OK
+    expect = orc.round_bf16(orc.to_f64(w.data, "bf16") * (1 - 0.002))
+    assert np.max(np.abs(to_f64(wt) - expect) / np.maximum(np.abs(expect), 1e-30)) <= 2.0 ** -8
