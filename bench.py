@@ -2,8 +2,9 @@
 
 One step = one full Muon update (momentum + Nesterov, Frobenius normalisation,
 Newton-Schulz with the path chosen by the measured-cost autotune, shape-scaled
-decoupled-decay update) of the 2560 x 9728 bf16 matrix, through the C ABI, with
-parameters, momentum and gradient resident in HBM.  L2 is flushed (256 MiB
+decoupled-decay update) of the 2560 x 9728 bf16 matrix, through the C ABI's
+persistent group (muon_group_step, the optimizer object of a training loop),
+with parameters, momentum and gradient resident in HBM.  L2 is flushed (256 MiB
 write) between timed steps, outside the per-step CUDA events.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -274,11 +275,13 @@ def bench_gpu(args):
         data = "synthetic: seeded torch device RNG, same distributions (workloads.py shapes)"
     hp = dict(lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    # the optimizer object of a training loop: registered once, stepped many times
+    group = mg.MuonGroup(params, grads, moms)
     dtype_code = mg.MUON_BF16 if wl.param_dtype == "bf16" else mg.MUON_F32
 
     # warm-up (the first step autotunes every distinct shape)
     for _ in range(args.warmup):
-        mg.muon_step(params, grads, moms, **hp)
+        group.step(**hp)
     torch.cuda.synchronize()
     st = mg.muon_sync_status()
     if st != mg.MUON_OK:
@@ -311,7 +314,7 @@ def bench_gpu(args):
         for i in range(args.steps):
             flush.zero_()                      # L2 flush, outside the step's events
             evs[i][0].record()
-            mg.muon_step(params, grads, moms, **hp)
+            group.step(**hp)
             evs[i][1].record()
         torch.cuda.synchronize()
         if dist is not None:
@@ -343,7 +346,7 @@ def bench_gpu(args):
         eev[i][0].record()
         for dg, hg in zip(grads, host_g):
             dg.copy_(hg, non_blocking=True)
-        mg.muon_step(params, grads, moms, **hp)
+        group.step(**hp)
         for hw, p in zip(host_w, params):
             hw.copy_(p, non_blocking=True)
         eev[i][1].record()
@@ -384,7 +387,9 @@ def bench_gpu(args):
                    "mom_dtype": wl.mom_dtype, "ns_paths": paths, "segments": "2+2+1", "steps_ns": 5,
                    "lr": wl.lr, "beta": wl.beta, "wd": wl.wd, "nesterov": wl.nesterov,
                    "l2": "flushed between timed steps (256 MiB device write outside the step events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "api": "muon_group_step (CUDA graph replay after the first step); "
+                          "kernel breakdown from a second pass with per-launch events (direct launches)"},
         "ns_tflops": {"algorithmic": ns_tflops, "nominal": nom_per_step * world / (ms * 1e-3) / 1e12,
                       "frac_of_bf16_peak": ns_tflops / world / peaks["bf16_tflops"],
                       "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
@@ -407,6 +412,7 @@ def bench_gpu(args):
         line["cpu_baseline"] = run_cpu_baseline(wl)
     elif rank == 0 and world == 1:
         line["cpu_baseline"] = None
+    group.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

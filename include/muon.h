@@ -126,6 +126,29 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms,
               int nesterov, void* stream);
 
 /*
+ * Persistent groups: the optimizer object of a training loop.  The caller
+ * registers a fixed set of matrices once (same arguments as muon_step); the
+ * group buckets them, chooses the paths (autotuning shapes not yet measured),
+ * and owns its workspace and device pointer table.  muon_group_step then runs
+ * one Muon step over the whole set: the first step after creation (or after a
+ * configuration or tune-cache change) launches its kernels directly and the
+ * following steps replay a CUDA graph captured on the group's own stream,
+ * preceded on `stream` by a 16-byte copy of the step's hyper-parameters into a
+ * device block the kernels read, so learning-rate schedules need no recapture.
+ * MUON_GRAPH=0 disables the replay.  The pointers must stay valid for the
+ * group's lifetime; a group belongs to the device that was current at
+ * creation and is used by one host thread at a time.  The group's workspace is
+ * allocated at its first step, so make that step before any stream capture of
+ * your own.  muon_group_destroy synchronises the group's work and frees it.
+ */
+typedef struct muon_group muon_group;
+int muon_group_create(void* const* params, const void* const* grads, void* const* moms,
+                      const int64_t* ms, const int64_t* ns, int64_t count,
+                      int param_dtype, int mom_dtype, muon_group** out);
+int muon_group_step(muon_group* group, float lr, float beta, float wd, int nesterov, void* stream);
+int muon_group_destroy(muon_group* group);
+
+/*
  * NS configuration used by muon_step (process-wide, mutex-guarded).
  * coeffs/steps as above; segments/num_segments give the Gram segmentation
  * (default 2+2+1: "MuonX" page, section 3.2); path is a muon_path.

@@ -37,6 +37,7 @@ EXPORTS = (
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
+    "muon_group_create", "muon_group_step", "muon_group_destroy",
 )
 
 _lib = None
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
         "muon_kernel_timing_read": (i32, [ctypes.c_char_p, i64p, dp, dp, i32]),
         "muon_debug_gemm": (i32, [vp, vp, vp, i64, i64, i64, i64, i32, i32, i32, i32,
                                   f32, f32, f32, f32, i32, vp]),
+        "muon_group_create": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), i64p, i64p, i64,
+                                    i32, i32, ctypes.POINTER(vp)]),
+        "muon_group_step": (i32, [vp, f32, f32, f32, i32, vp]),
+        "muon_group_destroy": (i32, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -172,11 +177,19 @@ def muon_ns_orthogonalize_noalloc(x, coeffs=QUINTIC, steps: int = 5, segments=(2
 
 def muon_step(params, grads, moms, lr: float, beta: float, wd: float, nesterov: bool, stream=None):
     """One Muon step over lists of matrices (updated in place: params, moms)."""
+    arr = _step_arrays(params, grads, moms)
+    if arr is None:
+        return
+    _check(lib().muon_step(*arr, float(lr), float(beta), float(wd), 1 if nesterov else 0, _stream_ptr(stream)),
+           "muon_step")
+
+
+def _step_arrays(params, grads, moms):
     k = len(params)
     if not (len(grads) == k and len(moms) == k):
         raise ValueError("params, grads and moms must have the same length")
     if k == 0:
-        return
+        return None
     pd = _dtype_code(params[0])
     md = _dtype_code(moms[0])
     for i in range(k):
@@ -191,10 +204,53 @@ def muon_step(params, grads, moms, lr: float, beta: float, wd: float, nesterov: 
             raise TypeError(f"dtype mismatch at {i}")
     VP = ctypes.c_void_p * k
     I64 = ctypes.c_int64 * k
-    _check(lib().muon_step(VP(*[p.data_ptr() for p in params]), VP(*[g.data_ptr() for g in grads]),
-                           VP(*[m.data_ptr() for m in moms]), I64(*[p.shape[0] for p in params]),
-                           I64(*[p.shape[1] for p in params]), k, pd, md, float(lr), float(beta), float(wd),
-                           1 if nesterov else 0, _stream_ptr(stream)), "muon_step")
+    return (VP(*[p.data_ptr() for p in params]), VP(*[g.data_ptr() for g in grads]),
+            VP(*[m.data_ptr() for m in moms]), I64(*[p.shape[0] for p in params]),
+            I64(*[p.shape[1] for p in params]), k, pd, md)
+
+
+def muon_group_create(params, grads, moms):
+    """Registers a fixed set of matrices; returns an opaque group handle."""
+    arr = _step_arrays(params, grads, moms)
+    if arr is None:
+        raise ValueError("a group needs at least one matrix")
+    out = ctypes.c_void_p()
+    _check(lib().muon_group_create(*arr, ctypes.byref(out)), "muon_group_create")
+    return out.value
+
+
+def muon_group_step(handle, lr: float, beta: float, wd: float, nesterov: bool, stream=None):
+    _check(lib().muon_group_step(handle, float(lr), float(beta), float(wd), 1 if nesterov else 0,
+                                 _stream_ptr(stream)), "muon_group_step")
+
+
+def muon_group_destroy(handle):
+    if handle:
+        lib().muon_group_destroy(handle)
+
+
+class MuonGroup:
+    """The optimizer object of a training loop: a fixed set of (param, grad,
+    momentum) CUDA tensors stepped many times.  The tensors must stay alive and
+    at the same addresses for the group's lifetime (update them in place)."""
+
+    def __init__(self, params, grads, moms):
+        self._refs = (list(params), list(grads), list(moms))
+        self.handle = muon_group_create(*self._refs)
+
+    def step(self, lr: float, beta: float = 0.95, wd: float = 0.0, nesterov: bool = True, stream=None):
+        muon_group_step(self.handle, lr, beta, wd, nesterov, stream)
+
+    def close(self):
+        if self.handle:
+            muon_group_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def muon_set_ns_config(coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1), path: int = MUON_PATH_AUTO):

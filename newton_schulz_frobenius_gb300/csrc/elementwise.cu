@@ -73,6 +73,8 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
     const int tr = blockIdx.x / tiles_c;
     const int tc = blockIdx.x % tiles_c;
     const MatEntry e = a.mats[b];
+    const float beta = a.hyper ? a.hyper[1] : a.beta;
+    const int nesterov = a.hyper ? (a.hyper[3] != 0.f) : a.nesterov;
     const int lr = threadIdx.x >> 2;          // row within the tile
     const int seg = (threadIdx.x & 3) * 16;   // first of 16 columns
     const bool vec = a.vec_ok != 0;
@@ -100,9 +102,9 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
             load16(e.mom, a.mom_dtype, off, valid, vec, mo);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float mn = fmaf(a.beta, mo[j], g[j]);          // M' = beta M + G
+                const float mn = fmaf(beta, mo[j], g[j]);            // M' = beta M + G
                 mo[j] = mn;
-                u[j] = a.nesterov ? fmaf(a.beta, mn, g[j]) : mn;     // U = G + beta M'
+                u[j] = nesterov ? fmaf(beta, mn, g[j]) : mn;         // U = G + beta M'
             }
             // momentum is stored in its own dtype; U continues from the fp32 M'
             store16(e.mom, a.mom_dtype, off, valid, vec, mo);

@@ -170,8 +170,10 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
     // EPI_UPDATE / EPI_OUT: caller matrices through the table.
     const MatEntry e = a.mats[b];
     const int od = a.out_dtype;
-    const float keep = 1.0f - a.lr * a.wd;
-    const float step = a.lr * a.scale;
+    const float lr = a.hyper ? a.hyper[0] : a.lr;
+    const float wd = a.hyper ? a.hyper[2] : a.wd;
+    const float keep = 1.0f - lr * wd;
+    const float step = lr * a.scale;
     if (!e.trans) {
         const int64_t off = (int64_t)r * a.N + c0;
         if (a.epi == EPI_UPDATE) {

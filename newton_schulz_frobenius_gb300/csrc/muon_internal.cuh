@@ -67,6 +67,7 @@ struct GemmArgs {
     float lr, wd, scale;
     int tile_n;             // tensor-core tile N extent (128 or 256)
     int* status;            // device status word
+    const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd
 };
 
 // Launchers (return the CUDA error of the launch).
@@ -87,6 +88,7 @@ struct PrepArgs {
     float* partials;        // [batch][nparts]
     int nparts;
     int vec_ok;             // caller rows are 16-byte aligned for vector access
+    const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides beta, nesterov
 };
 int prep_num_parts(int m, int n);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
@@ -106,6 +108,7 @@ struct SmallArgs {
     int segs[16];
     int vec_ok;             // caller rows 16-byte aligned, 8-element multiples
     int* status;
+    const float* hyper;     // optional device block {lr, beta, wd, nesterov}
 };
 bool small_ns_fits(int m, int n, int nseg, const int* segs);
 cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s);

@@ -178,6 +178,8 @@ __device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X) {
     const int raw_cols = e.trans ? a.m : a.n;
     const int64_t total = (int64_t)raw_rows * raw_cols;
     const bool step = (a.mode == 0);
+    const float beta = a.hyper ? a.hyper[1] : a.beta;
+    const int nesterov = a.hyper ? (a.hyper[3] != 0.f) : a.nesterov;
     float ss = 0.f;
     auto put = [&](int rr, int cc, const float (&u)[8], int cnt) {
         if (!e.trans && cnt == 8) {
@@ -222,9 +224,9 @@ __device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X) {
                 if (step) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float mn = fmaf(a.beta, mo[uu][k], g[uu][k]);
+                        const float mn = fmaf(beta, mo[uu][k], g[uu][k]);
                         mo[uu][k] = mn;
-                        u[k] = a.nesterov ? fmaf(a.beta, mn, g[uu][k]) : mn;
+                        u[k] = nesterov ? fmaf(beta, mn, g[uu][k]) : mn;
                     }
                     store8(e.mom, e0, a.mom_dtype, mo[uu]);
                 } else {
@@ -241,9 +243,9 @@ __device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X) {
             const float g = ld_elem(e.grad, i, a.param_dtype);
             float u = g;
             if (step) {
-                const float mn = fmaf(a.beta, ld_elem(e.mom, i, a.mom_dtype), g);
+                const float mn = fmaf(beta, ld_elem(e.mom, i, a.mom_dtype), g);
                 st_elem(e.mom, i, mn, a.mom_dtype);
-                u = a.nesterov ? fmaf(a.beta, mn, g) : mn;
+                u = nesterov ? fmaf(beta, mn, g) : mn;
             }
             ss = fmaf(u, u, ss);
             float uv[8] = {u, 0, 0, 0, 0, 0, 0, 0};
@@ -431,8 +433,10 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
                 }
             } else {
                 // O (rows < m, columns < n): update the caller's W or write O
-                const float keep = 1.0f - a.lr * a.wd;
-                const float stepc = a.lr * a.scale;
+                const float lr = a.hyper ? a.hyper[0] : a.lr;
+                const float wd = a.hyper ? a.hyper[2] : a.wd;
+                const float keep = 1.0f - lr * wd;
+                const float stepc = lr * a.scale;
                 const int od = a.param_dtype;
                 for (int k = hw; k < nck * 2; k += 2) {
                     const int c0 = 32 * k;

@@ -1,0 +1,84 @@
+"""Persistent groups (muon_group_*): a registered set of matrices stepped many
+times must give exactly the results of muon_step on the same inputs, with the
+hyper-parameters changing from step to step, whether the steps replay a
+captured CUDA graph or launch directly."""
+import pytest
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as pkg
+    yield pkg
+    pkg.muon_set_ns_config(pkg.QUINTIC, 5, (2, 2, 1), pkg.MUON_PATH_AUTO)
+
+
+def _make(shapes, pdt, mdt, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    W = [(torch.randn(s, generator=g, device="cuda") * 0.02).to(pdt) for s in shapes]
+    G = [(torch.randn(s, generator=g, device="cuda") * 0.03).to(pdt) for s in shapes]
+    M = [torch.zeros(s, device="cuda", dtype=mdt) for s in shapes]
+    return W, G, M
+
+
+SHAPES = [(128, 512), (512, 128), (128, 512), (256, 640), (640, 256), (96, 96), (1, 24)]
+SCHEDULE = [(0.02, 0.95, 0.1, True), (0.01, 0.9, 0.05, False), (0.03, 0.95, 0.0, True), (0.015, 0.8, 0.1, True)]
+
+
+@pytest.mark.parametrize("graph", ["1", "0"])
+@pytest.mark.parametrize("mdt", [torch.bfloat16, torch.float32])
+def test_group_matches_muon_step(mg, monkeypatch, graph, mdt):
+    monkeypatch.setenv("MUON_GRAPH", graph)
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_AUTO)
+    Wa, Ga, Ma = _make(SHAPES, torch.bfloat16, mdt, 11)
+    Wb, Gb, Mb = [w.clone() for w in Wa], [g.clone() for g in Ga], [m.clone() for m in Ma]
+    group = mg.MuonGroup(Wb, Gb, Mb)
+    try:
+        for i, (lr, beta, wd, nest) in enumerate(SCHEDULE):
+            # fresh gradients each step, written in place
+            for ga, gb in zip(Ga, Gb):
+                ga.mul_(-0.7).add_(0.001 * (i + 1))
+                gb.copy_(ga)
+            mg.muon_step(Wa, Ga, Ma, lr=lr, beta=beta, wd=wd, nesterov=nest)
+            group.step(lr=lr, beta=beta, wd=wd, nesterov=nest)
+            torch.cuda.synchronize()
+            assert mg.muon_sync_status() == mg.MUON_OK
+            for x, y in zip(Wa + Ma, Wb + Mb):
+                assert torch.equal(x, y), i
+    finally:
+        group.close()
+
+
+def test_group_counts_its_launches_and_replans(mg, monkeypatch):
+    monkeypatch.setenv("MUON_GRAPH", "1")
+    W, G, M = _make([(256, 640), (128, 512)], torch.bfloat16, torch.bfloat16, 5)
+    group = mg.MuonGroup(W, G, M)
+    try:
+        group.step(lr=0.02)                       # direct
+        c0 = mg.muon_launch_count()
+        group.step(lr=0.02)                       # captures and replays
+        c1 = mg.muon_launch_count()
+        group.step(lr=0.01)                       # replays
+        c2 = mg.muon_launch_count()
+        assert c1 - c0 == c2 - c1 > 0
+        mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_PLAIN)   # plans change
+        group.step(lr=0.01)
+        assert mg.muon_last_path(256, 640, mg.MUON_BF16) == mg.MUON_PATH_PLAIN
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+    finally:
+        group.close()
+        mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_AUTO)
+
+
+def test_group_validation(mg):
+    W, G, M = _make([(64, 64)], torch.bfloat16, torch.bfloat16, 3)
+    with pytest.raises(ValueError):
+        mg.MuonGroup([], [], [])
+    with pytest.raises(mg.MuonError):
+        h = mg.MuonGroup(W, G, M)
+        mg.muon_group_step(h.handle, float("nan"), 0.9, 0.0, False)

@@ -1,0 +1,85 @@
+"""Evidence for the bf16 path's precision policy, on the CPU.
+
+The NS iteration is simulated with the storage roundings of the CUDA path
+(bf16 X, fp32-accumulated products, Gram-space matrices either bf16 or TF32,
+the applied transform in bf16) and compared with the fp64 oracle.  The cases
+are the ones that decide the policy: Gram NS with bf16 Gram space misses the
+2% bar on small and square shapes, TF32 Gram space meets it, and a
+polynomial whose linear term uses a more precise G than its quadratic term is
+worse than a consistent one.
+"""
+import numpy as np
+import pytest
+
+from oracle import muon_oracle as orc
+from workloads import gen_matrix
+
+
+def _bits(x, bits):
+    mant, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(mant, bits)), e - bits)
+
+
+def bf16(x):
+    return _bits(x, 8)
+
+
+def tf32(x):
+    return _bits(x, 11)
+
+
+def f32(x):
+    return x.astype(np.float32).astype(np.float64)
+
+
+def simulate(U, segs, sq, lin_fp32=False, coeffs=orc.QUINTIC):
+    a, b, c = coeffs
+    X, tr = orc.orient(U)
+    inv = 1.0 / (np.sqrt((X * X).sum()) + orc.EPS)
+    X = bf16(X)
+    m = X.shape[0]
+    I = np.eye(m)
+    for si, L in enumerate(segs):
+        al = inv if si == 0 else 1.0
+        Gacc = f32(X @ X.T) * al * al
+        G = sq(Gacc)
+        Q = None
+        for j in range(1, L + 1):
+            lin = Gacc if (lin_fp32 and j == 1) else G
+            P = sq(a * I + b * lin + c * f32(G @ G))
+            Q = P if j == 1 else sq(f32(P @ Q))
+            if j < L:
+                G = sq(f32(sq(f32(P @ G)) @ P))
+        X = bf16(f32(bf16(Q) @ X) * al)
+    return X.T if tr else X
+
+
+def _err(shape, segs, sq, lin_fp32=False, seeds=(200, 201)):
+    worst = 0.0
+    for s in seeds:
+        U = orc.to_f64(gen_matrix(s, 0, *shape, 0.03, "bf16").data, "bf16")
+        path = "plain" if all(L == 1 for L in segs) else "gram"
+        O = orc.orthogonalize(U, path, segments=segs if path == "gram" else (2, 2, 1))
+        worst = max(worst, np.linalg.norm(simulate(U, segs, sq, lin_fp32) - O) / np.linalg.norm(O))
+    return worst
+
+
+@pytest.mark.parametrize("shape,segs", [((130, 130), (2, 3)), ((37, 200), (2, 2, 1)), ((8, 16), (2, 2, 1))])
+def test_gram_small_or_square_needs_tf32_gram_space(shape, segs):
+    assert _err(shape, segs, bf16) > 0.02
+    assert _err(shape, segs, tf32) < 0.02
+
+
+@pytest.mark.parametrize("shape", [(128, 512), (256, 1024)])
+def test_gram_rectangular_is_fine_in_bf16(shape):
+    assert _err(shape, (2, 2, 1), bf16) < 0.012
+
+
+def test_plain_gains_nothing_from_tf32():
+    e_b = _err((37, 200), (1, 1, 1, 1, 1), bf16)
+    e_t = _err((37, 200), (1, 1, 1, 1, 1), tf32)
+    assert e_b < 0.02 and abs(e_b - e_t) < 0.2 * e_b
+
+
+def test_polynomial_needs_one_rounded_g():
+    assert _err((1, 64), (1, 1, 1, 1, 1), bf16, lin_fp32=True) > 2 * _err((1, 64), (1, 1, 1, 1, 1), bf16)
