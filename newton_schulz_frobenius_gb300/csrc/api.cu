@@ -41,6 +41,14 @@ static int log_level() {
 
 static thread_local std::string t_last_error;
 
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("MUON_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 static void logf(int lvl, const char* fmt, ...) {
     if (log_level() < lvl) return;
     va_list ap;

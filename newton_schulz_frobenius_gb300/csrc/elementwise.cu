@@ -68,6 +68,8 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
     __shared__ float tile[PT][PT + 1];
     __shared__ float red[PTHREADS / 32];
 
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     const int tiles_c = (a.n + PT - 1) / PT;
     const int tr = blockIdx.x / tiles_c;
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(256)
 norm_finalize_kernel(const float* __restrict__ partials, int nparts, float eps,
                      float* __restrict__ inv, int* status) {
     __shared__ double red[8];
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     double s = 0.0;
     for (int i = threadIdx.x; i < nparts; i += 256) s += (double)partials[(int64_t)b * nparts + i];
@@ -195,14 +199,12 @@ int prep_num_parts(int m, int n) {
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
     dim3 grid(prep_num_parts(a.m, a.n), a.batch);
-    prep_kernel<<<grid, PTHREADS, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prep_kernel, grid, dim3(PTHREADS), 0, s, a);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
                                  float* inv, int* status, cudaStream_t s) {
-    norm_finalize_kernel<<<batch, 256, 0, s>>>(partials, nparts, eps, inv, status);
-    return cudaGetLastError();
+    return launch_pdl(norm_finalize_kernel, dim3(batch), dim3(256), 0, s, partials, nparts, eps, inv, status);
 }
 
 cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale, uint32_t seed,

@@ -321,6 +321,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = (args.K + KE - 1) / KE;
+    pdl_wait();          // operands, G, W and the scale come from earlier kernels
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -544,8 +546,8 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     }
     sc.total = sc.per_batch * a.batch;
     const int grid = sc.total < num_sms ? sc.total : num_sms;
-    gemm_tc_kernel<BN, B_KMAJOR, TF32><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mA, mB, a, sc);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tc_kernel<BN, B_KMAJOR, TF32>, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA,
+                      mB, a, sc);
 }
 
 }  // namespace tc

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/muon.h"
 
 namespace muon {
@@ -121,6 +123,33 @@ cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, f
 // (autotune input only; never touches caller data).
 cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale,
                                   uint32_t seed, cudaStream_t s);
+
+// Programmatic dependent launch: a kernel launched this way may start (and run
+// its set-up: barrier init, TMEM allocation, tensor-map prefetch) while the
+// previous kernel on the stream finishes.  Every library kernel executes
+// pdl_wait() before it reads anything another kernel produced and
+// pdl_trigger() only after that, so a dependent grid launches only once all
+// CTAs of its predecessor are resident or done.  MUON_PDL=0 turns it off.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel-class bookkeeping for launch counting and optional event timing.
 enum KernelClass : int {

@@ -286,6 +286,8 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
+    pdl_wait();          // the caller's matrices may come from the previous kernel
+    pdl_trigger();
 
     const int nck = (a.n + 63) / 64;            // X chunks in use
     constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false);
@@ -511,8 +513,7 @@ cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s) {
     if (!small_ns_fits(a.m, a.n, a.nseg, a.segs) || a.batch < 1) return cudaErrorInvalidValue;
     if (a.param_dtype != MUON_BF16) return cudaErrorInvalidValue;
     const int grid = a.batch < num_sms ? a.batch : num_sms;
-    small::small_ns_kernel<<<grid, small::NT, small::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(small::small_ns_kernel, dim3(grid), dim3(small::NT), (size_t)small::SMEM_BYTES, s, a);
 }
 
 }  // namespace muon
