@@ -224,7 +224,7 @@ def _measured_traffic(kernel_key):
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get(kernel_key)
+        e = d.get("symmetric_products" if kernel_key.startswith("gemm_tc_kernel symmetric") else kernel_key)
         if e and e.get("kernel_hash") == _kernel_hash() and e.get("workload") == WORKLOAD_SEL[0]:
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -357,9 +357,11 @@ def bench_gpu(args):
 
     peaks = _peaks()
     # dominant kernel: the tensor-core product instance with the largest device time
-    groups = {"gemm_tc_apply": ("gemm_tc_apply", "gemm_tc_apply_update"),
-              "gemm_tc_syrk": ("gemm_tc_syrk",), "gemm_tc_square": ("gemm_tc_square",),
-              "gemm_fp32": ("gemm_fp32",), "small_ns_fused": ("small_ns_fused",)}
+    # grouped by kernel instance as ncu lists them: the symmetric products (XX^T
+    # and the Gram-space products) share one instance, the long applies another
+    groups = {"gemm_tc_kernel symmetric products (XX^T, G^2+poly, PG, (PG)P, PQ)": ("gemm_tc_syrk", "gemm_tc_square"),
+              "gemm_tc_kernel long apply QX (incl. fused update)": ("gemm_tc_apply", "gemm_tc_apply_update"),
+              "gemm_simt_kernel (fp32 path)": ("gemm_fp32",), "small_ns_kernel (fused small matrices)": ("small_ns_fused",)}
     best, best_ms, best_work, best_n = None, -1.0, 0.0, 0
     for gname, members in groups.items():
         tot = sum(ktimes.get(k, (0, 0.0, 0.0))[1] for k in members)
@@ -370,11 +372,16 @@ def bench_gpu(args):
     roofline = None
     if best_n:
         achieved = best_work / (best_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roofline = {"kernel": best, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        if best.startswith("gemm_simt"):
+            # fp32 FFMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (unit counts and clock)
+            peak, bound, src = 152 * 128 * 2 * 2.07e9 / 1e12, "alu", "derived FFMA peak (152 SMs x 128 lanes x 2 x 2.07 GHz)"
+        else:
+            peak, bound = peaks["bf16_tflops"], "tensor"
+            src = f"{peaks['source']} bf16_tflops (burst: kernels timed inside a ~ms step)"
+        roofline = {"kernel": best, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "launches": best_n, "avg_launch_ms": best_ms / best_n,
-                    "traffic": _measured_traffic(best),
-                    "peak_source": f"{peaks['source']} bf16_tflops (burst: kernels timed inside a ~ms step)"}
+                    "work_per_launch_flop": best_work / best_n,
+                    "traffic": _measured_traffic(best), "peak_source": src}
     step_total_kernel_ms = sum(v[1] for v in ktimes.values()) / args.steps
     ns_tflops = alg_per_step * world / (ms * 1e-3) / 1e12
 

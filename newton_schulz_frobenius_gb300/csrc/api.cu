@@ -295,6 +295,7 @@ struct NsPlan {
     int path;       // MUON_PATH_PLAIN or MUON_PATH_GRAM
     int tile_n;     // tensor-core N extent of the long products
     int sym_tile_n; // tensor-core N extent of the symmetric products (128 or 256)
+    int sym_dense;  // compute all tiles of the symmetric products (no mirroring)
     int gram_tf32;  // bf16 path: Gram-space matrices kept in TF32 (else bf16)
     int fused;      // run the whole update of each matrix in one CTA (small_ns.cu)
 };
@@ -312,9 +313,10 @@ static int gram_space_tf32(int path, int m, int n) {
 }
 
 static NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_segs, int path, int tile_n,
-                        int m, int n, int sym_tile_n = 128) {
+                        int m, int n, int sym_tile_n = 128, int sym_dense = 0) {
     NsPlan p;
     p.sym_tile_n = sym_tile_n;
+    p.sym_dense = sym_dense;
     p.gram_tf32 = gram_space_tf32(path, m, n);
     p.fused = 0;
     p.a = coeffs[0];
@@ -433,7 +435,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
         g.A = A; g.lda = L.ldm; g.strideA = strideM;
         g.B = Bm; g.ldb = L.ldm; g.strideB = strideM;
         g.M = m; g.N = m; g.K = m; g.batch = B;
-        g.symmetric = 1;
+        g.symmetric = plan.sym_dense ? 0 : 1;
         g.epi = EPI_STORE;
         g.C = C; g.ldc = L.ldm; g.strideC = strideM;
         g.tile_n = plan.sym_tile_n;
@@ -453,7 +455,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
             g.A = X; g.lda = L.ldx; g.strideA = strideX;
             g.B = X; g.ldb = L.ldx; g.strideB = strideX;
             g.M = m; g.N = m; g.K = n; g.batch = B;
-            g.symmetric = 1;
+            g.symmetric = plan.sym_dense ? 0 : 1;
             g.epi = EPI_STORE;
             g.C = G; g.ldc = L.ldm; g.strideC = strideM;
             g.tile_n = plan.sym_tile_n;
@@ -571,6 +573,7 @@ struct TuneEntry {
     double ms_per_matrix;
     int fused;
     int sym_tile_n;
+    int sym_dense;
 };
 using TuneKey = std::tuple<std::string, int, int, int64_t, int64_t, int>;   // device, sms, cudart, m, n, dtype
 static std::map<TuneKey, TuneEntry> g_tune;
@@ -658,32 +661,26 @@ static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dt
     if (r) return r;
     char* base = w->base;
 
-    struct Cand { int path, tile_n, sym_tile_n; };
-    std::vector<Cand> cands;
-    const int tiles[2] = {256, 128};
-    const int ntiles = (dtype == MUON_BF16) ? 2 : 1;
-    for (int ti = 0; ti < ntiles; ++ti)
-        for (int si = 0; si < ntiles; ++si) {
-            cands.push_back({MUON_PATH_PLAIN, tiles[ti], tiles[1 - si]});
-            if (!cfg.segments.empty()) cands.push_back({MUON_PATH_GRAM, tiles[ti], tiles[1 - si]});
-        }
     cudaEvent_t e0, e1;
     MUON_CUDA(cudaEventCreate(&e0));
     MUON_CUDA(cudaEventCreate(&e1));
     FinalEpi fin{EPI_STORE, nullptr, dtype, 0.f, 0.f, 0.f};
     const float scale = std::sqrt(3.0f / ((float)m * (float)n));
-    TuneEntry best{MUON_PATH_PLAIN, 256, 1e300, 0, 128};
+    struct Cand { int path, tile_n, sym_tile_n, sym_dense; };
+    const bool bf = (dtype == MUON_BF16);
+    TuneEntry best{MUON_PATH_PLAIN, 256, 1e300, 0, 128, 0};
     const int reps = 3;
-    for (auto& c : cands) {
-        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, c.path, c.tile_n, m, n, c.sym_tile_n);
+    auto measure = [&](const Cand& c, double* out_ms) -> int {
+        NsPlan plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, c.path, c.tile_n, m, n, c.sym_tile_n,
+                                c.sym_dense);
         std::vector<float> times;
         for (int rep = 0; rep <= reps; ++rep) {
             cudaError_t e = launch_fill_synthetic(base + L.off_X, (int64_t)B * m * L.ldx, dtype, scale,
                                                   0x5eed0000u + (uint32_t)rep, s);
             if (e != cudaSuccess) return cuda_fail(e, "fill launch");
             MUON_CUDA(cudaEventRecord(e0, s));
-            r = run_ns(dc, s, base, L, m, n, B, dtype, plan, false, fin);
-            if (r) return r;
+            int rr = run_ns(dc, s, base, L, m, n, B, dtype, plan, false, fin);
+            if (rr) return rr;
             MUON_CUDA(cudaEventRecord(e1, s));
             MUON_CUDA(cudaEventSynchronize(e1));
             float ms = 0.f;
@@ -691,10 +688,27 @@ static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dt
             if (rep > 0) times.push_back(ms);   // rep 0 is the warm-up
         }
         std::sort(times.begin(), times.end());
-        const double med = times[times.size() / 2] / B;
-        logf(2, "autotune %dx%d dtype %d path %d tile %d sym tile %d: %.4f ms/matrix", m, n, dtype, c.path,
-             c.tile_n, c.sym_tile_n, med);
-        if (med < best.ms_per_matrix) best = TuneEntry{c.path, c.tile_n, med, 0, c.sym_tile_n};
+        *out_ms = times[times.size() / 2] / B;
+        logf(2, "autotune %dx%d dtype %d path %d tile %d sym %d%s: %.4f ms/matrix", m, n, dtype, c.path, c.tile_n,
+             c.sym_tile_n, c.sym_dense ? " dense" : "", *out_ms);
+        if (*out_ms < best.ms_per_matrix) best = TuneEntry{c.path, c.tile_n, *out_ms, 0, c.sym_tile_n, c.sym_dense};
+        return MUON_OK;
+    };
+    // stage 1: path x long-product tile, symmetric products as 128-wide lower-triangle tiles
+    for (int tile : {256, 128}) {
+        if (!bf && tile == 128) continue;
+        for (int path : {MUON_PATH_PLAIN, MUON_PATH_GRAM}) {
+            if (path == MUON_PATH_GRAM && cfg.segments.empty()) continue;
+            double ms;
+            if ((r = measure(Cand{path, tile, 128, 0}, &ms))) return r;
+        }
+    }
+    // stage 2: the symmetric products' tile and form for the winning path and tile
+    const int bp = best.path, bt = best.tile_n;
+    for (const Cand& c : {Cand{bp, bt, 256, 0}, Cand{bp, bt, 128, 1}, Cand{bp, bt, 256, 1}}) {
+        if (!bf && c.sym_tile_n == 256) continue;
+        double ms;
+        if ((r = measure(c, &ms))) return r;
     }
     // the one-CTA-per-matrix kernel, on B synthetic matrices stored contiguously
     for (int path : {MUON_PATH_PLAIN, MUON_PATH_GRAM}) {
@@ -722,7 +736,7 @@ static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dt
         std::sort(times.begin(), times.end());
         const double med = times[times.size() / 2] / B;
         logf(2, "autotune %dx%d fused path %d: %.4f ms/matrix", m, n, path, med);
-        if (med < best.ms_per_matrix) best = TuneEntry{path, 256, med, 1, 128};
+        if (med < best.ms_per_matrix) best = TuneEntry{path, 256, med, 1, 128, 0};
     }
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
@@ -744,7 +758,7 @@ static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype
     }
     if (path == MUON_PATH_GRAM && cfg.segments.empty()) path = MUON_PATH_PLAIN;
     const TuneKey key = tune_key(dc, m, n, dtype);
-    TuneEntry ent{-1, 256, 0.0, 0, 128};
+    TuneEntry ent{-1, 256, 0.0, 0, 128, 0};
     bool have = false;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -772,7 +786,11 @@ static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype
     }
     const int tile_n = (have && ent.path == path) ? ent.tile_n : 256;
     const int sym_tile_n = (have && ent.path == path) ? ent.sym_tile_n : 128;
-    *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n, m, n, sym_tile_n);
+    const int sym_dense = (have && ent.path == path) ? ent.sym_dense : 0;
+    *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n, m, n, sym_tile_n, sym_dense);
+    if (const char* f = std::getenv("MUON_SYM_DENSE")) {    // override for tests: 0 triangle, 1 all tiles
+        if (f[0] == '0' || f[0] == '1') plan->sym_dense = f[0] - '0';
+    }
     // the fused small-matrix kernel: as measured, else whenever it applies
     const bool measured = have && ent.path == path;
     plan->fused = small_eligible(*plan, m, n, dtype) && (measured ? ent.fused != 0 : true);
@@ -783,7 +801,7 @@ static int save_tune_file(const char* path) {
     std::lock_guard<std::mutex> lk(g_mu);
     std::ofstream f(path);
     if (!f) return fail(MUON_EINVAL, "cannot write tune cache %s", path);
-    f << "muon-tune v3\n";
+    f << "muon-tune v4\n";
     int nwritten = 0;
     for (auto& kv : g_tune) {
         std::string dev = std::get<0>(kv.first);
@@ -791,7 +809,7 @@ static int save_tune_file(const char* path) {
         f << dev << '\t' << std::get<1>(kv.first) << '\t' << std::get<2>(kv.first) << '\t' << std::get<3>(kv.first)
           << '\t' << std::get<4>(kv.first) << '\t' << std::get<5>(kv.first) << '\t' << kv.second.path << '\t'
           << kv.second.tile_n << '\t' << kv.second.ms_per_matrix << '\t' << kv.second.fused << '\t'
-          << kv.second.sym_tile_n << '\n';
+          << kv.second.sym_tile_n << '\t' << kv.second.sym_dense << '\n';
         ++nwritten;
     }
     return nwritten;
@@ -1072,7 +1090,7 @@ int muon_tune_load(const char* path) {
     std::ifstream f(path);
     if (!f) return 0;
     std::string line;
-    if (!std::getline(f, line) || line != "muon-tune v3") return 0;
+    if (!std::getline(f, line) || line != "muon-tune v4") return 0;
     DevCtx dc;
     int r = get_dev(dc);
     if (r) return r;
@@ -1083,7 +1101,7 @@ int muon_tune_load(const char* path) {
         std::string dev, tok;
         std::vector<std::string> cols;
         while (std::getline(ss, tok, '\t')) cols.push_back(tok);
-        if (cols.size() != 11) continue;
+        if (cols.size() != 12) continue;
         try {
             const int sms = std::stoi(cols[1]), cuv = std::stoi(cols[2]);
             const int64_t m = std::stoll(cols[3]), n = std::stoll(cols[4]);
@@ -1091,6 +1109,8 @@ int muon_tune_load(const char* path) {
             const double ms = std::stod(cols[8]);
             const int fused = std::stoi(cols[9]);
             const int sym_tile = std::stoi(cols[10]);
+            const int sym_dense = std::stoi(cols[11]);
+            if (sym_dense != 0 && sym_dense != 1) continue;
             if (fused != 0 && fused != 1) continue;
             if (sym_tile != 128 && sym_tile != 256) continue;
             if (cols[0] != dc.name || sms != dc.sms || cuv != cv) continue;          // stale: other device/runtime
@@ -1098,7 +1118,7 @@ int muon_tune_load(const char* path) {
             if (path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM) continue;
             if (tile != 128 && tile != 256) continue;
             std::lock_guard<std::mutex> lk(g_mu);
-            g_tune[TuneKey{dc.name, sms, cuv, m, n, dt}] = TuneEntry{path, tile, ms, fused, sym_tile};
+            g_tune[TuneKey{dc.name, sms, cuv, m, n, dt}] = TuneEntry{path, tile, ms, fused, sym_tile, sym_dense};
             ++loaded;
             g_cfg_version.fetch_add(1);
         } catch (...) {

@@ -115,17 +115,51 @@ __device__ __forceinline__ void load_row_run(const void* base, int64_t off, floa
     }
 }
 
-// One thread, one row r, columns c0 .. c0+W-1.  Every global load of a chunk
-// is issued before its first store (the caller's W is both read and written,
-// so a load placed after a store to it could not be moved ahead of it).
-// Row runs use 16-byte vector accesses; the mirrored half of a symmetric
-// product and the caller's matrix of a tall (transposed) bucket are written
-// column by column, which is coalesced across the 32 lanes of a warp because
-// the lanes of a tensor-core epilogue warp own 32 consecutive rows.
+// Loads, for one thread's row r and columns c0 .. c0+W-1, the values the
+// epilogue will combine with the product: G for EPI_POLY, the caller's W for
+// EPI_UPDATE (nothing otherwise).  Split from epi_row_chunk so a caller can
+// issue the next chunk's loads before it processes the current one.
 template <int W>
-__device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, int c0, float (&v)[W]) {
+__device__ __forceinline__ void epi_load_chunk(const GemmArgs& a, const MatEntry& e, int b, int r, int c0,
+                                               float (&g)[W]) {
     if (r >= a.M) return;
-    const float s = epi_alpha(a, b);
+    const int nvalid = min(W, a.N - c0);
+    if (nvalid <= 0) return;
+    if (a.epi == EPI_POLY) {
+        const int64_t goff = (int64_t)b * a.strideG + (int64_t)r * a.ldg + c0;
+        if (nvalid == W) {
+            load_row_run<W>(a.Gin, goff, g, a.dtype);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(a.Gin, goff + j, a.dtype) : 0.f;
+        }
+    } else if (a.epi == EPI_UPDATE) {
+        const int od = a.out_dtype;
+        if (!e.trans) {
+            const int64_t off = (int64_t)r * a.N + c0;
+            if (nvalid == W) {
+                load_row_run<W>(e.w, off, g, od);
+            } else {
+#pragma unroll
+                for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(e.w, off + j, od) : 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(e.w, (int64_t)(c0 + j) * a.M + r, od) : 0.f;
+        }
+    }
+}
+
+// One thread, one row r, columns c0 .. c0+W-1, scale s (epi_alpha), table
+// entry e (EPI_UPDATE / EPI_OUT) and the chunk's preloaded values g
+// (epi_load_chunk).  Row runs use 16-byte vector stores; the mirrored half of
+// a symmetric product and the caller's matrix of a tall (transposed) bucket
+// are written column by column, which is coalesced across the 32 lanes of a
+// warp because the lanes of a tensor-core epilogue warp own 32 consecutive rows.
+template <int W, bool MIRROR = true>
+__device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, const MatEntry& e, int b, int r, int c0,
+                                              float (&v)[W], float s, const float (&g)[W]) {
+    if (r >= a.M) return;
     const int nvalid = min(W, a.N - c0);
     if (nvalid <= 0) return;
 #pragma unroll
@@ -135,14 +169,6 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
         const int64_t cbase = (int64_t)b * a.strideC;
         const int cd = a.c_dtype;
         if (a.epi == EPI_POLY) {
-            float g[W];
-            const int64_t goff = (int64_t)b * a.strideG + (int64_t)r * a.ldg + c0;
-            if (nvalid == W) {
-                load_row_run<W>(a.Gin, goff, g, a.dtype);
-            } else {
-#pragma unroll
-                for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(a.Gin, goff + j, a.dtype) : 0.f;
-            }
 #pragma unroll
             for (int j = 0; j < W; ++j) v[j] = a.pc * v[j] + a.pb * g[j] + ((c0 + j) == r ? a.pa : 0.f);
         }
@@ -159,7 +185,7 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
             for (int j = 0; j < W; ++j)
                 if (j < nvalid && (!a.symmetric || c0 + j <= r)) st_elem(a.C, roff + j, v[j], cd);
         }
-        if (a.symmetric) {
+        if (MIRROR && a.symmetric) {
 #pragma unroll
             for (int j = 0; j < W; ++j)
                 if (j < nvalid && c0 + j < r) st_elem(a.C, cbase + (int64_t)(c0 + j) * a.ldc + r, v[j], cd);
@@ -167,26 +193,18 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
         return;
     }
 
-    // EPI_UPDATE / EPI_OUT: caller matrices through the table.
-    const MatEntry e = a.mats[b];
+    // EPI_UPDATE / EPI_OUT: the caller's matrix through the table entry
     const int od = a.out_dtype;
     const float lr = a.hyper ? a.hyper[0] : a.lr;
     const float wd = a.hyper ? a.hyper[2] : a.wd;
     const float keep = 1.0f - lr * wd;
     const float step = lr * a.scale;
+    if (a.epi == EPI_UPDATE) {
+#pragma unroll
+        for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * g[j]);
+    }
     if (!e.trans) {
         const int64_t off = (int64_t)r * a.N + c0;
-        if (a.epi == EPI_UPDATE) {
-            float w[W];
-            if (nvalid == W) {
-                load_row_run<W>(e.w, off, w, od);
-            } else {
-#pragma unroll
-                for (int j = 0; j < W; ++j) w[j] = (j < nvalid) ? ld_elem(e.w, off + j, od) : 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * w[j]);
-        }
         if (nvalid == W) {
             store_row_run<W>(e.w, off, v, od);
         } else {
@@ -196,17 +214,59 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, int b, int r, i
         }
     } else {
         // caller matrix is n x m: oriented (r, c) lives at c * m + r
-        if (a.epi == EPI_UPDATE) {
-            float w[W];
-#pragma unroll
-            for (int j = 0; j < W; ++j) w[j] = (j < nvalid) ? ld_elem(e.w, (int64_t)(c0 + j) * a.M + r, od) : 0.f;
-#pragma unroll
-            for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * w[j]);
-        }
 #pragma unroll
         for (int j = 0; j < W; ++j)
             if (j < nvalid) st_elem(e.w, (int64_t)(c0 + j) * a.M + r, v[j], od);
     }
+}
+
+// Mirrored half of a symmetric product for one warp's 32 x 32 chunk (rows
+// r0.., columns c0..): element (r, c) with c < r is also written to (c, r).
+// The warp's final values v (lane = row) go through a 32 x 33 fp32 staging
+// area, then every lane writes one 8-column segment of a mirrored row, so a
+// store instruction covers 8 rows x 64 bytes (bf16) instead of one column.
+// The staging layout is bank-conflict-free for the row writes (bank
+// lane + j) and for the column reads (bank 8s + k + i).
+__device__ __forceinline__ void epi_mirror_staged(const GemmArgs& a, int b, int r0, int c0, const float (&v)[32],
+                                                  float (*stage)[33]) {
+    const int lane = threadIdx.x & 31;
+    if (c0 >= r0 + 31) return;              // no element of the chunk lies strictly below the diagonal
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[lane][j] = v[j];
+    __syncwarp();
+    const int64_t cbase = (int64_t)b * a.strideC;
+    const int sg = lane & 3;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+        const int i = pass * 8 + (lane >> 2);    // mirrored row c0 + i
+        const int c = c0 + i;
+        const int rb = r0 + 8 * sg;              // its columns rb .. rb+7 (rows of the chunk)
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = stage[8 * sg + k][i];
+        if (c < a.N) {
+            const int64_t off = cbase + (int64_t)c * a.ldc + rb;
+            if (c < rb && rb + 7 < a.M) {
+                store_row_run<8>(a.C, off, w, a.c_dtype);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (rb + k < a.M && c < rb + k) st_elem(a.C, off + k, w[k], a.c_dtype);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// Convenience for callers without pipelining: scale, table entry and loads
+// for one chunk, then the epilogue.
+template <int W>
+__device__ __forceinline__ void epi_row_chunk_once(const GemmArgs& a, int b, int r, int c0, float (&v)[W]) {
+    MatEntry e{};
+    if (a.epi == EPI_UPDATE || a.epi == EPI_OUT) e = a.mats[b];
+    float g[W];
+    epi_load_chunk<W>(a, e, b, r, c0, g);
+    epi_row_chunk<W>(a, e, b, r, c0, v, epi_alpha(a, b), g);
 }
 
 }  // namespace muon

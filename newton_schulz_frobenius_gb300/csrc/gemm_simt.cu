@@ -84,7 +84,7 @@ gemm_simt_kernel(const __grid_constant__ GemmArgs a, int tiles_m) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float v[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
-        epi_row_chunk<4>(a, b, row0 + ty * 4 + i, col0 + tx * 4, v);
+        epi_row_chunk_once<4>(a, b, row0 + ty * 4 + i, col0 + tx * 4, v);
     }
 }
 

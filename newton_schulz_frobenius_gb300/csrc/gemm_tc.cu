@@ -48,10 +48,11 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 7;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+    static constexpr int MIRROR_BYTES = NEPI * 32 * 33 * 4;   // per epilogue warp: one 32 x 33 fp32 chunk
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + MIRROR_BYTES + NUM_BARS * 8 + 16 + 1024;
 };
 
 // ---------------------------------------------------------------------------
@@ -282,7 +283,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
+    float* mirror_stage = reinterpret_cast<float*>(sB + S * C::B_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES + C::MIRROR_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -420,6 +422,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else {
         // ---------------- epilogue (warps 2..9) ----------------
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
+        float (*mstage)[33] = reinterpret_cast<float (*)[33]>(mirror_stage + (warp - 2) * 32 * 33);
         const int half = (warp - 2) / 4;           // which half of the tile's columns
         constexpr int HALF_COLS = BN / 2;
         int acc = 0;
@@ -444,20 +447,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         prefetch_l2(wb + ((int64_t)c * args.M + tm * BM + q * 32) * ob);
                 }
             }
+            // per-tile scalars and the first chunk's G / W loads are issued
+            // before the wait, so their latency hides behind the main loop
+            const float scale = epi_alpha(args, b);
+            MatEntry ent{};
+            if (args.epi == EPI_UPDATE || args.epi == EPI_OUT) ent = args.mats[b];
+            const int row0 = tm * BM + q * 32;
+            const int warp_row_max = row0 + 31;
+            const int ch_beg = half * (HALF_COLS / 32), ch_end = (half + 1) * (HALF_COLS / 32);
+            const bool loads = (args.epi == EPI_POLY || args.epi == EPI_UPDATE);
+            float gcur[32], gnxt[32];
+            if (loads) epi_load_chunk<32>(args, ent, b, row0 + lane, tn * BN + ch_beg * 32, gcur);
             // every lane observes the barrier itself; the warp proceeds only together
             const bool ok = wait_bounded(accf0 + 8 * acc, aphase, abort_flag, args.status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int row0 = tm * BM + q * 32;
-            const int warp_row_max = row0 + 31;
 #pragma unroll 1
-            for (int ch = half * (HALF_COLS / 32); ch < (half + 1) * (HALF_COLS / 32); ++ch) {
+            for (int ch = ch_beg; ch < ch_end; ++ch) {
                 const int col0 = tn * BN + ch * 32;
                 if (col0 >= args.N) break;
                 if (args.symmetric && col0 > warp_row_max) continue;
+                if (loads && ch + 1 < ch_end)      // next chunk's loads fly while this one is processed
+                    epi_load_chunk<32>(args, ent, b, row0 + lane, col0 + 32, gnxt);
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-                epi_row_chunk<32>(args, b, row0 + lane, col0, v);
+                epi_row_chunk<32, false>(args, ent, b, row0 + lane, col0, v, scale, gcur);
+                if (args.symmetric) epi_mirror_staged(args, b, row0, col0, v, mstage);
+                if (loads) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) gcur[j] = gnxt[j];
+                }
             }
             tc_fence_before();
             __syncwarp();

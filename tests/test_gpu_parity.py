@@ -202,7 +202,7 @@ def test_autotune_and_cache_round_trip(mg, tmp_path):
     assert mg.muon_last_path(256, 768, mg.MUON_BF16) in (mg.MUON_PATH_PLAIN, mg.MUON_PATH_GRAM)
     assert mg.muon_sync_status() == mg.MUON_OK
     text = p.read_text().splitlines()
-    assert text[0] == "muon-tune v3" and len(text) >= 3
+    assert text[0] == "muon-tune v4" and len(text) >= 3
     # a corrupt line is skipped, the rest loads
     p.write_text("\n".join(text + ["garbage\tline"]) + "\n")
     assert mg.muon_tune_load(str(p)) == len(text) - 1
@@ -240,3 +240,17 @@ def test_small_fused_zero_and_tiny(mg, monkeypatch):
     assert mg.muon_sync_status() == mg.MUON_OK
     expect = orc.round_bf16(orc.to_f64(w.data, "bf16") * (1 - 0.002))
     assert np.max(np.abs(to_f64(wt) - expect) / np.maximum(np.abs(expect), 1e-30)) <= 2.0 ** -8
+
+
+@pytest.mark.parametrize("dense", ["0", "1"])
+@pytest.mark.parametrize("path", ["plain", "gram"])
+def test_symmetric_products_both_forms(mg, monkeypatch, dense, path):
+    """The Gram-space products as lower-triangle tiles with mirroring, or as
+    all tiles, give the same update within the bar."""
+    monkeypatch.setenv("MUON_SYM_DENSE", dense)
+    monkeypatch.setenv("MUON_SMALL", "0")
+    code = mg.MUON_PATH_PLAIN if path == "plain" else mg.MUON_PATH_GRAM
+    for err, q, m_ok, _ in _step_case(mg, [(256, 768), (768, 256), (200, 200)], "bf16", "bf16", code, True,
+                                      9500, 0.02, steps=2):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
