@@ -199,6 +199,25 @@ const char* muon_last_error_message(void);
 int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_segments,
                   double* nominal, double* algorithmic);
 
+/*
+ * Owner placement for a multi-rank optimizer step ("DMuon" news page, section 3;
+ * "DMuon" summary, section 2.3): each of `count` matrices (shapes ms[i] x ns[i])
+ * gets one owner rank in [0, ranks) that runs its update, so that the
+ * predicted per-rank time is balanced.  Costs: the tune cache's measured
+ * milliseconds per matrix when every oriented shape has an entry for `dtype`
+ * (*measured_out = 1), otherwise the algorithmic FLOPs of the path the library
+ * picks without measurements (*measured_out = 0).  Greedy longest-processing-
+ * time first, the pages' fallback to their MILP: matrices in decreasing cost
+ * (stable in index), each to the least-loaded rank (ties to the lower rank).
+ * Host-only and deterministic, so every rank computes the same plan.
+ *   owner_out     count entries (required when count > 0)
+ *   load_out      ranks entries or NULL: predicted cost per rank
+ *   makespan_out  NULL or the largest per-rank cost
+ *   measured_out  NULL or 1 / 0 as above
+ */
+int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, int ranks,
+                    int* owner_out, double* load_out, double* makespan_out, int* measured_out);
+
 /* ---- diagnostics (not part of the method) ---------------------------------- */
 
 /* Total kernels this library has launched in this process. */

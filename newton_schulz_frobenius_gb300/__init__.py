@@ -37,7 +37,7 @@ EXPORTS = (
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
-    "muon_group_create", "muon_group_step", "muon_group_destroy",
+    "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan",
 )
 
 _lib = None
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
                                     i32, i32, ctypes.POINTER(vp)]),
         "muon_group_step": (i32, [vp, f32, f32, f32, i32, vp]),
         "muon_group_destroy": (i32, [vp]),
+        "muon_owner_plan": (i32, [i64p, i64p, i64, i32, i32, ip, dp, dp, ip]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -338,3 +339,19 @@ def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.
                                  float(alpha), float(pa), float(pb), float(pc), tile_n, _stream_ptr(stream)),
            "muon_debug_gemm")
     return C
+
+
+def muon_owner_plan(shapes, ranks: int, dtype: int = MUON_BF16):
+    """Owner rank per matrix for a multi-rank step (greedy longest-processing-
+    time first on measured or modelled per-matrix costs).
+    Returns (owners, per-rank loads, makespan, measured)."""
+    shapes = list(shapes)
+    k = len(shapes)
+    I64 = ctypes.c_int64 * max(1, k)
+    owners = (ctypes.c_int * max(1, k))()
+    loads = (ctypes.c_double * max(1, ranks))()
+    mk = ctypes.c_double()
+    meas = ctypes.c_int()
+    _check(lib().muon_owner_plan(I64(*[s[0] for s in shapes]), I64(*[s[1] for s in shapes]), k, dtype, ranks,
+                                 owners, loads, ctypes.byref(mk), ctypes.byref(meas)), "muon_owner_plan")
+    return list(owners)[:k], list(loads)[:ranks], mk.value, bool(meas.value)

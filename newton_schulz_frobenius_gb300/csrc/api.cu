@@ -1664,3 +1664,71 @@ int muon_group_destroy(muon_group* g) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Owner placement for a multi-rank step: every matrix gets one owner rank
+// that runs its update ("DMuon" news page, section 3; summary, section 2.3).
+// The pages minimise the predicted makespan with an MILP over measured
+// per-shape costs and fall back to a greedy heuristic when the search space
+// is too large; this is that fallback, longest processing time first.
+// ---------------------------------------------------------------------------
+
+extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, int ranks,
+                               int* owner_out, double* load_out, double* makespan_out, int* measured_out) {
+    if (count < 0 || ranks < 1) return fail(MUON_EINVAL, "count < 0 or ranks < 1");
+    if (count > 0 && (!ms || !ns || !owner_out)) return fail(MUON_EINVAL, "NULL array argument");
+    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    for (int64_t i = 0; i < count; ++i)
+        if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "matrix %lld has a zero side", (long long)i);
+    NsConfig cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cfg = g_cfg;
+    }
+    // cost per matrix: measured ms per matrix when every shape has a tune entry
+    // (measured on this process's device), else algorithmic FLOPs of the path
+    // the library picks without measurements
+    std::vector<double> cost((size_t)count, 0.0);
+    bool measured = count > 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int64_t i = 0; i < count && measured; ++i) {
+            const int64_t m = std::min(ms[i], ns[i]), n = std::max(ms[i], ns[i]);
+            bool found = false;
+            for (auto& kv : g_tune) {
+                if (std::get<3>(kv.first) == m && std::get<4>(kv.first) == n && std::get<5>(kv.first) == dtype) {
+                    cost[(size_t)i] = kv.second.ms_per_matrix;
+                    found = true;
+                    break;
+                }
+            }
+            measured = found;
+        }
+    }
+    if (!measured) {
+        for (int64_t i = 0; i < count; ++i) {
+            const int m = (int)std::min(ms[i], ns[i]), n = (int)std::max(ms[i], ns[i]);
+            const int path = (n > m && !cfg.segments.empty()) ? MUON_PATH_GRAM : MUON_PATH_PLAIN;
+            cost[(size_t)i] = plan_alg_flops(make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, 256, m, n), m, n);
+        }
+    }
+    std::vector<int64_t> order((size_t)count);
+    for (int64_t i = 0; i < count; ++i) order[(size_t)i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int64_t x, int64_t y) { return cost[(size_t)x] > cost[(size_t)y]; });
+    std::vector<double> load((size_t)ranks, 0.0);
+    for (int64_t i : order) {
+        int best = 0;
+        for (int rk = 1; rk < ranks; ++rk)
+            if (load[(size_t)rk] < load[(size_t)best]) best = rk;
+        owner_out[i] = best;
+        load[(size_t)best] += cost[(size_t)i];
+    }
+    double mk = 0.0;
+    for (double l : load) mk = std::max(mk, l);
+    if (load_out)
+        for (int rk = 0; rk < ranks; ++rk) load_out[rk] = load[(size_t)rk];
+    if (makespan_out) *makespan_out = mk;
+    if (measured_out) *measured_out = measured ? 1 : 0;
+    return MUON_OK;
+}
