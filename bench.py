@@ -176,9 +176,11 @@ def bench_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
+    if args.workload == ADAMW_WORKLOAD:
+        return bench_reference_adamw(args)
     from oracle import muon_oracle as orc
     from workloads import WORKLOADS, gen_matrix, zeros_matrix
-    wl = WORKLOADS[WORKLOAD]
+    wl = WORKLOADS[args.workload]
     idx, r, c = next(wl.matrices())
     seed = wl.seed(idx)
     W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
@@ -187,22 +189,24 @@ def bench_reference(args):
 
     def step():
         orc.muon_step(W.data, M.data, G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov,
-                      path="gram", param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype)
+                      path=path, param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype)
 
+    path = "gram" if max(r, c) > min(r, c) else "plain"
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = args.steps * wl.count / el
+    value = args.steps / el              # one matrix per step
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "matrices": wl.count, "shape": [r, c], "ns_path": "gram 2+2+1"},
+            "config": {"workload": args.workload, "matrices": wl.count, "shape": [r, c], "ns_path": path},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"one full Muon step of the {r}x{c} matrix per step (numpy fp64)"},
+                             "sample": f"one full Muon step of the workload's first matrix ({r}x{c}) "
+                                       f"per step (numpy fp64)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -246,6 +250,172 @@ def _gen_device_inputs(torch, wl, device):
         grads.append((torch.randn((r, c), generator=g, device=device) * wl.grad_std).to(pdt))
         moms.append(torch.zeros((r, c), device=device, dtype=mdt))
     return params, grads, moms
+
+
+ADAMW_WORKLOAD = "adamw_nonmatrix_7b"
+
+
+ADAMW_SIZES = [32000 * 4096, 32000 * 4096] + [4096] * 65
+ADAMW_HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+
+
+def adamw_cpu_baseline(max_seconds=20.0):
+    """The fp64 AdamW oracle as it stands on the host cores, on a bounded
+    sample: consecutive 4M-element slices of the embedding table."""
+    import numpy as np
+    from oracle import adamw_oracle as ad
+    from workloads import gen_matrix, zeros_matrix
+    n = 1 << 22
+    P = gen_matrix(4242, 1, 1, n, 0.02, "bf16").data.reshape(-1)
+    G = gen_matrix(4242, 0, 1, n, 1e-3, "bf16").data.reshape(-1)
+    M = zeros_matrix(1, n, "f32").data.reshape(-1)
+    V = zeros_matrix(1, n, "f32").data.reshape(-1)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        r = ad.adamw_step(P, G, M, V, step=done + 1, param_dtype="bf16", state_dtype="f32", **ADAMW_HP)
+        M, V = r["m_new"].astype(np.float32), r["v_new"].astype(np.float32)
+        done += 1
+        el = time.perf_counter() - t0
+        if el * (done + 1) / done > max_seconds or done >= 8:
+            break
+    return {"value": 22.0 * n * done / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} AdamW step(s) over {n} bf16 parameters with fp32 moments (numpy fp64), "
+                      f"22 algorithmic bytes per element", "seconds": el}
+
+
+def bench_reference_adamw(args):
+    """--impl reference for the AdamW workload: the fp64 oracle on 4M-element
+    slices, one slice per step."""
+    import numpy as np
+    from oracle import adamw_oracle as ad
+    from workloads import gen_matrix, zeros_matrix
+    n = 1 << 22
+    P = gen_matrix(4242, 1, 1, n, 0.02, "bf16").data.reshape(-1)
+    G = gen_matrix(4242, 0, 1, n, 1e-3, "bf16").data.reshape(-1)
+    M = zeros_matrix(1, n, "f32").data.reshape(-1)
+    V = zeros_matrix(1, n, "f32").data.reshape(-1)
+    t = 0
+
+    def step():
+        nonlocal t, M, V
+        t += 1
+        r = ad.adamw_step(P, G, M, V, step=t, param_dtype="bf16", state_dtype="f32", **ADAMW_HP)
+        M, V = r["m_new"].astype(np.float32), r["v_new"].astype(np.float32)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = 22.0 * n * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": "AdamW step over the non-matrix parameters (GB/s)", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": ADAMW_WORKLOAD, "elements_per_step": n, "param_dtype": "bf16",
+                       "state_dtype": "f32", "bytes_per_element": 22},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"AdamW over {n} bf16 parameters per step (numpy fp64)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_adamw(args):
+    """AdamW over the parameters a 7B-class model keeps off Muon: token
+    embedding and output head (32000 x 4096 each, bf16), 65 RMSNorm vectors of
+    4096 (bf16); fp32 moments.  HBM-bound: algorithmic bytes per element =
+    read p, g (2+2) + read/write m, v (4+4+4+4) + write p (2) = 22."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as mg
+    g = torch.Generator(device="cuda").manual_seed(4242)
+    sizes = ADAMW_SIZES
+    P = [(torch.randn(n, generator=g, device="cuda") * 0.02).to(torch.bfloat16) for n in sizes]
+    G = [(torch.randn(n, generator=g, device="cuda") * 1e-3).to(torch.bfloat16) for n in sizes]
+    M = [torch.zeros(n, device="cuda") for n in sizes]
+    V = [torch.zeros(n, device="cuda") for n in sizes]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    t = 0
+
+    def step():
+        nonlocal t
+        t += 1
+        mg.muon_adamw_step(P, G, M, V, step=t, **ADAMW_HP)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed pass (value): device events around each step, L2 flushed outside them
+    clk = ClockSampler(0)
+    clk.start()
+    n0 = mg.muon_launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    launches = mg.muon_launch_count() - n0
+    clocks = clk.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    nbytes = 22.0 * sum(sizes)
+
+    # instrumented pass: per-launch events on the library's stream
+    mg.muon_kernel_timing_read()
+    mg.muon_set_kernel_timing(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    mg.muon_set_kernel_timing(False)
+    kl, kms, work = mg.muon_kernel_timing_read()["adamw"]
+    achieved = work / (kms * 1e-3) / 1e9
+
+    # end to end: gradients H2D from pinned host, the step, parameters D2H to pinned host
+    host_g = [x.cpu().pin_memory() for x in G]
+    host_p = [torch.empty_like(x, device="cpu").pin_memory() for x in P]
+    e2e_steps = max(3, min(args.steps, 10))
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        eev[i][0].record()
+        for dg, hg in zip(G, host_g):
+            dg.copy_(hg, non_blocking=True)
+        step()
+        for hp, dp in zip(host_p, P):
+            hp.copy_(dp, non_blocking=True)
+        eev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
+    h2d = sum(x.numel() * x.element_size() for x in G)
+    d2h = sum(x.numel() * x.element_size() for x in P)
+
+    peaks = _peaks()
+    line = {"metric": "AdamW step over the non-matrix parameters (GB/s)", "value": nbytes / (ms * 1e-3) / 1e9,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: seeded torch device RNG",
+            "config": {"workload": ADAMW_WORKLOAD, "elements": sum(sizes), "param_dtype": "bf16",
+                       "state_dtype": "f32", "bytes_per_element": 22, **ADAMW_HP,
+                       "l2": "flushed between timed steps (256 MiB device write outside the step events)"},
+            "roofline": {"kernel": "adamw_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": _measured_traffic("adamw"),
+                         "launches": kl, "peak_source": f"{peaks['source']} hbm_gbs"},
+            "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "what": "gradients H2D from pinned host, muon_adamw_step, parameters D2H to pinned host"},
+            "gpu_launches": launches,
+            "clocks": clocks}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = adamw_cpu_baseline()
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def bench_gpu(args):
@@ -441,6 +611,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return bench_reference(args)
+    if args.workload == ADAMW_WORKLOAD:
+        return bench_adamw(args)
     return bench_gpu(args)
 
 

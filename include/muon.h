@@ -200,6 +200,24 @@ int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_s
                   double* nominal, double* algorithmic);
 
 /*
+ * AdamW step for the parameters that stay off Muon ("MuonX" page, section 2:
+ * hidden 2-D weight matrices use Muon while embeddings and biases stay on
+ * AdamW), all tensors in one launch.  The pages do not print AdamW; this is
+ * the standard decoupled-decay form with 1-based step t:
+ *   m' = b1 m + (1 - b1) g,  v' = b2 v + (1 - b2) g^2,
+ *   p' = p (1 - lr wd) - lr m'/(1 - b1^t) / (sqrt(v'/(1 - b2^t)) + eps).
+ *   params[i], grads[i]      device pointers, numels[i] elements (param_dtype)
+ *   exp_avg[i], exp_avg_sq[i] device pointers, moments (state_dtype), in place
+ * Tensors may have any shape (flattened) and alignment; 16-byte aligned ones
+ * take the vector path.  The pointer tables travel through the library's
+ * workspace, so the first call may allocate.
+ */
+int muon_adamw_step(void* const* params, const void* const* grads, void* const* exp_avg,
+                    void* const* exp_avg_sq, const int64_t* numels, int64_t count,
+                    int param_dtype, int state_dtype, float lr, float beta1, float beta2,
+                    float eps, float wd, int64_t step, void* stream);
+
+/*
  * Owner placement for a multi-rank optimizer step ("DMuon" news page, section 3;
  * "DMuon" summary, section 2.3): each of `count` matrices (shapes ms[i] x ns[i])
  * gets one owner rank in [0, ranks) that runs its update, so that the

@@ -37,7 +37,7 @@ EXPORTS = (
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
-    "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan",
+    "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan", "muon_adamw_step",
 )
 
 _lib = None
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         "muon_group_step": (i32, [vp, f32, f32, f32, i32, vp]),
         "muon_group_destroy": (i32, [vp]),
         "muon_owner_plan": (i32, [i64p, i64p, i64, i32, i32, ip, dp, dp, ip]),
+        "muon_adamw_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                  i64p, i64, i32, i32, f32, f32, f32, f32, f32, i64, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -355,3 +357,26 @@ def muon_owner_plan(shapes, ranks: int, dtype: int = MUON_BF16):
     _check(lib().muon_owner_plan(I64(*[s[0] for s in shapes]), I64(*[s[1] for s in shapes]), k, dtype, ranks,
                                  owners, loads, ctypes.byref(mk), ctypes.byref(meas)), "muon_owner_plan")
     return list(owners)[:k], list(loads)[:ranks], mk.value, bool(meas.value)
+
+
+def muon_adamw_step(params, grads, exp_avgs, exp_avg_sqs, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                    eps: float = 1e-8, wd: float = 0.0, step: int = 1, stream=None):
+    """AdamW over lists of CUDA tensors of any shape (params, moments in place)."""
+    k = len(params)
+    if not (len(grads) == k and len(exp_avgs) == k and len(exp_avg_sqs) == k):
+        raise ValueError("tensor lists must have the same length")
+    if k == 0:
+        return
+    pd, sd = _dtype_code(params[0]), _dtype_code(exp_avgs[0])
+    for i in range(k):
+        for t, nm, dt in ((params[i], "param", pd), (grads[i], "grad", pd), (exp_avgs[i], "exp_avg", sd),
+                          (exp_avg_sqs[i], "exp_avg_sq", sd)):
+            _cuda_contig(t, nm)
+            if _dtype_code(t) != dt or t.numel() != params[i].numel():
+                raise TypeError(f"{nm} {i}: dtype or size mismatch")
+    VP = ctypes.c_void_p * k
+    _check(lib().muon_adamw_step(VP(*[t.data_ptr() for t in params]), VP(*[t.data_ptr() for t in grads]),
+                                 VP(*[t.data_ptr() for t in exp_avgs]), VP(*[t.data_ptr() for t in exp_avg_sqs]),
+                                 (ctypes.c_int64 * k)(*[t.numel() for t in params]), k, pd, sd, float(lr),
+                                 float(beta1), float(beta2), float(eps), float(wd), int(step),
+                                 _stream_ptr(stream)), "muon_adamw_step")

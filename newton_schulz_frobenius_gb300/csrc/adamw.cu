@@ -1,0 +1,82 @@
+// AdamW step for the parameters that stay off Muon ("MuonX" page, section 2:
+// embeddings and biases keep AdamW), every tensor of the call in one launch.
+//
+// The host cuts the tensors into chunks of CHUNK_ELEMS elements; CTA k
+// handles chunk k: 16-byte vector loads and stores where the tensor's
+// pointers allow it, scalar otherwise.  Per element it reads p, g, m, v and
+// writes p, m, v once, so the kernel is bound by HBM bandwidth.
+//   m' = b1 m + (1 - b1) g,  v' = b2 v + (1 - b2) g^2
+//   p' = p - [ lr wd p + (lr / bc1) m' / (sqrt(v') / sqrt(bc2) + eps) ]
+// with bc1 = 1 - b1^t and bc2 = 1 - b2^t computed on the host in double.  The
+// bracket is formed first and subtracted once: a factor (1 - lr wd) rounded to
+// fp32 would carry an error of the same sign into every element, comparable
+// to the update itself at small lr.
+#include "muon_internal.cuh"
+#include "epilogue.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int AT = 256;
+
+__device__ __forceinline__ void adam8(const AdamArgs& a, float (&p)[8], const float (&g)[8], float (&m)[8],
+                                      float (&v)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] = fmaf(a.beta1, m[k], (1.0f - a.beta1) * g[k]);
+        v[k] = fmaf(a.beta2, v[k], (1.0f - a.beta2) * g[k] * g[k]);
+        const float denom = fmaf(sqrtf(v[k]), a.inv_sqrt_bc2, a.eps);
+        p[k] -= fmaf(a.lr_wd, p[k], a.step_size * (m[k] / denom));
+    }
+}
+
+__global__ void __launch_bounds__(AT) adamw_kernel(const __grid_constant__ AdamArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const AdamChunk ch = a.chunks[blockIdx.x];
+    const AdamTensor t = a.tensors[ch.tensor];
+    const int pd = a.param_dtype, sd = a.state_dtype;
+    const bool vec = t.vec_ok && (ch.start % 8 == 0);
+    for (int i = threadIdx.x * 8; i < ch.len; i += AT * 8) {
+        const int64_t off = ch.start + i;
+        const int cnt = min(8, ch.len - i);
+        float p[8], g[8], m[8], v[8];
+        if (vec && cnt == 8) {
+            load_row_run<8>(t.p, off, p, pd);
+            load_row_run<8>(t.g, off, g, pd);
+            load_row_run<8>(t.m, off, m, sd);
+            load_row_run<8>(t.v, off, v, sd);
+            adam8(a, p, g, m, v);
+            store_row_run<8>(t.p, off, p, pd);
+            store_row_run<8>(t.m, off, m, sd);
+            store_row_run<8>(t.v, off, v, sd);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const bool in = k < cnt;
+                p[k] = in ? ld_elem(t.p, off + k, pd) : 0.f;
+                g[k] = in ? ld_elem(t.g, off + k, pd) : 0.f;
+                m[k] = in ? ld_elem(t.m, off + k, sd) : 0.f;
+                v[k] = in ? ld_elem(t.v, off + k, sd) : 0.f;
+            }
+            adam8(a, p, g, m, v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k < cnt) {
+                    st_elem(t.p, off + k, p[k], pd);
+                    st_elem(t.m, off + k, m[k], sd);
+                    st_elem(t.v, off + k, v[k], sd);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_adamw(const AdamArgs& a, int nchunks, cudaStream_t s) {
+    return launch_pdl(adamw_kernel, dim3(nchunks), dim3(AT), 0, s, a);
+}
+
+}  // namespace muon

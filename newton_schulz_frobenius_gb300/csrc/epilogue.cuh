@@ -197,11 +197,13 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, const MatEntry&
     const int od = a.out_dtype;
     const float lr = a.hyper ? a.hyper[0] : a.lr;
     const float wd = a.hyper ? a.hyper[2] : a.wd;
-    const float keep = 1.0f - lr * wd;
+    const float lrwd = lr * wd;
     const float step = lr * a.scale;
     if (a.epi == EPI_UPDATE) {
+        // W - (lr wd W + step O): the decrement is formed first and subtracted
+        // once, so an fp32-rounded factor (1 - lr wd) never scales every W
 #pragma unroll
-        for (int j = 0; j < W; ++j) v[j] = fmaf(-step, v[j], keep * g[j]);
+        for (int j = 0; j < W; ++j) v[j] = g[j] - fmaf(lrwd, g[j], step * v[j]);
     }
     if (!e.trans) {
         const int64_t off = (int64_t)r * a.N + c0;

@@ -115,6 +115,32 @@ struct SmallArgs {
 bool small_ns_fits(int m, int n, int nseg, const int* segs);
 cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s);
 
+// AdamW over many tensors in one launch (adamw.cu).
+constexpr int ADAM_CHUNK_ELEMS = 8192;
+struct AdamTensor {
+    void* p;
+    const void* g;
+    void* m;
+    void* v;
+    int vec_ok;             // all four pointers 16-byte aligned
+    int pad;
+};
+struct AdamChunk {
+    int64_t start;          // first element of the chunk within its tensor
+    int tensor;
+    int len;
+};
+struct AdamArgs {
+    const AdamTensor* tensors;
+    const AdamChunk* chunks;
+    int param_dtype, state_dtype;
+    float beta1, beta2, eps;
+    float lr_wd;            // lr * wd
+    float step_size;        // lr / (1 - beta1^t)
+    float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
+};
+cudaError_t launch_adamw(const AdamArgs& a, int nchunks, cudaStream_t s);
+
 // inv[b] = 1 / (sqrt(sum(partials[b][:])) + eps); flags a non-finite sum.
 cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
                                  float* inv, int* status, cudaStream_t s);
@@ -154,7 +180,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Kernel-class bookkeeping for launch counting and optional event timing.
 enum KernelClass : int {
     KC_PREP = 0, KC_NORM = 1, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
-    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_COUNT = 9
+    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_ADAMW = 9, KC_COUNT = 10
 };
 void note_launch_begin(int kclass, cudaStream_t s);
 void note_launch_end(int kclass, double work, cudaStream_t s);

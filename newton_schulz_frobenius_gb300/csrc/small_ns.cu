@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
                 // O (rows < m, columns < n): update the caller's W or write O
                 const float lr = a.hyper ? a.hyper[0] : a.lr;
                 const float wd = a.hyper ? a.hyper[2] : a.wd;
-                const float keep = 1.0f - lr * wd;
+                const float lrwd = lr * wd;
                 const float stepc = lr * a.scale;
                 const int od = a.param_dtype;
                 for (int k = hw; k < nck * 2; k += 2) {
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
                             else
                                 for (int j = 0; j < 32; ++j) w[j] = j < nv ? ld_elem(e.w, off + j, od) : 0.f;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = fmaf(-stepc, v[j], keep * w[j]);
+                            for (int j = 0; j < 32; ++j) v[j] = w[j] - fmaf(lrwd, w[j], stepc * v[j]);
                         }
                         if (nv == 32) store_row_run<32>(e.w, off, v, od);
                         else
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             if (j < nv) {
-                                const float o = a.mode == 0 ? fmaf(-stepc, v[j], keep * w[j]) : v[j];
+                                const float o = a.mode == 0 ? w[j] - fmaf(lrwd, w[j], stepc * v[j]) : v[j];
                                 st_elem(e.w, (int64_t)(c0 + j) * a.m + r, o, od);
                             }
                         }

@@ -1,6 +1,9 @@
 """Plain fp64 CPU oracle of the AdamW step for the parameters that stay off
-Muon (embeddings, biases, norms): TEST INFRASTRUCTURE ONLY, imported by
-``tests/`` alone.  Pinned by ``tests/test_adamw_oracle_pins.py``.
+Muon (embeddings, biases, norms).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/`` and the CPU-baseline and reference
+legs of ``bench.py`` may import this module; the library never calls it and
+shares no code with it.  Pinned by ``tests/test_adamw_oracle_pins.py``.
 
 Source: "MuonX: DMuon 调整多卡分工, Gram NS 降低计算量" (CSDN), section 2 — the
 hidden 2-D weight matrices are updated by Muon while embeddings and biases stay
