@@ -226,6 +226,23 @@ def test_small_bucket_fused_step(mg, monkeypatch, path, mom_dtype):
         assert m_ok
 
 
+@pytest.mark.parametrize("mom_dtype", ["bf16", "f32"])
+def test_fused_256_rows_step(mg, monkeypatch, mom_dtype):
+    """Plain NS of 128 < m <= 256, n <= 256 matrices in the 256-row form of the
+    one-CTA-per-matrix kernel (A kept as three symmetric blocks, A01 read
+    transposed): square, ragged and transposed shapes, two steps."""
+    monkeypatch.setenv("MUON_SMALL", "1")
+    shapes = [(256, 256), (192, 256), (256, 192), (256, 200), (130, 130), (256, 256)]
+    before = mg.muon_launch_count()
+    res = _step_case(mg, shapes, "bf16", mom_dtype, mg.MUON_PATH_PLAIN, True, 8600, 0.0316, steps=2)
+    # buckets 256x256, 192x256, 200x256, 130x130: one launch each per step
+    assert mg.muon_launch_count() - before == 8
+    for err, q, m_ok, pname in res:
+        assert pname == "plain"
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+
+
 def test_small_fused_zero_and_tiny(mg, monkeypatch):
     monkeypatch.setenv("MUON_SMALL", "1")
     for shape in ((1, 8), (3, 5), (64, 64)):
