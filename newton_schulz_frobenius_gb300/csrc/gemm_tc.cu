@@ -23,7 +23,13 @@
 // products, TF32 on fp32 storage (kind::tf32, K = 8) for the m x m Gram-space
 // products; either way one k-block is 128 bytes of every operand row.
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
-// of tile t overlaps the main loop of tile t+1.  Every mbarrier wait is bounded:
+// of tile t overlaps the main loop of tile t+1.
+// Paired launches (PAIR, 128 x 256 tiles): 2-CTA clusters take row blocks 2p
+// and 2p+1 of one column tile; each CTA loads its own A and half of the shared
+// B tile with a cluster-multicast TMA into both CTAs, and each MMA issuer
+// commits to the stage's empty barrier in both CTAs (count 2), so neither
+// refills a stage the other still reads.  Same tiles and K order, so the
+// results equal the unpaired kernel's bit for bit.  Every mbarrier wait is bounded:
 // after WAIT_LIMIT_NS it sets an abort flag and the status word, waits (again
 // bounded) for its own copies and products in flight, frees TMEM and returns.
 #include "muon_internal.cuh"
@@ -31,6 +37,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace muon {
@@ -142,6 +149,41 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Multicast variant: the box lands at the same shared-memory offset in every
+// CTA of ctaMask, and each of their mbarriers at `bar`'s offset receives the
+// byte count.  Used only between the two CTAs of a cluster on this GPU.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                               int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_idx() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs of the cluster arrives and waits.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
                  : "memory");
@@ -166,6 +208,15 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Arrives on the mbarrier at `bar`'s offset in every CTA of ctaMask once the
+// products issued so far by this thread complete.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -239,13 +290,28 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 // sym == 1: square 128 x 128 tiles with tn <= tm (lower triangle).
 // sym == 2: 128 x 256 tiles that meet the lower triangle, tn <= tm / 2; row
 // blocks 2p and 2p+1 both hold p + 1 tiles, so p(p+1) tiles precede block 2p.
+// pair != 0 (sym 0 or 2): a unit is the two tiles (2p, tn) and (2p+1, tn),
+// one per CTA of a cluster (rank selects the row block); tiles_m then counts
+// row-block pairs, and in sym 2 pair p holds tn = 0 .. p.
 struct TileSched {
-    int tiles_m, tiles_n, per_batch, total, sym;
+    int tiles_m, tiles_n, per_batch, total, sym, pair;
 
-    __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn) const {
+    __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn, int rank = 0) const {
         b = t / per_batch;
         const int l = t - b * per_batch;
-        if (sym == 2) {
+        if (pair) {
+            int p;
+            if (sym) {
+                p = (int)((sqrtf(8.0f * (float)l + 1.0f) - 1.0f) * 0.5f);
+                while (p * (p + 1) / 2 > l) --p;
+                while ((p + 1) * (p + 2) / 2 <= l) ++p;
+                tn = l - p * (p + 1) / 2;
+            } else {
+                p = l % tiles_m;
+                tn = l / tiles_m;
+            }
+            tm = 2 * p + rank;
+        } else if (sym == 2) {
             int p = (int)((sqrtf(4.0f * (float)l + 1.0f) - 1.0f) * 0.5f);
             while (p * (p + 1) > l) --p;
             while ((p + 1) * (p + 2) <= l) ++p;
@@ -269,7 +335,7 @@ struct TileSched {
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int BN, bool B_KMAJOR, bool TF32>
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ GemmArgs args, const TileSched sched) {
@@ -296,11 +362,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Paired launches: the two CTAs of a cluster take the two row blocks of a
+    // unit; each loads its own A and half of the shared B tile, multicast to
+    // both, so a stage may be refilled only when both CTAs have consumed it.
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int unit0 = PAIR ? (int)cluster_idx() : (int)blockIdx.x;
+    const int ustep = PAIR ? (int)cluster_count() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);
         }
         mbar_init(accf0, 1);
         mbar_init(accf0 + 8, 1);
@@ -320,6 +392,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();     // the peer's barriers exist before anything targets them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = (args.K + KE - 1) / KE;
@@ -335,9 +408,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+            for (int t = unit0; t < sched.total && ok; t += ustep) {
                 int b, tm, tn;
-                sched.decode(t, b, tm, tn);
+                sched.decode(t, b, tm, tn, rank);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, args.status)) {
                         ok = false;
@@ -346,7 +419,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
-                    if (B_KMAJOR) {
+                    if (PAIR) {
+                        // this CTA's half of B, into both CTAs
+                        if (B_KMAJOR) {
+                            tma_load_3d_mc(smem_u32(sB + stage * C::B_BYTES + rank * (BN / 2) * BK_BYTES), &tmB, fb,
+                                           kb * KE, tn * BN + rank * (BN / 2), b, (uint16_t)0x3);
+                        } else {
+#pragma unroll
+                            for (int q = rank * (BN / 128); q < (rank + 1) * (BN / 128); ++q)
+                                tma_load_3d_mc(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmB, fb,
+                                               tn * BN + q * 64, kb * BK, b, (uint16_t)0x3);
+                        }
+                    } else if (B_KMAJOR) {
                         tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN, b);
                     } else {
 #pragma unroll
@@ -377,7 +461,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int acc = 0;
             uint32_t aphase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+            for (int t = unit0; t < sched.total && ok; t += ustep) {
                 if (!wait_bounded(acce0 + 8 * acc, aphase ^ 1u, abort_flag, args.status)) {
                     ok = false;
                     break;
@@ -401,7 +485,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         if (TF32) tc_mma_tf32(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
                         else tc_mma_bf16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty0 + 8 * stage);
+                    if (PAIR) tc_commit_mc(empty0 + 8 * stage, (uint16_t)0x3);
+                    else tc_commit(empty0 + 8 * stage);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -427,9 +512,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         constexpr int HALF_COLS = BN / 2;
         int acc = 0;
         uint32_t aphase = 0;
-        for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+        for (int t = unit0; t < sched.total; t += ustep) {
             int b, tm, tn;
-            sched.decode(t, b, tm, tn);
+            sched.decode(t, b, tm, tn, rank);
             if (args.epi == EPI_UPDATE) {
                 // the update reads the caller's W: start pulling this tile's
                 // part into L2 while the products are still accumulating
@@ -442,7 +527,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (r < args.M)
                         for (int c = cbeg; c < min(cbeg + HALF_COLS, args.N); c += 128 / ob)
                             prefetch_l2(wb + ((int64_t)r * args.N + c) * ob);
-                } else {
+                } else if (tm * BM + q * 32 < args.M) {
                     for (int c = cbeg + lane; c < min(cbeg + HALF_COLS, args.N); c += 32)
                         prefetch_l2(wb + ((int64_t)c * args.M + tm * BM + q * 32) * ob);
                 }
@@ -488,6 +573,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();     // no multicast copy or remote arrive targets this CTA any more
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -531,14 +617,31 @@ bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_KMAJOR, bool TF32>
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     using C = Cfg<BN>;
+    auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, B_KMAJOR, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::SMEM_BYTES);
+    static int max_clusters = 0;
+    std::call_once(attr_once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (attr_err == cudaSuccess && PAIR) {
+            // how many 2-CTA clusters of this kernel fit on the device at once
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (num_sms / 2));
+            cfg.blockDim = dim3(NTHREADS);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+            if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+        }
     });
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -547,8 +650,9 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if (!make_map(&mA, a.A, TF32, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda,
                   (uint64_t)a.strideA, KE, BM))
         return cudaErrorInvalidValue;
+    // a paired K-major B tile arrives as two halves of BN / 2 rows
     bool okB = B_KMAJOR ? make_map(&mB, a.B, TF32, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
-                                   (uint64_t)a.ldb, (uint64_t)a.strideB, KE, BN)
+                                   (uint64_t)a.ldb, (uint64_t)a.strideB, KE, PAIR ? BN / 2 : BN)
                         : make_map(&mB, a.B, TF32, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch,
                                    (uint64_t)a.ldb, (uint64_t)a.strideB, 64, BK);
     if (!okB) return cudaErrorInvalidValue;
@@ -557,16 +661,39 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     sc.tiles_m = (a.M + BM - 1) / BM;
     sc.tiles_n = (a.N + BN - 1) / BN;
     sc.sym = a.symmetric ? (BN == 256 ? 2 : 1) : 0;
-    if (sc.sym == 2) {
+    sc.pair = PAIR ? 1 : 0;
+    if (PAIR) {
+        const int pm = (sc.tiles_m + 1) / 2;
+        sc.tiles_m = pm;
+        sc.per_batch = sc.sym ? pm * (pm + 1) / 2 : pm * sc.tiles_n;
+    } else if (sc.sym == 2) {
         sc.per_batch = 0;
         for (int tm = 0; tm < sc.tiles_m; ++tm) sc.per_batch += tm / 2 + 1;
     } else {
         sc.per_batch = a.symmetric ? sc.tiles_m * (sc.tiles_m + 1) / 2 : sc.tiles_m * sc.tiles_n;
     }
     sc.total = sc.per_batch * a.batch;
-    const int grid = sc.total < num_sms ? sc.total : num_sms;
-    return launch_pdl(gemm_tc_kernel<BN, B_KMAJOR, TF32>, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA,
-                      mB, a, sc);
+    if (!PAIR) {
+        const int grid = sc.total < num_sms ? sc.total : num_sms;
+        return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, a, sc);
+    }
+    int clusters = std::min(num_sms / 2, max_clusters);
+    if (sc.total < clusters) clusters = sc.total;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB, a, sc);
 }
 
 }  // namespace tc
@@ -584,18 +711,25 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
         return cudaErrorInvalidValue;
     if ((int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + 127) / 128) > (int64_t)1 << 30)
         return cudaErrorInvalidValue;
-    // symmetric products default to 128 x 128 tiles, the others to 128 x 256
+    // symmetric products default to 128 x 128 tiles, the others to 128 x 256;
+    // 128 x 256 tiles may run as 2-CTA clusters sharing the B tile
     const int bn = a.symmetric ? (a.tile_n == 256 ? 256 : 128) : (a.tile_n == 128 ? 128 : 256);
+    const bool pair = (bn == 256) && (a.pair > 0 || (a.pair < 0 && !a.symmetric));
     if (tf32) {
-        return bn == 128 ? tc::launch_impl<128, true, true>(a, num_sms, s)
-                         : tc::launch_impl<256, true, true>(a, num_sms, s);
+        if (bn == 128) return tc::launch_impl<128, true, true, false>(a, num_sms, s);
+        return pair ? tc::launch_impl<256, true, true, true>(a, num_sms, s)
+                    : tc::launch_impl<256, true, true, false>(a, num_sms, s);
     }
     if (bn == 128) {
-        return a.b_kmajor ? tc::launch_impl<128, true, false>(a, num_sms, s)
-                          : tc::launch_impl<128, false, false>(a, num_sms, s);
+        return a.b_kmajor ? tc::launch_impl<128, true, false, false>(a, num_sms, s)
+                          : tc::launch_impl<128, false, false, false>(a, num_sms, s);
     }
-    return a.b_kmajor ? tc::launch_impl<256, true, false>(a, num_sms, s)
-                      : tc::launch_impl<256, false, false>(a, num_sms, s);
+    if (pair) {
+        return a.b_kmajor ? tc::launch_impl<256, true, false, true>(a, num_sms, s)
+                          : tc::launch_impl<256, false, false, true>(a, num_sms, s);
+    }
+    return a.b_kmajor ? tc::launch_impl<256, true, false, false>(a, num_sms, s)
+                      : tc::launch_impl<256, false, false, false>(a, num_sms, s);
 }
 
 }  // namespace muon

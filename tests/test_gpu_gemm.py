@@ -159,3 +159,37 @@ def test_poly_tf32(mg):
     ref = a * torch.eye(m, device="cuda", dtype=torch.float64) + b * Gd + c * torch.matmul(Gd, Gd)
     err = ((P.double() - ref).norm() / ref.norm()).item()
     assert err < 2e-3, err
+
+
+@pytest.mark.parametrize("kind,M,N,K,batch", [
+    ("kmajor", 256, 512, 320, 2), ("kmajor", 384, 1000, 136, 1), ("kmajor", 200, 264, 72, 3),
+    ("sym", 896, 896, 136, 1), ("sym", 384, 384, 1000, 2), ("sym", 260, 260, 200, 1),
+    ("mn", 200, 304, 136, 2), ("mn", 640, 1000, 512, 1), ("mn", 384, 256, 256, 3),
+    ("tf32", 384, 384, 520, 2), ("tf32sym", 896, 896, 136, 1)])
+def test_paired_products(mg, monkeypatch, kind, M, N, K, batch):
+    """128 x 256 tiles run as 2-CTA clusters whose CTAs share the B tile by
+    multicast (row blocks 2p and 2p+1; an odd last block reads zeros and stores
+    nothing).  Same tiles and K order as the unpaired kernel, so the results
+    are bitwise equal to it, and they match the fp64 product."""
+    tf32 = kind.startswith("tf32")
+    dtype = torch.float32 if tf32 else torch.bfloat16
+    sym = kind in ("sym", "tf32sym")
+    kmajor = kind != "mn"
+    A = _rand((batch, M, K), dtype, 21, scale=1.0 / np.sqrt(K))
+    B = A if sym else (_rand((batch, N, K), dtype, 22) if kmajor else _rand((batch, K, N), dtype, 23))
+    out = []
+    for pair in ("0", "1"):
+        monkeypatch.setenv("MUON_PAIR", pair)
+        C = torch.full((batch, M, N), float("nan"), dtype=dtype, device="cuda")
+        mg.muon_debug_gemm(A, B, C, b_kmajor=kmajor, symmetric=sym, tile_n=256, tf32=tf32)
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+        out.append(C)
+    assert torch.equal(out[0], out[1])
+    Bt = B.double().transpose(1, 2) if kmajor else B.double()
+    ref = torch.matmul(A.double(), Bt)
+    if tf32:
+        err = ((out[1].double() - ref).norm() / ref.norm()).item()
+        assert err < 2e-3, err
+    else:
+        _check(out[1], ref, dtype)
