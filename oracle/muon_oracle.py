@@ -61,12 +61,29 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u32.view(np.float32).astype(np.float64)
 
 
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 storage bits -> exact fp64 values, decoded from the
+    format's definition: sign bit, 5-bit exponent (bias 15), 10-bit fraction;
+    exponent 0 holds the subnormals fraction * 2^-24, exponent 31 inf/nan."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(u >> 15, -1.0, 1.0)
+    e = (u >> 10) & 0x1F
+    f = (u & 0x3FF).astype(np.float64)
+    normal = np.ldexp(1024.0 + f, np.maximum(e, 1) - 25)       # (1 + f/1024) * 2^(e-15)
+    sub = np.ldexp(f, -24)
+    val = np.where(e == 0, sub, normal)
+    val = np.where(e == 31, np.where(f == 0, np.inf, np.nan), val)
+    return sign * val
+
+
 def to_f64(data: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact fp64 view of stored bytes (fp32 array or bf16 uint16 bits)."""
+    """Exact fp64 view of stored bytes (fp32 array, bf16 or fp16 uint16 bits)."""
     if dtype == "f32":
         return np.asarray(data, dtype=np.float32).astype(np.float64)
     if dtype == "bf16":
         return bf16_bits_to_f64(data)
+    if dtype == "f16":
+        return f16_bits_to_f64(data)
     raise ValueError(dtype)
 
 
@@ -81,17 +98,46 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(np.rint(np.ldexp(mant, 8)), expo - 8)   # rint: ties to even
 
 
+def round_f16(x: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest binary16 value (ties to even), returned as fp64.
+
+    Eleven significant bits for |x| >= 2^-14; below that the subnormal
+    quantum 2^-24 applies; magnitudes that round beyond 65504 become inf.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    mant, expo = np.frexp(x)                          # |mant| in [0.5, 1)
+    q = np.maximum(expo - 11, -24)                    # exponent of the last kept bit
+    r = np.ldexp(np.rint(np.ldexp(x, -q)), q)         # rint: ties to even
+    return np.where(np.abs(r) > 65504.0, np.copysign(np.inf, x), r)
+
+
 def round_f32(x: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
 
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
-    return round_f32(x) if dtype == "f32" else round_bf16(x)
+    if dtype == "f32":
+        return round_f32(x)
+    if dtype == "f16":
+        return round_f16(x)
+    return round_bf16(x)
 
 
 def bf16_bits_from_f64(x: np.ndarray) -> np.ndarray:
     """Storage bits of values that are already exact bf16 numbers."""
     return (np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def f16_bits_from_f64(x: np.ndarray) -> np.ndarray:
+    """Storage bits of values that are already exact binary16 numbers."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def bits_from_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage array (fp32 values or 16-bit bits) of values exact in `dtype`."""
+    if dtype == "f32":
+        return np.asarray(x, dtype=np.float64).astype(np.float32)
+    return f16_bits_from_f64(x) if dtype == "f16" else bf16_bits_from_f64(x)
 
 
 # ---------------------------------------------------------------------------

@@ -395,3 +395,46 @@ def test_planted_mistake_is_caught(monkeypatch, name, target, mutant):
     assert _all_pins_hold()
     monkeypatch.setattr(orc, target, mutant)
     assert not _all_pins_hold(), name
+
+
+# ---------------------------------------------------------------------------
+# binary16 storage (the fp16 working type): the decoder and the rounding are
+# written from the IEEE format; numpy's own half conversions are independent
+# implementations of the same definition.
+# ---------------------------------------------------------------------------
+
+def test_f16_decode_all_bit_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    mine = orc.f16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    assert np.array_equal(mine[finite], ref[finite])
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def test_f16_rounding_matches_ieee():
+    r = orc.round_f16
+    # ties to even at 1, above the largest finite value, and in the subnormals
+    assert r(np.array(1.0 + 2.0 ** -11)) == 1.0
+    assert r(np.array(1.0 + 3 * 2.0 ** -11)) == 1.0 + 2.0 ** -9
+    assert r(np.array(65519.0)) == 65504.0
+    assert np.isinf(r(np.array(65520.0))) and r(np.array(-65520.0)) < 0
+    assert r(np.array(2.0 ** -25)) == 0.0
+    assert r(np.array(3 * 2.0 ** -26)) == 2.0 ** -24
+    assert r(np.array(2.0 ** -14 - 2.0 ** -25)) == 2.0 ** -14     # tie between the last subnormal and 2^-14
+    # random values over the whole range against numpy's double -> half
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.standard_normal(200000) * np.exp2(rng.uniform(-30, 17, 200000)),
+        (rng.integers(-2048, 2048, 20000) + 0.5) * np.exp2(rng.integers(-24, 5, 20000)).astype(np.float64)])
+    want = x.astype(np.float16).astype(np.float64)
+    got = r(x)
+    same = (got == want) | (np.isinf(got) & np.isinf(want) & (np.sign(got) == np.sign(want)))
+    assert same.all(), x[~same][:5]
+
+
+def test_f16_storage_roundtrip():
+    x = orc.round_f16(np.linspace(-3, 3, 1001))
+    assert np.array_equal(orc.to_f64(orc.f16_bits_from_f64(x), "f16"), x)
+    assert np.array_equal(orc.round_to(x, "f16"), x)

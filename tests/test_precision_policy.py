@@ -1,4 +1,4 @@
-"""Evidence for the bf16 path's precision policy, on the CPU.
+"""Evidence for the precision policy of the 16-bit paths, on the CPU.
 
 The NS iteration is simulated with the storage roundings of the CUDA path
 (bf16 X, fp32-accumulated products, Gram-space matrices either bf16 or TF32,
@@ -83,3 +83,65 @@ def test_plain_gains_nothing_from_tf32():
 
 def test_polynomial_needs_one_rounded_g():
     assert _err((1, 64), (1, 1, 1, 1, 1), bf16, lin_fp32=True) > 2 * _err((1, 64), (1, 1, 1, 1, 1), bf16)
+
+
+# ---------------------------------------------------------------------------
+# fp16 working type (ten stored mantissa bits, range to 65504, subnormals
+# below 2^-14): X and every Gram-space matrix in fp16, products accumulated in
+# fp32.  X is stored already divided by ||U||_F; storing the unscaled U, as
+# the bf16 path does, would put small gradients into fp16's subnormals.
+# ---------------------------------------------------------------------------
+
+f16 = orc.round_f16
+
+
+def simulate_f16(U, segs, prescale=True, coeffs=orc.QUINTIC):
+    a, b, c = coeffs
+    X, tr = orc.orient(U)
+    inv = 1.0 / (np.sqrt((X * X).sum()) + orc.EPS)
+    X = f16(X * inv) if prescale else f16(X)
+    m = X.shape[0]
+    I = np.eye(m)
+    for si, L in enumerate(segs):
+        al = 1.0 if (prescale or si > 0) else inv
+        G = f16(f32(X @ X.T) * al * al)
+        Q = None
+        for j in range(1, L + 1):
+            P = f16(a * I + b * G + c * f32(G @ G))
+            Q = P if j == 1 else f16(f32(P @ Q))
+            if j < L:
+                G = f16(f32(f16(f32(P @ G)) @ P))
+        X = f16(f32(Q @ X) * al)
+    return X.T if tr else X
+
+
+def _err16(shape, segs, std=0.03, prescale=True, seeds=(200, 201), src="f16"):
+    worst = 0.0
+    for s in seeds:
+        U = orc.to_f64(gen_matrix(s, 0, *shape, std, src).data, src)
+        path = "plain" if all(L == 1 for L in segs) else "gram"
+        O = orc.orthogonalize(U, path, segments=segs if path == "gram" else (2, 2, 1))
+        worst = max(worst, np.linalg.norm(simulate_f16(U, segs, prescale) - O) / np.linalg.norm(O))
+    return worst
+
+
+@pytest.mark.parametrize("shape,segs", [
+    ((128, 512), (2, 3)), ((128, 512), (2, 2, 1)), ((256, 1024), (2, 3)), ((130, 130), (2, 3)),
+    ((37, 200), (2, 2, 1)), ((96, 300), (1, 1, 1, 1, 1))])
+def test_f16_meets_the_bar_with_f16_gram_space(shape, segs):
+    e16 = _err16(shape, segs)
+    assert e16 < 0.01, e16
+
+
+@pytest.mark.parametrize("shape,segs", [((128, 512), (2, 2, 1)), ((256, 1024), (2, 2, 1)), ((96, 300), (1, 1, 1, 1, 1))])
+def test_f16_is_more_accurate_than_bf16(shape, segs):
+    sq = bf16 if shape[0] >= 128 and shape[1] >= 2 * shape[0] else tf32
+    assert _err16(shape, segs) < 0.5 * _err(shape, segs, sq)
+
+
+def test_f16_needs_the_prescaled_x_for_small_gradients():
+    # bf16 gradients of size 1e-6 with fp16 NS: unscaled in fp16 they would be
+    # subnormal (spacing 2^-24 = 6e-8); divided by ||U|| first they are not
+    scaled = _err16((64, 256), (2, 2, 1), std=1e-6, prescale=True, src="bf16")
+    unscaled = _err16((64, 256), (2, 2, 1), std=1e-6, prescale=False, src="bf16")
+    assert scaled < 0.005 and unscaled > 0.01 and unscaled > 5 * scaled, (scaled, unscaled)

@@ -82,15 +82,23 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f32_to_f16_bits(x32: np.ndarray) -> np.ndarray:
+    """Round fp32 values to IEEE binary16 (nearest, ties to even, numpy's
+    conversion); returns uint16 bits."""
+    return np.ascontiguousarray(x32, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
 @dataclass
 class HostMatrix:
     """One generated matrix: raw storage bytes plus its shape and dtype name."""
     rows: int
     cols: int
-    dtype: str                 # "f32" or "bf16"
-    data: np.ndarray           # float32 (f32) or uint16 bits (bf16), shape (rows, cols)
+    dtype: str                 # "f32", "bf16" or "f16"
+    data: np.ndarray           # float32 (f32) or uint16 bits (bf16, f16), shape (rows, cols)
 
     def as_f32(self) -> np.ndarray:
+        if self.dtype == "f16":
+            return self.data.view(np.float16).astype(np.float32)
         return self.data if self.dtype == "f32" else bf16_bits_to_f32(self.data)
 
 
@@ -101,6 +109,8 @@ def gen_matrix(seed: int, stream: int, rows: int, cols: int, std: float, dtype: 
         return HostMatrix(rows, cols, dtype, x)
     if dtype == "bf16":
         return HostMatrix(rows, cols, dtype, f32_to_bf16_bits(x).reshape(rows, cols))
+    if dtype == "f16":
+        return HostMatrix(rows, cols, dtype, f32_to_f16_bits(x).reshape(rows, cols))
     raise ValueError(dtype)
 
 
