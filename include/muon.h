@@ -54,7 +54,12 @@ typedef enum {
     MUON_ENOTSUP = -7      /* no sm_103a device / feature unavailable */
 } muon_status;
 
-typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+/* Storage types.  MUON_F16 (IEEE binary16) is the working type of the
+ * open-source Gram NS the "MuonX" page (section 3.2) mentions, which splits the
+ * five steps into segments of 2 and 3; MuonX itself keeps bf16 with 2+2+1.
+ * Both are reachable: the segment list through muon_set_ns_config, the
+ * working type through the storage type or muon_set_ns_precision. */
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1, MUON_F16 = 2 } muon_dtype;
 
 typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muon_path;
 
@@ -65,8 +70,10 @@ typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muo
  *              Read as the NS input U, overwritten with O = NS(U/(||U||_F+eps)).
  *              Each matrix is normalised on its own.  A matrix with m > n is
  *              processed as its transpose; the result is written back untransposed.
- *   dtype      MUON_F32 (fp32 path: fp32 FFMA products) or MUON_BF16 (bf16
- *              tensor-core products, fp32 accumulation, bf16 intermediates).
+ *   dtype      storage type of the matrices: MUON_F32 (fp32 path: fp32 FFMA
+ *              products), MUON_BF16 or MUON_F16 (16-bit tensor-core products,
+ *              fp32 accumulation, 16-bit intermediates of the NS precision:
+ *              the storage type unless muon_set_ns_precision chose the other).
  *   coeffs     (a, b, c) of one NS step X <- aX + (bA + cA^2)X, A = XX^T.
  *   steps      number of NS steps (>= 1).
  *   segments   NULL or num_segments == 0: plain NS.  Otherwise Gram NS with
@@ -117,8 +124,10 @@ int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, int64_t batch
  *   lr, beta, wd, nesterov   hyper-parameters of the update above.
  * Matrices are bucketed by oriented shape; each bucket runs the NS path chosen
  * by muon_set_ns_config (auto: measured-cost autotune per shape, cached).
- * param_dtype MUON_F32 selects the fp32 path, MUON_BF16 the tensor-core path;
- * mom_dtype may be either.  Arrays are host arrays of length `count`.
+ * param_dtype MUON_F32 selects the fp32 path, MUON_BF16 or MUON_F16 the
+ * tensor-core path (NS in the precision muon_set_ns_precision selects, by
+ * default the parameters' own); mom_dtype may be any of the three.  Arrays are
+ * host arrays of length `count`.
  */
 int muon_step(void* const* params, const void* const* grads, void* const* moms,
               const int64_t* ms, const int64_t* ns, int64_t count,
@@ -157,6 +166,17 @@ int muon_group_destroy(muon_group* group);
  */
 int muon_set_ns_config(const float coeffs[3], int steps, const int* segments,
                        int num_segments, int path);
+
+/*
+ * Working precision of NS for 16-bit parameters (process-wide, like the
+ * configuration above): -1 (default) uses the parameters' own type, MUON_BF16
+ * or MUON_F16 forces that type for X and the m x m iteration matrices.  fp16
+ * keeps three more mantissa bits than bf16 at the cost of range, so its path
+ * stores X already divided by ||U||_F (the momentum kernel runs twice: first
+ * the sum of squares, then momentum and the scaled U).  fp32 parameters always
+ * take the fp32 path.  Returns MUON_EDTYPE for any other value.
+ */
+int muon_set_ns_precision(int dtype);
 
 /*
  * Measured-cost autotune ("DMuon" news page, section 3; "DMuon" summary,
@@ -206,8 +226,10 @@ int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_s
  * the standard decoupled-decay form with 1-based step t:
  *   m' = b1 m + (1 - b1) g,  v' = b2 v + (1 - b2) g^2,
  *   p' = p (1 - lr wd) - lr m'/(1 - b1^t) / (sqrt(v'/(1 - b2^t)) + eps).
- *   params[i], grads[i]      device pointers, numels[i] elements (param_dtype)
- *   exp_avg[i], exp_avg_sq[i] device pointers, moments (state_dtype), in place
+ *   params[i], grads[i]      device pointers, numels[i] elements (param_dtype:
+ *                            MUON_F32, MUON_BF16 or MUON_F16)
+ *   exp_avg[i], exp_avg_sq[i] device pointers, moments (state_dtype: MUON_F32 or
+ *                            MUON_BF16; fp16 lacks the range of v), in place
  * Tensors may have any shape (flattened) and alignment; 16-byte aligned ones
  * take the vector path.  The pointer tables travel through the library's
  * workspace, so the first call may allocate.
@@ -264,10 +286,10 @@ int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms,
  *   values, mirrored (C[j][i] = C[i][j]); valid when the exact product is
  *   symmetric.  poly != 0 (symmetric only, A == B == G) writes
  *   pa*I + pb*G + pc*(G G) instead of the product.
- *   C is M x N.  dtype is the storage type of A, B and C: MUON_BF16 (bf16
- *   tensor cores), MUON_F32 (fp32 FFMA), or 2 = fp32 storage multiplied on the
- *   TF32 tensor path (the kind the bf16 NS path uses for its Gram-space
- *   products; B must be K-major).  tile_n selects the N extent of the
+ *   C is M x N.  dtype is the storage type of A, B and C: MUON_BF16 or MUON_F16
+ *   (16-bit tensor cores), MUON_F32 (fp32 FFMA), or 3 = fp32 storage
+ *   multiplied on the TF32 tensor path (the kind the bf16 NS path uses for
+ *   some Gram-space products; B must be K-major).  tile_n selects the N extent of the
  *   tensor-core tile (0 = default, 128 or 256).
  */
 int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

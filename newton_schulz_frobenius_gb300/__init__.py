@@ -24,6 +24,7 @@ MUON_ENOTSUP = -7
 
 MUON_F32 = 0
 MUON_BF16 = 1
+MUON_F16 = 2
 
 MUON_PATH_AUTO = 0
 MUON_PATH_PLAIN = 1
@@ -33,7 +34,8 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 
 #: every entry point include/muon.h declares
 EXPORTS = (
-    "muon_ns_orthogonalize", "muon_ns_orthogonalize_noalloc", "muon_step", "muon_set_ns_config", "muon_autotune",
+    "muon_ns_orthogonalize", "muon_ns_orthogonalize_noalloc", "muon_step", "muon_set_ns_config",
+    "muon_set_ns_precision", "muon_autotune",
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
@@ -121,7 +123,9 @@ def _dtype_code(t) -> int:
         return MUON_F32
     if t.dtype == torch.bfloat16:
         return MUON_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return MUON_F16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
 
 
 def _stream_ptr(stream) -> int:
@@ -256,6 +260,12 @@ class MuonGroup:
             pass
 
 
+def muon_set_ns_precision(dtype: int = -1):
+    """NS working precision for 16-bit parameters: -1 follows them, MUON_BF16
+    or MUON_F16 forces that type."""
+    _check(lib().muon_set_ns_precision(int(dtype)), "muon_set_ns_precision")
+
+
 def muon_set_ns_config(coeffs=QUINTIC, steps: int = 5, segments=(2, 2, 1), path: int = MUON_PATH_AUTO):
     c = (ctypes.c_float * 3)(*coeffs) if coeffs is not None else None
     segs, nseg = _ints(segments)
@@ -322,7 +332,7 @@ def muon_kernel_timing_read():
     return out
 
 
-MUON_DEBUG_TF32 = 2
+MUON_DEBUG_TF32 = 3
 
 
 def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.0, tile_n=0, stream=None,

@@ -269,6 +269,7 @@ struct NsConfig {
     int steps = 5;
     std::vector<int> segments{2, 2, 1};
     int path = MUON_PATH_AUTO;
+    int ns_precision = -1;      // 16-bit parameters: -1 follow them, or MUON_BF16 / MUON_F16
 };
 static NsConfig g_cfg;
 static std::atomic<uint64_t> g_cfg_version{1};   // bumped when plans may change (config, tune cache)
@@ -339,7 +340,7 @@ static GemmArgs gemm_base(int dtype, int* status) {
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
     a.dtype = dtype;
-    a.c_dtype = dtype == MUON_BF16 ? MUON_BF16 : MUON_F32;
+    a.c_dtype = is_half(dtype) ? dtype : MUON_F32;
     a.alpha = 1.0f;
     a.tile_n = 256;
     // 2-CTA clusters sharing the B tile: measured 3-6% faster on the long
@@ -355,7 +356,7 @@ static GemmArgs gemm_base(int dtype, int* status) {
 static int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
     const double mnk = (double)a.M * a.N * a.K * a.batch;
     const double work = a.symmetric ? mnk : 2.0 * mnk;
-    const bool tc = (a.dtype == MUON_BF16 || a.dtype == DT_TF32);
+    const bool tc = (is_half(a.dtype) || a.dtype == DT_TF32);
     const int kc = tc ? kclass : KC_SIMT;
     note_launch_begin(kc, s);
     cudaError_t e = tc ? launch_gemm_tc(a, dc.sms, s) : launch_gemm_simt(a, s);
@@ -364,7 +365,18 @@ static int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kcl
     return MUON_OK;
 }
 
-static size_t esize(int dtype) { return dtype == MUON_BF16 ? 2 : 4; }
+static size_t esize(int dtype) { return is_half(dtype) ? 2 : 4; }
+
+// Working precision of NS for parameters of this storage type: fp32 stays
+// fp32; 16-bit parameters use the configured 16-bit type, by default their own.
+static int ns_dtype(int param_dtype, const NsConfig& cfg) {
+    if (!is_half(param_dtype)) return MUON_F32;
+    return cfg.ns_precision < 0 ? param_dtype : cfg.ns_precision;
+}
+
+// Whether X holds the unscaled U (the 1 / ||U|| scale folded into the first
+// products) or U already divided by its norm (the fp16 path).
+static bool x_holds_u(int x_dtype) { return x_dtype != MUON_F16; }
 static int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
 
 // Workspace of one chunk of B matrices of oriented shape m x n.
@@ -427,9 +439,10 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
     const int64_t strideX = (int64_t)m * L.ldx;
     const int64_t strideM = (int64_t)m * L.ldm;
 
-    const bool bf = (dtype == MUON_BF16);
-    const bool tf = bf && plan.gram_tf32;
-    const int sq_dtype = bf ? (tf ? DT_TF32 : MUON_BF16) : MUON_F32;   // Gram-space operands
+    const bool tf = (dtype == MUON_BF16) && plan.gram_tf32;
+    // Gram-space operands: fp16 on the fp16 path (ten mantissa bits, like
+    // TF32), bf16 or TF32 on the bf16 path, fp32 on the FFMA path
+    const int sq_dtype = is_half(dtype) ? (tf ? DT_TF32 : dtype) : MUON_F32;
     auto gram_out = [&](GemmArgs& g, bool feeds_apply) {
         // TF32 Gram space: TF32-rounded fp32, or bf16 when it is the
         // transform the long apply consumes; otherwise the path's own dtype
@@ -552,18 +565,37 @@ static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLay
     p.nparts = L.nparts;
     p.vec_ok = vec_ok ? 1 : 0;
     p.hyper = hyper;
+    p.write_x = 1;
+    p.write_mom = 1;
     const double elems = (double)m * n * B;
-    const double bytes = elems * (esize(in_dtype) + (with_mom ? 2.0 * esize(mom_dtype) : 0.0) + esize(x_dtype));
+    const double in_bytes = elems * (esize(in_dtype) + (with_mom ? esize(mom_dtype) : 0.0));
+    const double bytes = in_bytes + elems * ((with_mom ? esize(mom_dtype) : 0.0) + esize(x_dtype));
+    float* inv = reinterpret_cast<float*>(base + L.off_inv);
+    const bool two_pass = !x_holds_u(x_dtype);
+    auto finalize = [&]() -> int {
+        note_launch_begin(KC_NORM, s);
+        cudaError_t e = launch_norm_finalize(p.partials, L.nparts, B, 1e-7f, inv, dc.status, s);
+        note_launch_end(KC_NORM, (double)L.nparts * B * 4.0, s);
+        return e == cudaSuccess ? MUON_OK : cuda_fail(e, "norm launch");
+    };
+    if (two_pass) {
+        // fp16 X: sums of U^2 first (nothing written), then momentum and U / ||U||
+        PrepArgs p1 = p;
+        p1.write_x = 0;
+        p1.write_mom = 0;
+        note_launch_begin(KC_PREP, s);
+        cudaError_t e = launch_prep(p1, s);
+        note_launch_end(KC_PREP, in_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+        int r = finalize();
+        if (r) return r;
+        p.x_scale = inv;
+    }
     note_launch_begin(KC_PREP, s);
     cudaError_t e = launch_prep(p, s);
     note_launch_end(KC_PREP, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-    note_launch_begin(KC_NORM, s);
-    e = launch_norm_finalize(p.partials, L.nparts, B, 1e-7f, reinterpret_cast<float*>(base + L.off_inv),
-                             dc.status, s);
-    note_launch_end(KC_NORM, (double)L.nparts * B * 4.0, s);
-    if (e != cudaSuccess) return cuda_fail(e, "norm launch");
-    return MUON_OK;
+    return two_pass ? MUON_OK : finalize();
 }
 
 }  // namespace muon
@@ -607,7 +639,7 @@ static int save_tune_file(const char* path);
 // Whether the one-CTA-per-matrix kernel can run this plan (bf16, m <= 128,
 // n <= 512, segments of length <= 2, bf16 Gram space).  MUON_SMALL=0 turns it off.
 static bool small_eligible(const NsPlan& p, int m, int n, int dtype) {
-    if (dtype != MUON_BF16 || p.gram_tf32 || !env_flag("MUON_SMALL", true)) return false;
+    if (dtype != MUON_BF16 || p.gram_tf32 || !env_flag("MUON_SMALL", true)) return false;   // bf16 NS only
     return small_ns_fits(m, n, (int)p.segs.size(), p.segs.data());
 }
 
@@ -674,7 +706,7 @@ static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dt
     FinalEpi fin{EPI_STORE, nullptr, dtype, 0.f, 0.f, 0.f};
     const float scale = std::sqrt(3.0f / ((float)m * (float)n));
     struct Cand { int path, tile_n, sym_tile_n, sym_dense; };
-    const bool bf = (dtype == MUON_BF16);
+    const bool bf = is_half(dtype);
     TuneEntry best{MUON_PATH_PLAIN, 256, 1e300, 0, 128, 0};
     const int reps = 3;
     auto measure = [&](const Cand& c, double* out_ms) -> int {
@@ -835,7 +867,7 @@ static int budget_bytes_chunk(size_t per_matrix, int count) {
     return (int)c;
 }
 
-static bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16; }
+static bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16 || d == MUON_F16; }
 
 }  // namespace muon
 
@@ -879,6 +911,15 @@ int muon_set_ns_config(const float coeffs[3], int steps, const int* segments, in
     return MUON_OK;
 }
 
+int muon_set_ns_precision(int dtype) {
+    if (dtype != -1 && dtype != MUON_BF16 && dtype != MUON_F16)
+        return fail(MUON_EDTYPE, "NS precision must be -1, MUON_BF16 or MUON_F16, got %d", dtype);
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_cfg.ns_precision = dtype;
+    g_cfg_version.fetch_add(1);
+    return MUON_OK;
+}
+
 int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype, const float coeffs[3],
                           int steps, const int* segments, int num_segments, void* stream) {
     if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
@@ -898,15 +939,17 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
     const int path = num_segments > 0 ? MUON_PATH_GRAM : MUON_PATH_PLAIN;
     std::vector<int> segs(segments, segments + num_segments);
     int tile_n = 256;
+    int nsd;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_tune.find(tune_key(dc, om, on, dtype));
+        nsd = ns_dtype(dtype, g_cfg);
+        auto it = g_tune.find(tune_key(dc, om, on, nsd));
         if (it != g_tune.end() && it->second.path == path) tile_n = it->second.tile_n;
     }
     NsPlan plan = make_plan(coeffs, steps, segs, path, tile_n, om, on);
 
     const size_t es = esize(dtype);
-    if (small_eligible(plan, om, on, dtype) && batch <= (1 << 20)) {
+    if (dtype == MUON_BF16 && small_eligible(plan, om, on, nsd) && batch <= (1 << 20)) {
         const size_t tb = align_up(sizeof(MatEntry) * (size_t)batch, 256);
         Workspace* w = nullptr;
         if ((r = ws_get(dc.device, s, tb, &w))) return r;
@@ -925,10 +968,10 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
         g_last_path[{om, on, dtype}] = path;
         return MUON_OK;
     }
-    const size_t per = chunk_layout(om, on, 1, dtype).total;
+    const size_t per = chunk_layout(om, on, 1, nsd).total;
     const int chunk = budget_bytes_chunk(per, (int)std::min<int64_t>(batch, 65535));
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)batch, 256);
-    const ChunkLayout L = chunk_layout(om, on, chunk, dtype);
+    const ChunkLayout L = chunk_layout(om, on, chunk, nsd);
     Workspace* w = nullptr;
     if ((r = ws_get(dc.device, s, table_bytes + L.total, &w))) return r;
 
@@ -943,11 +986,11 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
     for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
         const int B = (int)std::min<int64_t>(chunk, batch - b0);
-        const ChunkLayout LB = chunk_layout(om, on, B, dtype);
-        if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, dtype, false, 0, 0.f, vec_ok)))
+        const ChunkLayout LB = chunk_layout(om, on, B, nsd);
+        if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, nsd, false, 0, 0.f, vec_ok)))
             return r;
         FinalEpi fin{EPI_OUT, d_table + b0, dtype, 0.f, 0.f, 0.f};
-        if ((r = run_ns(dc, s, cbase, LB, om, on, B, dtype, plan, true, fin))) return r;
+        if ((r = run_ns(dc, s, cbase, LB, om, on, B, nsd, plan, x_holds_u(nsd), fin))) return r;
     }
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -995,19 +1038,22 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
             it->second.push_back(i);
         }
     }
+    const int nsd = ns_dtype(param_dtype, cfg);
     std::vector<NsPlan> plans(keys.size());
     std::vector<int> chunks(keys.size());
     size_t chunk_need = 0;
     for (size_t k = 0; k < keys.size(); ++k) {
         const int m = keys[k].first, n = keys[k].second;
         const int cnt = (int)buckets[keys[k]].size();
-        if ((r = choose_plan(dc, s, m, n, param_dtype, cnt, cfg, &plans[k]))) return r;
+        if ((r = choose_plan(dc, s, m, n, nsd, cnt, cfg, &plans[k]))) return r;
+        // the fused kernel reads bf16 parameters and bf16 or fp32 momentum
+        if (param_dtype != MUON_BF16 || mom_dtype == MUON_F16) plans[k].fused = 0;
         if (plans[k].fused) {
             chunks[k] = cnt;            // one launch, no workspace beyond the table
             continue;
         }
-        chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, param_dtype).total, cnt);
-        chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], param_dtype).total);
+        chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, nsd).total, cnt);
+        chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], nsd).total);
     }
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)count, 256);
     Workspace* w = nullptr;
@@ -1042,13 +1088,13 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
         }
         for (size_t c0 = 0; c0 < idx.size(); c0 += chunks[k]) {
             const int B = (int)std::min<size_t>(chunks[k], idx.size() - c0);
-            const ChunkLayout L = chunk_layout(m, n, B, param_dtype);
+            const ChunkLayout L = chunk_layout(m, n, B, nsd);
             const MatEntry* dm = d_table + first + c0;
-            if ((r = run_prep(dc, s, cbase, L, m, n, B, dm, param_dtype, mom_dtype, param_dtype, true, nesterov,
-                              beta, vec_ok)))
+            if ((r = run_prep(dc, s, cbase, L, m, n, B, dm, param_dtype, mom_dtype, nsd, true, nesterov, beta,
+                              vec_ok)))
                 return r;
             FinalEpi fin{EPI_UPDATE, dm, param_dtype, lr, wd, scale};
-            if ((r = run_ns(dc, s, cbase, L, m, n, B, param_dtype, plans[k], true, fin))) return r;
+            if ((r = run_ns(dc, s, cbase, L, m, n, B, nsd, plans[k], x_holds_u(nsd), fin))) return r;
         }
         first += idx.size();
         std::lock_guard<std::mutex> lk(g_mu);
@@ -1074,12 +1120,13 @@ int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype
         if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "bad shape at %lld", (long long)i);
         shapes[{(int)std::min(ms[i], ns[i]), (int)std::max(ms[i], ns[i])}] += 1;
     }
+    const int nsd = ns_dtype(dtype, cfg);
     for (auto& kv : shapes) {
         TuneEntry ent;
         const int B = std::max(1, std::min(kv.second, 16));
-        if ((r = autotune_shape(dc, s, kv.first.first, kv.first.second, dtype, B, cfg, &ent))) return r;
+        if ((r = autotune_shape(dc, s, kv.first.first, kv.first.second, nsd, B, cfg, &ent))) return r;
         std::lock_guard<std::mutex> lk(g_mu);
-        g_tune[tune_key(dc, kv.first.first, kv.first.second, dtype)] = ent;
+        g_tune[tune_key(dc, kv.first.first, kv.first.second, nsd)] = ent;
     }
     if (const char* p = std::getenv("MUON_TUNE_CACHE")) save_tune_file(p);
     g_cfg_version.fetch_add(1);
@@ -1260,7 +1307,7 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
     if ((symmetric || poly) && M != N) return fail(MUON_EINVAL, "symmetric product needs M == N");
     if (poly && (!symmetric || K != M)) return fail(MUON_EINVAL, "poly needs a symmetric square product");
     if (tile_n != 0 && tile_n != 128 && tile_n != 256) return fail(MUON_EINVAL, "tile_n must be 0, 128 or 256");
-    if (dtype == MUON_BF16 || dtype == DT_TF32) {
+    if (is_half(dtype) || dtype == DT_TF32) {
         const int64_t ldb = b_kmajor ? K : N;
         const int64_t epr = dtype == DT_TF32 ? 4 : 8;
         if ((K % epr) || (ldb % epr) || (reinterpret_cast<uintptr_t>(A) % 16) || (reinterpret_cast<uintptr_t>(B) % 16))
@@ -1372,7 +1419,12 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
     if (r) return r;
 
     const int om = (int)std::min(m, n), on = (int)std::max(m, n);
-    const ChunkLayout L = chunk_layout(om, on, (int)batch, dtype);
+    int nsd;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        nsd = ns_dtype(dtype, g_cfg);
+    }
+    const ChunkLayout L = chunk_layout(om, on, (int)batch, nsd);
     const size_t status_bytes = 256;
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)batch, 256);
     const size_t need = status_bytes + table_bytes + L.total;
@@ -1401,10 +1453,10 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
     std::vector<int> segs(segments, segments + num_segments);
     NsPlan plan = make_plan(coeffs, steps, segs, path, 256, om, on);
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
-    if ((r = run_prep(dc, s, cbase, L, om, on, (int)batch, d_table, dtype, dtype, dtype, false, 0, 0.f, vec_ok)))
+    if ((r = run_prep(dc, s, cbase, L, om, on, (int)batch, d_table, dtype, dtype, nsd, false, 0, 0.f, vec_ok)))
         return r;
     FinalEpi fin{EPI_OUT, d_table, dtype, 0.f, 0.f, 0.f};
-    return run_ns(dc, s, cbase, L, om, on, (int)batch, dtype, plan, true, fin);
+    return run_ns(dc, s, cbase, L, om, on, (int)batch, nsd, plan, x_holds_u(nsd), fin);
 }
 
 // ---------------------------------------------------------------------------
@@ -1420,6 +1472,7 @@ struct muon_group {
     DevCtx dc;
     int64_t count = 0;
     int param_dtype = 0, mom_dtype = 0;
+    int ns_dtype = 0;                               // NS working precision of the current plans
     std::vector<MatEntry> entries;                  // bucket order
     std::vector<std::pair<int, int>> keys;          // oriented shape per bucket
     std::vector<int64_t> bucket_first, bucket_size;
@@ -1460,13 +1513,13 @@ static int group_enqueue(muon_group* g, cudaStream_t s) {
         const float scale = 0.2f * std::sqrt((float)n);
         for (int64_t c0 = 0; c0 < cnt; c0 += g->chunks[k]) {
             const int B = (int)std::min<int64_t>(g->chunks[k], cnt - c0);
-            const ChunkLayout L = chunk_layout(m, n, B, g->param_dtype);
+            const ChunkLayout L = chunk_layout(m, n, B, g->ns_dtype);
             const MatEntry* dm = g->d_table + first + c0;
-            if ((r = run_prep(g->dc, s, g->cbase, L, m, n, B, dm, g->param_dtype, g->mom_dtype, g->param_dtype, true,
+            if ((r = run_prep(g->dc, s, g->cbase, L, m, n, B, dm, g->param_dtype, g->mom_dtype, g->ns_dtype, true,
                               0, 0.f, g->vec_ok[k] != 0, g->d_hyper)))
                 return r;
             FinalEpi fin{EPI_UPDATE, dm, g->param_dtype, 0.f, 0.f, scale, g->d_hyper};
-            if ((r = run_ns(g->dc, s, g->cbase, L, m, n, B, g->param_dtype, plan, true, fin))) return r;
+            if ((r = run_ns(g->dc, s, g->cbase, L, m, n, B, g->ns_dtype, plan, x_holds_u(g->ns_dtype), fin))) return r;
         }
     }
     return MUON_OK;
@@ -1491,16 +1544,19 @@ static int group_plan(muon_group* g, cudaStream_t s) {
     size_t chunk_need = 0;
     g->plans.assign(g->keys.size(), NsPlan{});
     g->chunks.assign(g->keys.size(), 1);
+    g->ns_dtype = ns_dtype(g->param_dtype, cfg);
     for (size_t k = 0; k < g->keys.size(); ++k) {
         const int m = g->keys[k].first, n = g->keys[k].second;
         const int cnt = (int)g->bucket_size[k];
-        if ((r = choose_plan(g->dc, s, m, n, g->param_dtype, cnt, cfg, &g->plans[k]))) return r;
+        if ((r = choose_plan(g->dc, s, m, n, g->ns_dtype, cnt, cfg, &g->plans[k]))) return r;
+        // the fused kernel reads bf16 parameters and bf16 or fp32 momentum
+        if (g->param_dtype != MUON_BF16 || g->mom_dtype == MUON_F16) g->plans[k].fused = 0;
         if (g->plans[k].fused) {
             g->chunks[k] = cnt;
             continue;
         }
-        g->chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, g->param_dtype).total, cnt);
-        chunk_need = std::max(chunk_need, chunk_layout(m, n, g->chunks[k], g->param_dtype).total);
+        g->chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, g->ns_dtype).total, cnt);
+        chunk_need = std::max(chunk_need, chunk_layout(m, n, g->chunks[k], g->ns_dtype).total);
     }
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)g->count, 256);
     const size_t need = table_bytes + 256 + chunk_need;
@@ -1697,13 +1753,14 @@ extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t cou
     // the library picks without measurements
     std::vector<double> cost((size_t)count, 0.0);
     bool measured = count > 0;
+    const int nsd = ns_dtype(dtype, cfg);       // tune entries are kept per NS precision
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int64_t i = 0; i < count && measured; ++i) {
             const int64_t m = std::min(ms[i], ns[i]), n = std::max(ms[i], ns[i]);
             bool found = false;
             for (auto& kv : g_tune) {
-                if (std::get<3>(kv.first) == m && std::get<4>(kv.first) == n && std::get<5>(kv.first) == dtype) {
+                if (std::get<3>(kv.first) == m && std::get<4>(kv.first) == n && std::get<5>(kv.first) == nsd) {
                     cost[(size_t)i] = kv.second.ms_per_matrix;
                     found = true;
                     break;
@@ -1751,8 +1808,8 @@ extern "C" int muon_adamw_step(void* const* params, const void* const* grads, vo
     if (count < 0) return fail(MUON_EINVAL, "count < 0");
     if (count == 0) return MUON_OK;
     if (!params || !grads || !exp_avg || !exp_avg_sq || !numels) return fail(MUON_EINVAL, "NULL array argument");
-    if (!valid_dtype(param_dtype) || !valid_dtype(state_dtype))
-        return fail(MUON_EDTYPE, "dtypes %d / %d", param_dtype, state_dtype);
+    if (!valid_dtype(param_dtype) || !(state_dtype == MUON_F32 || state_dtype == MUON_BF16))
+        return fail(MUON_EDTYPE, "dtypes %d / %d (moments: fp32 or bf16)", param_dtype, state_dtype);
     if (step < 1) return fail(MUON_EINVAL, "step counts from 1");
     if (!std::isfinite(lr) || !std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(eps) ||
         !std::isfinite(wd) || beta1 < 0.f || beta1 >= 1.f || beta2 < 0.f || beta2 >= 1.f || eps < 0.f)

@@ -3,9 +3,12 @@
 //
 // Momentum smooths the gradient before Newton-Schulz ("MuonX" page, section 2);
 // the Frobenius normalisation places every singular value at or below 1 before
-// the iteration.  The scale 1/(||U||_F + eps) is not applied here: it is folded
-// into the first XX^T (as its square) and the first Q X of the NS path, so U is
-// read and written exactly once.
+// the iteration.  On the bf16 and fp32 paths the scale 1/(||U||_F + eps) is not
+// applied here: it is folded into the first XX^T (as its square) and the first
+// Q X of the NS path, so U is read and written exactly once.  fp16 has too
+// little range for an unscaled U (small gradients fall into its subnormals),
+// so the fp16 path runs the kernel twice: a first pass that only sums U^2, and
+// a second that updates the momentum and stores U / (||U||_F + eps).
 //
 // Layout: one CTA handles a 64 x 64 tile of the ORIENTED matrix (m <= n).  For
 // a tall caller matrix (trans = 1) the CTA reads the matching transposed tile of
@@ -24,7 +27,11 @@ constexpr int PTHREADS = 256;   // 64 rows x 4 segments of 16 elements
 __device__ __forceinline__ void load16(const void* p, int dtype, int64_t off, int valid, bool vec,
                                        float (&v)[16]) {
     if (vec && valid == 16) {
-        if (dtype == MUON_BF16) {
+        if (dtype == MUON_F16) {
+            const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p) + off);
+            unpack8_h(__ldg(q), v, true);
+            unpack8_h(__ldg(q + 1), v + 8, true);
+        } else if (dtype == MUON_BF16) {
             const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p) + off);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -109,7 +116,7 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
                 u[j] = nesterov ? fmaf(beta, mn, g[j]) : mn;         // U = G + beta M'
             }
             // momentum is stored in its own dtype; U continues from the fp32 M'
-            store16(e.mom, a.mom_dtype, off, valid, vec, mo);
+            if (a.write_mom) store16(e.mom, a.mom_dtype, off, valid, vec, mo);
         } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) u[j] = g[j];
@@ -124,7 +131,14 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
 
     const int64_t xb = (int64_t)b * a.strideX;
     const bool xvec = (a.ldx % 8) == 0;
-    if (!e.trans) {
+    if (a.x_scale) {
+        const float xs = a.x_scale[b];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) u[j] *= xs;
+    }
+    if (!a.write_x) {
+        // first pass of the fp16 path: sums only
+    } else if (!e.trans) {
         if (valid > 0) store16(a.X, a.x_dtype, xb + (int64_t)raw_r * a.ldx + raw_c0, valid, xvec, u);
     } else {
 #pragma unroll

@@ -14,14 +14,44 @@
 
 namespace muon {
 
+// Storage codes: MUON_F32 (and DT_TF32, fp32 storage), MUON_BF16, MUON_F16.
 __device__ __forceinline__ float ld_elem(const void* p, int64_t i, int dtype) {
     if (dtype == MUON_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+    if (dtype == MUON_F16) return __half2float(reinterpret_cast<const __half*>(p)[i]);
     return reinterpret_cast<const float*>(p)[i];
 }
 
 __device__ __forceinline__ void st_elem(void* p, int64_t i, float v, int dtype) {
     if (dtype == MUON_BF16) reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+    else if (dtype == MUON_F16) reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
     else reinterpret_cast<float*>(p)[i] = v;
+}
+
+// Eight 16-bit values (bf16 or fp16, round to nearest even) in one 16-byte word.
+__device__ __forceinline__ uint4 pack8_h(const float* v, bool f16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (f16) {
+            __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void unpack8_h(const uint4 q, float* v, bool f16) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = f16 ? __half22float2(*reinterpret_cast<const __half2*>(&w[k]))
+                             : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        v[2 * k] = f.x;
+        v[2 * k + 1] = f.y;
+    }
 }
 
 // Nearest TF32 value (10 explicit mantissa bits), ties to even, on the fp32
@@ -45,7 +75,16 @@ __device__ __forceinline__ float epi_alpha(const GemmArgs& a, int b) {
 // with 16-byte vector stores when the address allows it.
 template <int W>
 __device__ __forceinline__ void store_row_run(void* base, int64_t off, const float (&v)[W], int dtype) {
-    if (dtype == MUON_BF16) {
+    if (dtype == MUON_F16) {
+        __half* p = reinterpret_cast<__half*>(base) + off;
+        if ((W % 8) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < W; j += 8) *reinterpret_cast<uint4*>(p + j) = pack8_h(v + j, true);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) p[j] = __float2half_rn(v[j]);
+        }
+    } else if (dtype == MUON_BF16) {
         __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + off;
         if ((W % 8) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
 #pragma unroll
@@ -82,7 +121,16 @@ __device__ __forceinline__ void store_row_run(void* base, int64_t off, const flo
 // loads when the address allows it.
 template <int W>
 __device__ __forceinline__ void load_row_run(const void* base, int64_t off, float (&v)[W], int dtype) {
-    if (dtype == MUON_BF16) {
+    if (dtype == MUON_F16) {
+        const __half* p = reinterpret_cast<const __half*>(base) + off;
+        if ((W % 8) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < W; j += 8) unpack8_h(*reinterpret_cast<const uint4*>(p + j), v + j, true);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) v[j] = __half2float(p[j]);
+        }
+    } else if (dtype == MUON_BF16) {
         const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(base) + off;
         if ((W % 8) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
 #pragma unroll

@@ -19,9 +19,10 @@
 //               of the tile's columns with tcgen05.ld 32 at a time, fused
 //               epilogue from epilogue.cuh; while the main loop of a tile runs
 //               they prefetch into L2 the caller data their epilogue will read
-// Operand kinds: bf16 (kind::f16, K = 16 per instruction) for the long
-// products, TF32 on fp32 storage (kind::tf32, K = 8) for the m x m Gram-space
-// products; either way one k-block is 128 bytes of every operand row.
+// Operand kinds: bf16 or fp16 (kind::f16, K = 16 per instruction, A and B of
+// the same type) for the long products and the 16-bit Gram-space products,
+// TF32 on fp32 storage (kind::tf32, K = 8) for the Gram-space products that
+// need it; either way one k-block is 128 bytes of every operand row.
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
 // of tile t overlaps the main loop of tile t+1.
 // Paired launches (PAIR, 128 x 256 tiles): 2-CTA clusters take row blocks 2p
@@ -273,10 +274,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
-// K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16
+// (format code 1) or both fp16 (code 0), A K-major, B K-major or MN-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool b_mn_major, bool fp16) {
+    return (1u << 4) | (fp16 ? 0u : ((1u << 7) | (1u << 10))) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -342,7 +344,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
-    constexpr uint32_t IDESC = TF32 ? idesc_tf32(BM, BN) : idesc_bf16(BM, BN, !B_KMAJOR);
+    const uint32_t IDESC = TF32 ? idesc_tf32(BM, BN) : idesc_f16kind(BM, BN, !B_KMAJOR, args.dtype == MUON_F16);
     constexpr int KE = TF32 ? 32 : 64;    // elements per 128-byte k-block
 
     extern __shared__ uint8_t smem_raw[];
@@ -598,20 +600,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D tensor map (bf16 or fp32 elements) over `batch` matrices of `rows` x
-// `inner` (row pitch ld, matrix pitch stride, in elements), box box_inner x
-// box_rows x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t rows, uint64_t batch,
+// 3-D tensor map (fp32, bf16 or fp16 elements, by storage code) over `batch`
+// matrices of `rows` x `inner` (row pitch ld, matrix pitch stride, in
+// elements), box box_inner x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t batch,
               uint64_t ld, uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     if (batch <= 1) stride = ld * rows;
+    const bool f32 = !is_half(dtype);
     const uint64_t eb = f32 ? 4 : 2;
+    const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : (dtype == MUON_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
     cuuint64_t dims[3] = {inner, rows, batch};
     cuuint64_t strides[2] = {ld * eb, stride * eb};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, elem,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -647,13 +653,13 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
 
     CUtensorMap mA, mB;
     constexpr uint32_t KE = TF32 ? 32 : 64;   // elements per 128-byte k-block
-    if (!make_map(&mA, a.A, TF32, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda,
+    if (!make_map(&mA, a.A, a.dtype, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda,
                   (uint64_t)a.strideA, KE, BM))
         return cudaErrorInvalidValue;
     // a paired K-major B tile arrives as two halves of BN / 2 rows
-    bool okB = B_KMAJOR ? make_map(&mB, a.B, TF32, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
+    bool okB = B_KMAJOR ? make_map(&mB, a.B, a.dtype, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
                                    (uint64_t)a.ldb, (uint64_t)a.strideB, KE, PAIR ? BN / 2 : BN)
-                        : make_map(&mB, a.B, TF32, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch,
+                        : make_map(&mB, a.B, a.dtype, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch,
                                    (uint64_t)a.ldb, (uint64_t)a.strideB, 64, BK);
     if (!okB) return cudaErrorInvalidValue;
 
@@ -700,7 +706,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     const bool tf32 = (a.dtype == DT_TF32);
-    if (a.dtype != MUON_BF16 && !tf32) return cudaErrorInvalidValue;
+    if (!is_half(a.dtype) && !tf32) return cudaErrorInvalidValue;
     if (tf32 && !a.b_kmajor) return cudaErrorInvalidValue;
     if (a.M < 1 || a.N < 1 || a.K < 1 || a.batch < 1) return cudaErrorInvalidValue;
     if (a.symmetric && a.M != a.N) return cudaErrorInvalidValue;

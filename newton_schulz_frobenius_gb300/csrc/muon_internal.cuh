@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,10 +13,13 @@
 
 namespace muon {
 
-// Internal storage/arithmetic code next to MUON_F32 and MUON_BF16: fp32
-// storage whose values are consumed by the tensor cores as TF32 (10-bit
-// mantissa).  The bf16 path keeps its m x m Gram-space matrices in this form.
-constexpr int DT_TF32 = 2;
+// Internal storage/arithmetic code next to MUON_F32, MUON_BF16 and MUON_F16:
+// fp32 storage whose values are consumed by the tensor cores as TF32 (10-bit
+// mantissa).  The bf16 path keeps some m x m Gram-space matrices in this form.
+constexpr int DT_TF32 = 3;
+
+// 16-bit storage that the kind::f16 tensor-core products take (bf16 or fp16).
+__host__ __device__ constexpr bool is_half(int dtype) { return dtype == MUON_BF16 || dtype == MUON_F16; }
 
 // Bits of the per-device status word (read by muon_sync_status).
 enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
@@ -92,6 +96,9 @@ struct PrepArgs {
     int nparts;
     int vec_ok;             // caller rows are 16-byte aligned for vector access
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides beta, nesterov
+    int write_x;            // store U (times x_scale) into X
+    int write_mom;          // store M' (0: a first pass that only sums U^2)
+    const float* x_scale;   // optional per-matrix factor applied to U before it is stored
 };
 int prep_num_parts(int m, int n);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
