@@ -25,12 +25,14 @@
 // need it; either way one k-block is 128 bytes of every operand row.
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
 // of tile t overlaps the main loop of tile t+1.
-// Paired launches (PAIR, 128 x 256 tiles): 2-CTA clusters take row blocks 2p
-// and 2p+1 of one column tile; each CTA loads its own A and half of the shared
-// B tile with a cluster-multicast TMA into both CTAs, and each MMA issuer
-// commits to the stage's empty barrier in both CTAs (count 2), so neither
-// refills a stage the other still reads.  Same tiles and K order, so the
-// results equal the unpaired kernel's bit for bit.  Every mbarrier wait is bounded:
+// Paired launches (PAIR, 128 x 256 tiles per CTA): 2-CTA clusters run 2-SM
+// products (tcgen05 cta_group::2).  The CTAs take row blocks 2p and 2p+1 of
+// one 256-column tile; each loads its own A rows and its half of B, so a stage
+// is 32 KB instead of 48 KB and six stages fit; the odd CTA relays each filled
+// stage to the even CTA's full barrier, the even CTA issues M = 256 products
+// and commits to both CTAs' barriers, and both epilogues report to the even
+// CTA.  TMEM is allocated collectively by one warp of each CTA.  Same tiles
+// and K order, so the results equal the unpaired kernel's bit for bit.  Every mbarrier wait is bounded:
 // after WAIT_LIMIT_NS it sets an abort flag and the status word, waits (again
 // bounded) for its own copies and products in flight, frees TMEM and returns.
 #include "muon_internal.cuh"
@@ -51,12 +53,12 @@ constexpr int BK_BYTES = 128;
 constexpr int NEPI = 8;                        // epilogue warps
 constexpr int NTHREADS = 64 + 32 * NEPI;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;   // paired: this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : 6);
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int MIRROR_BYTES = NEPI * 32 * 33 * 4;   // per epilogue warp: one 32 x 33 fp32 chunk
@@ -150,18 +152,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset in every
-// CTA of ctaMask, and each of their mbarriers at `bar`'s offset receives the
-// byte count.  Used only between the two CTAs of a cluster on this GPU.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                               int c2, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -183,6 +173,64 @@ __device__ __forceinline__ uint32_t cluster_count() {
 // Every thread of both CTAs of the cluster arrives and waits.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on the mbarrier at the same shared offset in CTA `rank` of the
+// cluster, releasing this thread's earlier writes (epilogue: TMEM reads done).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(bar), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+
+// Relaxed remote arrive for the stage relay: it forwards a completion this
+// thread observed on its own mbarrier (bulk copies the copy engine finished),
+// and has no writes of its own to order, so it needs no cluster-scope fence
+// (a release here cost about 0.4 us per stage, serialising the pipeline).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar, uint32_t rank) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(bar), "r"(rank));
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+
+// 2-SM forms (a CTA pair of the cluster): TMEM allocated collectively by one
+// warp of each CTA at the same address; the even CTA issues M = 256 products
+// whose A rows and B columns are split between the two CTAs' shared memory
+// at the same offsets, each CTA's TMEM receiving its 128 rows; commits track
+// them and arrive on the barrier at `bar`'s offset in every CTA of the mask.
+__device__ __forceinline__ void tmem_alloc2(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_commit2(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma2_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
@@ -209,15 +257,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// Arrives on the mbarrier at `bar`'s offset in every CTA of ctaMask once the
-// products issued so far by this thread complete.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
 }
 
 __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -341,10 +380,12 @@ template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ GemmArgs args, const TileSched sched) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
-    const uint32_t IDESC = TF32 ? idesc_tf32(BM, BN) : idesc_f16kind(BM, BN, !B_KMAJOR, args.dtype == MUON_F16);
+    static_assert(!PAIR || BN == 256, "paired products use 128 x 256 tiles per CTA");
+    constexpr int MM = PAIR ? 2 * BM : BM;      // rows of one product instruction
+    const uint32_t IDESC = TF32 ? idesc_tf32(MM, BN) : idesc_f16kind(MM, BN, !B_KMAJOR, args.dtype == MUON_F16);
     constexpr int KE = TF32 ? 32 : 64;    // elements per 128-byte k-block
 
     extern __shared__ uint8_t smem_raw[];
@@ -364,22 +405,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Paired launches: the two CTAs of a cluster take the two row blocks of a
-    // unit; each loads its own A and half of the shared B tile, multicast to
-    // both, so a stage may be refilled only when both CTAs have consumed it.
+    // Paired launches (2-SM products): the two CTAs of a cluster take the two
+    // row blocks of a 256 x BN tile.  Each loads its own A rows and its half
+    // of B; the odd CTA relays "stage full" to the even CTA, which issues the
+    // M = 256 products and commits to both; both epilogues report to the even
+    // CTA's accumulator barrier.
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
     const int unit0 = PAIR ? (int)cluster_idx() : (int)blockIdx.x;
     const int ustep = PAIR ? (int)cluster_count() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);
+            mbar_init(full0 + 8 * s, (PAIR && rank == 0) ? 2 : 1);   // own copies (+ the peer's relay)
+            mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(accf0, 1);
         mbar_init(accf0 + 8, 1);
-        mbar_init(acce0, NEPI);
-        mbar_init(acce0 + 8, NEPI);
+        mbar_init(acce0, PAIR ? 2 * NEPI : NEPI);
+        mbar_init(acce0 + 8, PAIR ? 2 * NEPI : NEPI);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -389,8 +432,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc2(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -422,15 +470,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
                     if (PAIR) {
-                        // this CTA's half of B, into both CTAs
+                        // this CTA's half of B: rows (K-major) or columns (MN-major) rank * BN / 2 ..
                         if (B_KMAJOR) {
-                            tma_load_3d_mc(smem_u32(sB + stage * C::B_BYTES + rank * (BN / 2) * BK_BYTES), &tmB, fb,
-                                           kb * KE, tn * BN + rank * (BN / 2), b, (uint16_t)0x3);
+                            tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN + rank * (BN / 2),
+                                        b);
                         } else {
 #pragma unroll
-                            for (int q = rank * (BN / 128); q < (rank + 1) * (BN / 128); ++q)
-                                tma_load_3d_mc(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmB, fb,
-                                               tn * BN + q * 64, kb * BK, b, (uint16_t)0x3);
+                            for (int q = 0; q < BN / 128; ++q)
+                                tma_load_3d(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmB, fb,
+                                            tn * BN + rank * (BN / 2) + q * 64, kb * BK, b);
                         }
                     } else if (B_KMAJOR) {
                         tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN, b);
@@ -452,6 +500,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int s = 0; s < S; ++s)
                     if (issued[s] >= 0) wait_drain(full0 + 8 * s, (uint32_t)issued[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 && PAIR && rank == 1) {
+        // ---------------- relay (odd CTA of a pair) ----------------
+        // every completed stage of this CTA is reported to the even CTA's full
+        // barrier; this CTA refills it only after the even CTA's commit
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = unit0; t < sched.total && ok; t += ustep) {
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote_relaxed(full0 + 8 * stage, 0);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
             }
         }
         __syncwarp();
@@ -484,10 +555,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint64_t ad = sdesc(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_KMAJOR ? sdesc(b_base + kk * 32, 16, 1024)
                                                      : sdesc(b_base + kk * 2048, BK * 128, 1024);
-                        if (TF32) tc_mma_tf32(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
-                        else tc_mma_bf16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if (PAIR) {
+                            if (TF32) tc_mma2_tf32(d, ad, bd, IDESC, accum);
+                            else tc_mma2_bf16(d, ad, bd, IDESC, accum);
+                        } else {
+                            if (TF32) tc_mma_tf32(d, ad, bd, IDESC, accum);
+                            else tc_mma_bf16(d, ad, bd, IDESC, accum);
+                        }
                     }
-                    if (PAIR) tc_commit_mc(empty0 + 8 * stage, (uint16_t)0x3);
+                    if (PAIR) tc_commit2(empty0 + 8 * stage, (uint16_t)0x3);
                     else tc_commit(empty0 + 8 * stage);
                     if (++stage == S) {
                         stage = 0;
@@ -495,13 +572,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 if (!ok) break;
-                tc_commit(accf0 + 8 * acc);
+                if (PAIR) tc_commit2(accf0 + 8 * acc, (uint16_t)0x3);
+                else tc_commit(accf0 + 8 * acc);
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
             }
             if (!ok) {
                 // wait (bounded) for the products this thread issued
-                tc_commit(drain_bar);
+                if (PAIR) tc_commit2(drain_bar, (uint16_t)0x1);
+                else tc_commit(drain_bar);
                 wait_drain(drain_bar, 0);
             }
         }
@@ -567,7 +646,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            if (lane == 0) {
+                if (PAIR && rank == 1) mbar_arrive_remote(acce0 + 8 * acc, 0);
+                else mbar_arrive(acce0 + 8 * acc);
+            }
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
@@ -575,10 +657,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();     // no multicast copy or remote arrive targets this CTA any more
+    if (PAIR) cluster_sync();     // no product, commit or remote arrive targets this CTA any more
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if (PAIR) tmem_dealloc2(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -625,7 +708,7 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t inner, uint6
 
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -720,7 +803,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     // symmetric products default to 128 x 128 tiles, the others to 128 x 256;
     // 128 x 256 tiles may run as 2-CTA clusters sharing the B tile
     const int bn = a.symmetric ? (a.tile_n == 256 ? 256 : 128) : (a.tile_n == 128 ? 128 : 256);
-    const bool pair = (bn == 256) && (a.pair > 0 || (a.pair < 0 && !a.symmetric));
+    const bool pair = (bn == 256) && a.pair != 0;
     if (tf32) {
         if (bn == 128) return tc::launch_impl<128, true, true, false>(a, num_sms, s);
         return pair ? tc::launch_impl<256, true, true, true>(a, num_sms, s)

@@ -72,7 +72,7 @@ struct GemmArgs {
     int out_dtype;          // storage type of the caller's W / O
     float lr, wd, scale;
     int tile_n;             // tensor-core tile N extent (128 or 256)
-    int pair;               // tile_n 256 as 2-CTA clusters sharing each B tile: 1 on, 0 off, -1 non-symmetric only
+    int pair;               // tile_n 256 as 2-SM products on 2-CTA clusters: 0 off, otherwise on
     int* status;            // device status word
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd
 };
