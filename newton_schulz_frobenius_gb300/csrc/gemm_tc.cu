@@ -53,16 +53,20 @@ constexpr int BK_BYTES = 128;
 constexpr int NEPI = 8;                        // epilogue warps
 constexpr int NTHREADS = 64 + 32 * NEPI;
 
-template <int BN, bool PAIR = false>
+// MIR: the launch may be symmetric and needs the mirror staging (K-major B);
+// MN-major launches (the long applies) never are, and spend the 33 KB on one
+// more pipeline stage where a stage is 32 KB.
+template <int BN, bool PAIR = false, bool MIR = true>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;   // paired: this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : 6);
+    static constexpr int STAGES = (PAIR || BN == 128) ? (MIR ? 6 : 7) : 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int MIRROR_BYTES = NEPI * 32 * 33 * 4;   // per epilogue warp: one 32 x 33 fp32 chunk
+    static constexpr int MIRROR_BYTES = MIR ? NEPI * 32 * 33 * 4 : 0;   // per epilogue warp: one 32 x 33 fp32 chunk
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + MIRROR_BYTES + NUM_BARS * 8 + 16 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // ---------------------------------------------------------------------------
@@ -380,7 +384,7 @@ template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ GemmArgs args, const TileSched sched) {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, B_KMAJOR>;
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
     static_assert(!PAIR || BN == 256, "paired products use 128 x 256 tiles per CTA");
@@ -638,7 +642,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
                 epi_row_chunk<32, false>(args, ent, b, row0 + lane, col0, v, scale, gcur);
-                if (args.symmetric) epi_mirror_staged(args, b, row0, col0, v, mstage);
+                if (B_KMAJOR && args.symmetric) epi_mirror_staged(args, b, row0, col0, v, mstage);
                 if (loads) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) gcur[j] = gnxt[j];
@@ -708,7 +712,7 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t inner, uint6
 
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, B_KMAJOR>;
     auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -792,7 +796,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if (!is_half(a.dtype) && !tf32) return cudaErrorInvalidValue;
     if (tf32 && !a.b_kmajor) return cudaErrorInvalidValue;
     if (a.M < 1 || a.N < 1 || a.K < 1 || a.batch < 1) return cudaErrorInvalidValue;
-    if (a.symmetric && a.M != a.N) return cudaErrorInvalidValue;
+    if (a.symmetric && (a.M != a.N || !a.b_kmajor)) return cudaErrorInvalidValue;
     // TMA: 16-byte aligned bases and pitches
     const int64_t epr = tf32 ? 4 : 8;   // elements per 16 bytes
     auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
