@@ -175,8 +175,19 @@ norm_finalize_kernel(const float* __restrict__ partials, int nparts, float eps,
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x;
+    const float* pb = partials + (int64_t)b * nparts;
+    // eight independent loads in flight per thread, summed in double
     double s = 0.0;
-    for (int i = threadIdx.x; i < nparts; i += 256) s += (double)partials[(int64_t)b * nparts + i];
+    for (int i0 = threadIdx.x; i0 < nparts; i0 += 256 * 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + 256 * u;
+            v[u] = i < nparts ? pb[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += (double)v[u];
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
