@@ -188,4 +188,10 @@ WORKLOADS = {
         "stack_32L_7b_bf16_f32mom", 5, _transformer(32, 4096, 14336, kv=1024), "bf16", "f32",
         grad_std=math.sqrt(1e-3),
         note="32 layers: Wq,Wo 4096^2; Wk,Wv 1024x4096; Wgate,Wup 14336x4096; Wdown 4096x14336"),
+    # the open-source Gram NS configuration the MuonX page (section 3.2) names:
+    # fp16 working type, five steps as segments 2+3; same matrix as config 2
+    "single_2560x9728_f16_2p3": Workload(
+        "single_2560x9728_f16_2p3", 6, [(2560, 9728, 1)], "f16", "f16", grad_std=0.02,
+        nesterov=True, note="fp16 parameters and momentum, NS in fp16, Gram segments 2+3",
+        extra={"segments": (2, 3)}),
 }
