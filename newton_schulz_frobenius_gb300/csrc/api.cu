@@ -18,8 +18,10 @@
 #include <cstdlib>
 #include <cstring>
 #include <fstream>
+#include <functional>
 #include <map>
 #include <mutex>
+#include <queue>
 #include <sstream>
 #include <string>
 #include <tuple>
@@ -651,23 +653,66 @@ __global__ void table_fill_kernel(MatEntry* t, char* base, int64_t stride_bytes,
     }
 }
 
+static SmallBucket small_bucket(const NsPlan& p, const MatEntry* mats, int B, int m, int n, bool vec_ok) {
+    SmallBucket bk;
+    std::memset(&bk, 0, sizeof bk);
+    bk.mats = mats;
+    bk.batch = B; bk.m = m; bk.n = n;
+    bk.nseg = std::min((int)p.segs.size(), 8);
+    for (int i = 0; i < bk.nseg; ++i) bk.segs[i] = p.segs[i];
+    bk.vec_ok = vec_ok ? 1 : 0;
+    bk.scale = 0.2f * std::sqrt((float)n);
+    return bk;
+}
+
+// Arguments of a fused launch over one bucket, CTA c taking matrices c, c + grid, ...
 static SmallArgs small_args(const NsPlan& p, const MatEntry* mats, int B, int m, int n, int mode, int param_dtype,
                             int mom_dtype, int nesterov, float beta, float lr, float wd, bool vec_ok, int* status) {
     SmallArgs a;
     std::memset(&a, 0, sizeof a);
-    a.mats = mats;
-    a.batch = B; a.m = m; a.n = n;
+    a.nb = 1;
+    a.bk[0] = small_bucket(p, mats, B, m, n, vec_ok);
     a.mode = mode;
     a.param_dtype = param_dtype; a.mom_dtype = mom_dtype;
     a.nesterov = nesterov;
     a.beta = beta; a.lr = lr; a.wd = wd;
-    a.scale = 0.2f * std::sqrt((float)n);
     a.a = p.a; a.b = p.b; a.c = p.c;
-    a.nseg = (int)p.segs.size();
-    for (int i = 0; i < a.nseg && i < 16; ++i) a.segs[i] = p.segs[i];
-    a.vec_ok = vec_ok ? 1 : 0;
     a.status = status;
     return a;
+}
+
+// Work lists of one fused launch over several buckets: every matrix is an
+// item of its bucket's cost; items go, most expensive first, to the CTA with
+// the least work so far (longest processing time first), which balances
+// buckets whose matrix counts are not multiples of the SM count.  Output:
+// grid, per-CTA offsets ptr[grid + 1] and items (bucket << 24 | index).
+struct SmallWork {
+    int grid = 0;
+    std::vector<int> ptr, items;
+};
+static SmallWork small_work(const std::vector<int>& counts, const std::vector<double>& costs, int sms) {
+    SmallWork w;
+    std::vector<std::pair<double, int>> order;          // (cost, item)
+    for (size_t bi = 0; bi < counts.size(); ++bi)
+        for (int i = 0; i < counts[bi]; ++i) order.push_back({costs[bi], (int)(bi << 24) | i});
+    std::stable_sort(order.begin(), order.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+    const int total = (int)order.size();
+    w.grid = std::max(1, std::min(total, sms));
+    std::vector<std::vector<int>> lists((size_t)w.grid);
+    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<>> heap;
+    for (int c = 0; c < w.grid; ++c) heap.push({0.0, c});
+    for (const auto& it : order) {
+        auto top = heap.top();
+        heap.pop();
+        lists[(size_t)top.second].push_back(it.second);
+        heap.push({top.first + it.first, top.second});
+    }
+    w.ptr.assign((size_t)w.grid + 1, 0);
+    for (int c = 0; c < w.grid; ++c) {
+        w.ptr[(size_t)c + 1] = w.ptr[(size_t)c] + (int)lists[(size_t)c].size();
+        w.items.insert(w.items.end(), lists[(size_t)c].begin(), lists[(size_t)c].end());
+    }
+    return w;
 }
 
 // Algorithmic FLOPs of one NS update under this plan (symmetric results half).
@@ -689,6 +734,105 @@ static int run_small(const DevCtx& dc, cudaStream_t s, const SmallArgs& a, doubl
     note_launch_end(KC_SMALL, alg_flops, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused small-matrix launch");
     return MUON_OK;
+}
+
+// Fused launches of one step: the fused buckets in groups of at most
+// SMALL_MAX_BUCKETS, each group one launch with LPT work lists.  Costs per
+// matrix: the autotune's measured time of the fused kernel when every bucket
+// of the group has one, else a model (FLOPs at 12 TFLOP/s and 10 bytes per
+// element at 40 GB/s per SM; only the ratios matter).
+struct FusedLaunch {
+    std::vector<int> bks;       // bucket indices (into the caller's key order)
+    SmallWork work;
+    size_t off = 0;             // byte offset of ptr, items in the work block
+    size_t bytes = 0;
+};
+static std::vector<FusedLaunch> plan_fused(const DevCtx& dc, const std::vector<NsPlan>& plans,
+                                           const std::vector<std::pair<int, int>>& keys,
+                                           const std::vector<int64_t>& counts, int nsd, size_t* total_bytes) {
+    std::vector<FusedLaunch> out;
+    FusedLaunch cur;
+    for (size_t k = 0; k < keys.size(); ++k) {
+        if (!plans[k].fused) continue;
+        cur.bks.push_back((int)k);
+        if ((int)cur.bks.size() == SMALL_MAX_BUCKETS) {
+            out.push_back(cur);
+            cur = FusedLaunch{};
+        }
+    }
+    if (!cur.bks.empty()) out.push_back(cur);
+    size_t off = 0;
+    for (auto& fl : out) {
+        std::vector<int> cnt;
+        std::vector<double> measured, model;
+        bool all_measured = true;
+        for (int k : fl.bks) {
+            const int m = keys[(size_t)k].first, n = keys[(size_t)k].second;
+            cnt.push_back((int)counts[(size_t)k]);
+            model.push_back(plan_alg_flops(plans[(size_t)k], m, n) / 12e12 + (double)m * n * 10.0 / 40e9);
+            double ms = -1.0;
+            {
+                std::lock_guard<std::mutex> lk(g_mu);
+                auto it = g_tune.find(tune_key(dc, m, n, nsd));
+                if (it != g_tune.end() && it->second.fused) ms = it->second.ms_per_matrix;
+            }
+            measured.push_back(ms);
+            all_measured = all_measured && ms > 0.0;
+        }
+        fl.work = small_work(cnt, all_measured ? measured : model, dc.sms);
+        fl.off = off;
+        fl.bytes = align_up(sizeof(int) * (fl.work.ptr.size() + fl.work.items.size()), 256);
+        off += fl.bytes;
+    }
+    *total_bytes = off;
+    return out;
+}
+
+// Copies the work lists of `fl` into a host byte block at fl.off.
+static void pack_fused(const std::vector<FusedLaunch>& fl, char* block) {
+    for (const auto& f : fl) {
+        int* p = reinterpret_cast<int*>(block + f.off);
+        std::memcpy(p, f.work.ptr.data(), sizeof(int) * f.work.ptr.size());
+        std::memcpy(p + f.work.ptr.size(), f.work.items.data(), sizeof(int) * f.work.items.size());
+    }
+}
+
+// Arguments of fused launch `f`; mats_of(k) gives bucket k's device table.
+template <typename MatsOf>
+static SmallArgs fused_args(const FusedLaunch& f, const char* d_block, const std::vector<NsPlan>& plans,
+                            const std::vector<std::pair<int, int>>& keys, const std::vector<int64_t>& counts,
+                            const std::vector<char>& vec_ok, MatsOf mats_of, int mode, int param_dtype,
+                            int mom_dtype, int nesterov, float beta, float lr, float wd, int* status,
+                            const float* hyper) {
+    SmallArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.nb = (int)f.bks.size();
+    for (int j = 0; j < a.nb; ++j) {
+        const int k = f.bks[(size_t)j];
+        a.bk[j] = small_bucket(plans[(size_t)k], mats_of(k), (int)counts[(size_t)k], keys[(size_t)k].first,
+                               keys[(size_t)k].second, vec_ok[(size_t)k] != 0);
+    }
+    const int* p = reinterpret_cast<const int*>(d_block + f.off);
+    a.cta_ptr = p;
+    a.items = p + f.work.ptr.size();
+    a.grid = f.work.grid;
+    a.mode = mode;
+    a.param_dtype = param_dtype; a.mom_dtype = mom_dtype;
+    a.nesterov = nesterov;
+    a.beta = beta; a.lr = lr; a.wd = wd;
+    const NsPlan& p0 = plans[(size_t)f.bks[0]];
+    a.a = p0.a; a.b = p0.b; a.c = p0.c;
+    a.status = status;
+    a.hyper = hyper;
+    return a;
+}
+
+static double fused_flops(const FusedLaunch& f, const std::vector<NsPlan>& plans,
+                          const std::vector<std::pair<int, int>>& keys, const std::vector<int64_t>& counts) {
+    double t = 0.0;
+    for (int k : f.bks)
+        t += plan_alg_flops(plans[(size_t)k], keys[(size_t)k].first, keys[(size_t)k].second) * (double)counts[(size_t)k];
+    return t;
 }
 
 static int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int B, const NsConfig& cfg,
@@ -1055,35 +1199,61 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
         chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, nsd).total, cnt);
         chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], nsd).total);
     }
+    // per bucket: matrix count, first table row, 16-byte access
+    std::vector<int64_t> counts(keys.size()), firsts(keys.size());
+    std::vector<char> vecs(keys.size());
+    {
+        int64_t f = 0;
+        for (size_t k = 0; k < keys.size(); ++k) {
+            const auto& idx = buckets[keys[k]];
+            counts[k] = (int64_t)idx.size();
+            firsts[k] = f;
+            f += counts[k];
+            bool v = (keys[k].first % 8 == 0) && (keys[k].second % 8 == 0);
+            for (int64_t i : idx)
+                v = v && (reinterpret_cast<uintptr_t>(grads[i]) % 16 == 0) &&
+                    (reinterpret_cast<uintptr_t>(moms[i]) % 16 == 0);
+            vecs[k] = v ? 1 : 0;
+        }
+    }
+    size_t work_bytes = 0;
+    const std::vector<FusedLaunch> fused = plan_fused(dc, plans, keys, counts, nsd, &work_bytes);
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)count, 256);
     Workspace* w = nullptr;
-    if ((r = ws_get(dc.device, s, table_bytes + chunk_need, &w))) return r;
+    if ((r = ws_get(dc.device, s, table_bytes + work_bytes + chunk_need, &w))) return r;
 
-    std::vector<MatEntry> h;
-    h.reserve((size_t)count);
-    for (auto& k : keys)
-        for (int64_t i : buckets[k])
-            h.push_back(MatEntry{grads[i], moms[i], params[i], ms[i] > ns[i] ? 1 : 0, 0});
+    // the matrix table and the fused launches' work lists, as one byte block
+    static_assert(256 % sizeof(MatEntry) == 0, "ring rows tile 256 bytes");
+    std::vector<MatEntry> h((table_bytes + work_bytes) / sizeof(MatEntry));
+    {
+        size_t row = 0;
+        for (auto& k : keys)
+            for (int64_t i : buckets[k])
+                h[row++] = MatEntry{grads[i], moms[i], params[i], ms[i] > ns[i] ? 1 : 0, 0};
+        pack_fused(fused, reinterpret_cast<char*>(h.data()) + table_bytes);
+    }
     MatEntry* d_table = reinterpret_cast<MatEntry*>(w->base);
     if ((r = upload_table(*w, h, d_table, s))) return r;
-    char* cbase = w->base + table_bytes;
+    char* cbase = w->base + table_bytes + work_bytes;
+
+    // every fused bucket in one launch per group of buckets
+    for (const auto& f : fused) {
+        const SmallArgs sa = fused_args(f, w->base + table_bytes, plans, keys, counts, vecs,
+                                        [&](int k) { return d_table + firsts[(size_t)k]; }, 0, param_dtype, mom_dtype,
+                                        nesterov, beta, lr, wd, dc.status, nullptr);
+        if ((r = run_small(dc, s, sa, fused_flops(f, plans, keys, counts)))) return r;
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int k : f.bks) g_last_path[{keys[(size_t)k].first, keys[(size_t)k].second, param_dtype}] = plans[(size_t)k].path;
+    }
 
     size_t first = 0;
     for (size_t k = 0; k < keys.size(); ++k) {
         const int m = keys[k].first, n = keys[k].second;
         const auto& idx = buckets[keys[k]];
-        bool vec_ok = (m % 8 == 0) && (n % 8 == 0);
-        for (int64_t i : idx)
-            vec_ok = vec_ok && (reinterpret_cast<uintptr_t>(grads[i]) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(moms[i]) % 16 == 0);
+        const bool vec_ok = vecs[k] != 0;
         const float scale = 0.2f * std::sqrt((float)n);
         if (plans[k].fused) {
-            const SmallArgs sa = small_args(plans[k], d_table + first, (int)idx.size(), m, n, 0, param_dtype,
-                                            mom_dtype, nesterov, beta, lr, wd, vec_ok, dc.status);
-            if ((r = run_small(dc, s, sa, plan_alg_flops(plans[k], m, n) * (double)idx.size()))) return r;
             first += idx.size();
-            std::lock_guard<std::mutex> lk(g_mu);
-            g_last_path[{m, n, param_dtype}] = plans[k].path;
             continue;
         }
         for (size_t c0 = 0; c0 < idx.size(); c0 += chunks[k]) {
@@ -1477,6 +1647,8 @@ struct muon_group {
     std::vector<std::pair<int, int>> keys;          // oriented shape per bucket
     std::vector<int64_t> bucket_first, bucket_size;
     std::vector<char> vec_ok;
+    std::vector<FusedLaunch> fused;                 // fused launches and their work lists
+    char* d_work = nullptr;                         // work lists on the device
     std::vector<NsPlan> plans;
     std::vector<int> chunks;
     char* ws = nullptr;
@@ -1499,17 +1671,17 @@ namespace muon {
 
 static int group_enqueue(muon_group* g, cudaStream_t s) {
     int r;
+    for (const auto& f : g->fused) {
+        const SmallArgs sa = fused_args(f, g->d_work, g->plans, g->keys, g->bucket_size, g->vec_ok,
+                                        [&](int k) { return g->d_table + g->bucket_first[(size_t)k]; }, 0,
+                                        g->param_dtype, g->mom_dtype, 0, 0.f, 0.f, 0.f, g->dc.status, g->d_hyper);
+        if ((r = run_small(g->dc, s, sa, fused_flops(f, g->plans, g->keys, g->bucket_size)))) return r;
+    }
     for (size_t k = 0; k < g->keys.size(); ++k) {
         const int m = g->keys[k].first, n = g->keys[k].second;
         const int64_t first = g->bucket_first[k], cnt = g->bucket_size[k];
         const NsPlan& plan = g->plans[k];
-        if (plan.fused) {
-            SmallArgs sa = small_args(plan, g->d_table + first, (int)cnt, m, n, 0, g->param_dtype, g->mom_dtype, 0,
-                                      0.f, 0.f, 0.f, g->vec_ok[k] != 0, g->dc.status);
-            sa.hyper = g->d_hyper;
-            if ((r = run_small(g->dc, s, sa, plan_alg_flops(plan, m, n) * (double)cnt))) return r;
-            continue;
-        }
+        if (plan.fused) continue;
         const float scale = 0.2f * std::sqrt((float)n);
         for (int64_t c0 = 0; c0 < cnt; c0 += g->chunks[k]) {
             const int B = (int)std::min<int64_t>(g->chunks[k], cnt - c0);
@@ -1558,8 +1730,10 @@ static int group_plan(muon_group* g, cudaStream_t s) {
         g->chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, g->ns_dtype).total, cnt);
         chunk_need = std::max(chunk_need, chunk_layout(m, n, g->chunks[k], g->ns_dtype).total);
     }
+    size_t work_bytes = 0;
+    g->fused = plan_fused(g->dc, g->plans, g->keys, g->bucket_size, g->ns_dtype, &work_bytes);
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)g->count, 256);
-    const size_t need = table_bytes + 256 + chunk_need;
+    const size_t need = table_bytes + 256 + work_bytes + chunk_need;
     if (g->ws_bytes < need) {
         MUON_CUDA(cudaStreamSynchronize(s));
         group_drop_graph(g);
@@ -1574,9 +1748,17 @@ static int group_plan(muon_group* g, cudaStream_t s) {
         g->ws_bytes = need;
         g->d_table = reinterpret_cast<MatEntry*>(g->ws);
         g->d_hyper = reinterpret_cast<float*>(g->ws + table_bytes);
-        g->cbase = g->ws + table_bytes + 256;
         MUON_CUDA(cudaMemcpy(g->d_table, g->entries.data(), sizeof(MatEntry) * g->entries.size(),
                              cudaMemcpyHostToDevice));
+    }
+    // the fused launches' work lists after the hyper-parameter block, then the chunks
+    g->d_work = g->ws + table_bytes + 256;
+    g->cbase = g->d_work + work_bytes;
+    if (work_bytes) {
+        std::vector<char> blk(work_bytes);
+        pack_fused(g->fused, blk.data());
+        MUON_CUDA(cudaStreamSynchronize(s));
+        MUON_CUDA(cudaMemcpy(g->d_work, blk.data(), work_bytes, cudaMemcpyHostToDevice));
     }
     group_drop_graph(g);
     g->direct_done = false;

@@ -103,20 +103,33 @@ struct PrepArgs {
 int prep_num_parts(int m, int n);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
-// Whole update of small matrices (oriented m <= 128, m <= n <= 512, bf16,
-// segments of length 1 or 2), one CTA per matrix: see small_ns.cu.
-struct SmallArgs {
-    const MatEntry* mats;   // device table, one entry per matrix
+// Whole update of small matrices, one CTA per matrix (see small_ns.cu): the
+// oriented shapes of up to SMALL_MAX_BUCKETS buckets in one launch, each
+// bucket m <= 128 with n <= 512 (segments of length 1 or 2), or plain NS with
+// 128 < m <= n <= 256; bf16 parameters.
+constexpr int SMALL_MAX_BUCKETS = 8;
+struct SmallBucket {
+    const MatEntry* mats;   // device table, one entry per matrix of the bucket
     int batch, m, n;        // oriented shape
+    int nseg;
+    int segs[8];
+    int vec_ok;             // caller rows 16-byte aligned, 8-element multiples
+    float scale;            // shape scale of the update, 0.2 sqrt(n)
+};
+struct SmallArgs {
+    int nb;
+    SmallBucket bk[SMALL_MAX_BUCKETS];
+    // Work order: null: one bucket, CTA c takes matrices c, c + grid, ...;
+    // else CTA c takes items[cta_ptr[c] .. cta_ptr[c+1]), item = bucket << 24 | index
+    const int* cta_ptr;
+    const int* items;
+    int grid;               // CTAs of the launch (with a work list: its CTA count)
     int mode;               // 0: Muon step (momentum + fused update), 1: write O
     int param_dtype;        // MUON_BF16
     int mom_dtype;
     int nesterov;
-    float beta, lr, wd, scale;
+    float beta, lr, wd;
     float a, b, c;
-    int nseg;
-    int segs[16];
-    int vec_ok;             // caller rows 16-byte aligned, 8-element multiples
     int* status;
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}
 };

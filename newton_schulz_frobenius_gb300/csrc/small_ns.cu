@@ -234,11 +234,11 @@ __device__ __forceinline__ uint32_t stream_stages(const SmallArgs& a) {
 // flight); the rest takes one element per thread at a time.  ok turns false
 // if a piece does not arrive within the wait limit.
 template <int ROWS>
-__device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X, uint8_t* stage_ptr, Stream& st,
-                          bool& ok) {
+__device__ float prologue(const SmallArgs& a, const SmallBucket& bk, const MatEntry& e, uint8_t* X,
+                          uint8_t* stage_ptr, Stream& st, bool& ok) {
     const int tid = threadIdx.x;
-    const int raw_rows = e.trans ? a.n : a.m;
-    const int raw_cols = e.trans ? a.m : a.n;
+    const int raw_rows = e.trans ? bk.n : bk.m;
+    const int raw_cols = e.trans ? bk.m : bk.n;
     const int total = raw_rows * raw_cols;
     const bool step = (a.mode == 0);
     const float beta = a.hyper ? a.hyper[1] : a.beta;
@@ -256,7 +256,7 @@ __device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X, uin
             }
         }
     };
-    if (!a.vec_ok) {
+    if (!bk.vec_ok) {
         for (int i = tid; i < total; i += NT) {
             const float g = ld_elem(e.grad, i, a.param_dtype);
             float u = g;
@@ -352,14 +352,14 @@ __device__ float prologue(const SmallArgs& a, const MatEntry& e, uint8_t* X, uin
 // and written whole by a warp, not one row per lane.
 constexpr int OPITCH = 256 * 4 + 16;
 
-__device__ __noinline__ void write_out(const SmallArgs& a, const MatEntry& e, uint8_t* stage, uint32_t tl, int row0,
-                                       float alpha, int nck) {
+__device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk, const MatEntry& e, uint8_t* stage,
+                                       uint32_t tl, int row0, float alpha, int nck) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hw = warp >> 2, r = 32 * (warp & 3) + lane;
     const float lr = a.hyper ? a.hyper[0] : a.lr;
     const float wd = a.hyper ? a.hyper[2] : a.wd;
     const float lrwd = lr * wd;
-    const float stepc = lr * a.scale;
+    const float stepc = lr * bk.scale;
     const int od = a.param_dtype;
     const bool upd = (a.mode == 0);
     for (int col0 = 0; col0 < nck * 64; col0 += 256) {
@@ -385,21 +385,21 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const MatEntry& e, ui
         if (!e.trans) {
             // warp w: rows w, w+8, ...; lane l: columns 8l .. 8l+7 of the block
             const int c = 8 * lane, col = col0 + c;
-            if (c < bc && col < a.n) {
-                if (a.vec_ok) {
+            if (c < bc && col < bk.n) {
+                if (bk.vec_ok) {
                     // all sixteen rows' W in flight before the first is used
                     __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(e.w);
                     uint4 w[16];
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         const int row = row0 + warp + 8 * t;
-                        w[t] = (upd && row < a.m) ? *reinterpret_cast<const uint4*>(wp + (int64_t)row * a.n + col)
+                        w[t] = (upd && row < bk.m) ? *reinterpret_cast<const uint4*>(wp + (int64_t)row * bk.n + col)
                                                   : make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         const int i = warp + 8 * t, row = row0 + i;
-                        if (row >= a.m) continue;
+                        if (row >= bk.m) continue;
                         const float* so = reinterpret_cast<const float*>(stage + i * OPITCH) + c;
                         const float4 o0 = *reinterpret_cast<const float4*>(so);
                         const float4 o1 = *reinterpret_cast<const float4*>(so + 4);
@@ -410,13 +410,13 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const MatEntry& e, ui
 #pragma unroll
                             for (int j = 0; j < 8; ++j) o[j] = wf[j] - fmaf(lrwd, wf[j], stepc * o[j]);
                         }
-                        *reinterpret_cast<uint4*>(wp + (int64_t)row * a.n + col) = pack8(o);
+                        *reinterpret_cast<uint4*>(wp + (int64_t)row * bk.n + col) = pack8(o);
                     }
                 } else {
-                    for (int i = warp; i < 128 && row0 + i < a.m; i += 8) {
-                        const int64_t off = (int64_t)(row0 + i) * a.n + col;
+                    for (int i = warp; i < 128 && row0 + i < bk.m; i += 8) {
+                        const int64_t off = (int64_t)(row0 + i) * bk.n + col;
                         const float* so = reinterpret_cast<const float*>(stage + i * OPITCH) + c;
-                        for (int j = 0; j < 8 && col + j < a.n; ++j) {
+                        for (int j = 0; j < 8 && col + j < bk.n; ++j) {
                             float o = so[j];
                             if (upd) {
                                 const float w = ld_elem(e.w, off + j, od);
@@ -430,12 +430,12 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const MatEntry& e, ui
         } else {
             // the caller's matrix is the transpose: its row j is column j of O;
             // warp w: caller rows col0 + w, + 8, ...; lane l: elements l + 32 t
-            for (int jj = warp; jj < bc && col0 + jj < a.n; jj += 8) {
-                const int64_t rbase = (int64_t)(col0 + jj) * a.m;
+            for (int jj = warp; jj < bc && col0 + jj < bk.n; jj += 8) {
+                const int64_t rbase = (int64_t)(col0 + jj) * bk.m;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int i = lane + 32 * t, row = row0 + i;
-                    if (row >= a.m) continue;
+                    if (row >= bk.m) continue;
                     float o = reinterpret_cast<const float*>(stage + i * OPITCH)[jj];
                     if (upd) {
                         const float w = ld_elem(e.w, rbase + row, od);
@@ -449,49 +449,36 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const MatEntry& e, ui
     }
 }
 
+// Per-CTA state shared by the matrices a CTA processes.
+struct Ctx {
+    uint8_t *X, *S0, *S1, *S2;
+    float* red;              // 8 warp partials
+    float* inv_s;
+    uint32_t barA, tmem, tlane;
+    int tid, warp, lane, hw, r;
+    uint32_t phase;          // parity of the product barrier
+    Stream stream;
+};
+
+// The whole update of matrix b of bucket bk (ROWS: the X layout, 128 or 256
+// rows); nx: the CTA's next matrix (or null) whose inputs are pulled into L2
+// meanwhile.  Returns false when a bounded wait gave up.
 template <int ROWS>
-__global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__ SmallArgs a) {
+__device__ bool process(const SmallArgs& a, const SmallBucket& bk, int b, const MatEntry* nx, int64_t nx_elems,
+                        Ctx& c) {
     constexpr bool BIG = (ROWS == 256);
     constexpr int XCH = ROWS * 128;             // bytes of one X chunk
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* X = base;
-    uint8_t* S0 = base + X_BYTES;
-    uint8_t* S1 = S0 + S_BYTES;
-    uint8_t* S2 = S1 + S_BYTES;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(S2 + S_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);     // bar[0] products, bar[1..3] stages
-    float* red = reinterpret_cast<float*>(tmem_slot + 2);     // 8 warp partials
-    float* inv_s = red + 8;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, hw = warp >> 2;
-    const int r = 32 * q + lane;                                // this thread's TMEM lane
-    const uint32_t barA = smem_u32(bar);
-
-    if (tid == 0) {
-        for (int i = 0; i < 4; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barA + 8 * i) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
-    pdl_wait();          // the caller's matrices may come from the previous kernel
-    pdl_trigger();
-
-    const int nck = (a.n + 63) / 64;            // X chunks in use
-    const bool pad = (a.m != ROWS) || (a.n % 64 != 0);
+    uint8_t* const X = c.X;
+    uint8_t* const S0 = c.S0;
+    uint8_t* const S1 = c.S1;
+    uint8_t* const S2 = c.S2;
+    const uint32_t barA = c.barA, tmem = c.tmem, tlane = c.tlane;
+    const int tid = c.tid, warp = c.warp, lane = c.lane, hw = c.hw, r = c.r;
+    uint32_t& phase = c.phase;
+    const int nck = (bk.n + 63) / 64;           // X chunks in use
+    const bool pad = (bk.m != ROWS) || (bk.n % 64 != 0);
     constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
-    uint32_t phase = 0;
     bool ok = true;
-    Stream stream{barA + 8, smem_u32(S0), stream_stages(a), 0u, 0u};
 
     // One product round: make this thread's smem writes visible to the tensor
     // cores and let thread 0 issue (begin); wait for completion, bounded (finish).
@@ -574,171 +561,244 @@ __global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__
         }
     };
 
-    for (int b = blockIdx.x; b < a.batch && ok; b += gridDim.x) {
-        const MatEntry e = a.mats[b];
-        // zero the padding of X (only when there is padding), and start pulling
-        // this matrix's W into L2
-        if (pad) {
-            for (int i = tid; i < nck * (XCH / 16); i += NT) reinterpret_cast<uint4*>(X)[i] = make_uint4(0, 0, 0, 0);
-            __syncthreads();
-        }
-        if (a.mode == 0) {
-            const int64_t wbytes = (int64_t)a.m * a.n * 2;
-            for (int64_t off = (int64_t)tid * 128; off < wbytes; off += (int64_t)NT * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(e.w) + off));
-        }
-        float ss = prologue<ROWS>(a, e, X, S0, stream, ok);
-        if (!ok) break;
-        // while this matrix iterates, pull the next one's inputs into L2
-        if (b + (int)gridDim.x < a.batch) {
-            const MatEntry nx = a.mats[b + gridDim.x];
-            const int64_t elems = (int64_t)a.m * a.n;
-            const int64_t gbytes = elems * (a.param_dtype == MUON_BF16 ? 2 : 4);
-            const int64_t mbytes = elems * (a.mom_dtype == MUON_BF16 ? 2 : 4);
-            for (int64_t off = (int64_t)tid * 128; off < gbytes; off += (int64_t)NT * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(nx.grad) + off));
-            if (a.mode == 0)
-                for (int64_t off = (int64_t)tid * 128; off < mbytes; off += (int64_t)NT * 128)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(nx.mom) + off));
-        }
+    const MatEntry e = bk.mats[b];
+    // zero the padding of X (only when there is padding), and start pulling
+    // this matrix's W into L2
+    if (pad) {
+        for (int i = tid; i < nck * (XCH / 16); i += NT) reinterpret_cast<uint4*>(X)[i] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    }
+    if (a.mode == 0) {
+        const int64_t wbytes = (int64_t)bk.m * bk.n * 2;
+        for (int64_t off = (int64_t)tid * 128; off < wbytes; off += (int64_t)NT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(e.w) + off));
+    }
+    float ss = prologue<ROWS>(a, bk, e, X, S0, c.stream, ok);
+    if (!ok) return false;
+    // while this matrix iterates, pull the next one's inputs into L2
+    if (nx) {
+        const int64_t gbytes = nx_elems * (a.param_dtype == MUON_BF16 ? 2 : 4);
+        const int64_t mbytes = nx_elems * (a.mom_dtype == MUON_BF16 ? 2 : 4);
+        for (int64_t off = (int64_t)tid * 128; off < gbytes; off += (int64_t)NT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(nx->grad) + off));
+        if (a.mode == 0)
+            for (int64_t off = (int64_t)tid * 128; off < mbytes; off += (int64_t)NT * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(nx->mom) + off));
+    }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
-        if (tid == 0) {
-            double t = 0.0;
-            for (int w = 0; w < NT / 32; ++w) t += (double)red[w];
-            if (!isfinite(t)) atomicOr(a.status, STATUS_NONFINITE);
-            *inv_s = (float)(1.0 / (sqrt(t) + 1e-7));
-        }
-        __syncthreads();
-        const float inv = *inv_s;
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) c.red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
+        for (int w = 0; w < NT / 32; ++w) t += (double)c.red[w];
+        if (!isfinite(t)) atomicOr(a.status, STATUS_NONFINITE);
+        *c.inv_s = (float)(1.0 / (sqrt(t) + 1e-7));
+    }
+    __syncthreads();
+    const float inv = *c.inv_s;
 
-        if constexpr (!BIG) {
-            for (int si = 0; si < a.nseg && ok; ++si) {
-                const int L = a.segs[si];
-                const bool first = (si == 0), last = (si == a.nseg - 1);
-                const float gs = first ? inv * inv : 1.0f;
-                auto square = [&](const uint8_t* A, const uint8_t* B, uint32_t col) {
-                    return run([&] {
-                        for (int s = 0; s < 8; ++s) tc_mma(tmem + col, ks(A, s), ks(B, s), ID_SQ, s > 0 ? 1u : 0u);
-                    });
-                };
-                // G = X X^T -> TMEM [0, 128) -> S0
-                ok = run([&] {
-                    for (int s = 0; s < nck * 4; ++s) tc_mma(tmem, kx(0, s), kx(0, s), ID_SQ, s > 0 ? 1u : 0u);
+    if constexpr (!BIG) {
+        for (int si = 0; si < bk.nseg && ok; ++si) {
+            const int L = bk.segs[si];
+            const bool first = (si == 0), last = (si == bk.nseg - 1);
+            const float gs = first ? inv * inv : 1.0f;
+            auto square = [&](const uint8_t* A, const uint8_t* B, uint32_t col) {
+                return run([&] {
+                    for (int s = 0; s < 8; ++s) tc_mma(tmem + col, ks(A, s), ks(B, s), ID_SQ, s > 0 ? 1u : 0u);
                 });
-                if (!ok) break;
-                drain_store(0, S0, gs);
-                // P1 = aI + bG + cG^2 -> S1
-                if (!(ok = square(S0, S0, 128))) break;
-                drain_poly(128, S0, S1, true);
-                uint8_t* Q = S1;
-                if (L == 2) {
-                    if (!(ok = square(S1, S0, 256))) break;       // P1 G -> S2
-                    drain_store(256, S2, 1.f);
-                    if (!(ok = square(S2, S1, 0))) break;         // (P1 G) P1 = G' -> S0
-                    drain_store(0, S0, 1.f);
-                    if (!(ok = square(S0, S0, 128))) break;       // P2 = aI + bG' + cG'^2 -> S2
-                    drain_poly(128, S0, S2, true);
-                    if (!(ok = square(S2, S1, 256))) break;       // Q = P2 P1 -> S0
-                    drain_store(256, S0, 1.f);
-                    Q = S0;
-                }
-                // X <- Q X : TMEM [0, 64 nck)
-                ok = run([&] {
-                    for (int h = 0; h < 2; ++h) {
-                        const int nh = min(256, nck * 64 - 256 * h);
-                        if (nh <= 0) break;
-                        const uint32_t id = idesc_bf16(128, nh, false, true);
-                        for (int s = 0; s < 8; ++s) tc_mma(tmem + 256 * h, ks(Q, s), mx(16 * s, 4 * h), id, s > 0 ? 1u : 0u);
-                    }
-                });
-                if (!ok) break;
-                const float alpha = first ? inv : 1.0f;
-                if (!last) drain_x(0, 0, alpha);
-                else write_out(a, e, X, tlane, 0, alpha, nck);
+            };
+            // G = X X^T -> TMEM [0, 128) -> S0
+            ok = run([&] {
+                for (int s = 0; s < nck * 4; ++s) tc_mma(tmem, kx(0, s), kx(0, s), ID_SQ, s > 0 ? 1u : 0u);
+            });
+            if (!ok) break;
+            drain_store(0, S0, gs);
+            // P1 = aI + bG + cG^2 -> S1
+            if (!(ok = square(S0, S0, 128))) break;
+            drain_poly(128, S0, S1, true);
+            uint8_t* Q = S1;
+            if (L == 2) {
+                if (!(ok = square(S1, S0, 256))) break;       // P1 G -> S2
+                drain_store(256, S2, 1.f);
+                if (!(ok = square(S2, S1, 0))) break;         // (P1 G) P1 = G' -> S0
+                drain_store(0, S0, 1.f);
+                if (!(ok = square(S0, S0, 128))) break;       // P2 = aI + bG' + cG'^2 -> S2
+                drain_poly(128, S0, S2, true);
+                if (!(ok = square(S2, S1, 256))) break;       // Q = P2 P1 -> S0
+                drain_store(256, S0, 1.f);
+                Q = S0;
             }
-        } else {
-            constexpr uint32_t ID_WIDE = idesc_bf16(128, 256, false, false);
-            constexpr uint32_t ID_TT = idesc_bf16(128, 128, true, true);
-            constexpr uint32_t ID_KT = idesc_bf16(128, 128, false, true);
-            const uint32_t id_px = idesc_bf16(128, nck * 64, false, true);
-            const uint32_t id_px_t = idesc_bf16(128, nck * 64, true, true);
-            for (int it = 0; it < a.nseg && ok; ++it) {
-                const bool first = (it == 0), last = (it == a.nseg - 1);
-                const float gs = first ? inv * inv : 1.0f;
-                // A = X X^T: A00 -> TMEM [0, 128); rows 128.. (A10 | A11) -> [128, 384)
-                ok = run([&] {
-                    for (int s = 0; s < nck * 4; ++s) {
-                        tc_mma(tmem, kx(0, s), kx(0, s), ID_SQ, s > 0 ? 1u : 0u);
-                        tc_mma(tmem + 128, kx(128, s), kx(0, s), ID_WIDE, s > 0 ? 1u : 0u);
-                    }
-                });
-                if (!ok) break;
-                drain_store(0, S0, gs);
-                drain_store(128, S1, gs);
-                drain_store(256, S2, gs);
-                // A^2 blocks: C00 -> [0,128), C10 -> [128,256), C11 -> [256,384)
-                ok = run([&] {
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem, ks(S0, s), ks(S0, s), ID_SQ, s > 0 ? 1u : 0u);
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem, ms(S1, s), ms(S1, s), ID_TT, 1u);
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem + 128, ks(S1, s), ks(S0, s), ID_SQ, s > 0 ? 1u : 0u);
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem + 128, ks(S2, s), ms(S1, s), ID_KT, 1u);
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem + 256, ks(S1, s), ks(S1, s), ID_SQ, s > 0 ? 1u : 0u);
-                    for (int s = 0; s < 8; ++s) tc_mma(tmem + 256, ks(S2, s), ks(S2, s), ID_SQ, 1u);
-                });
-                if (!ok) break;
-                drain_poly(0, S0, S0, true);
-                drain_poly(128, S1, S1, false);
-                drain_poly(256, S2, S2, true);
-                // X <- P X: M-half h -> TMEM [256 h, 256 h + 64 nck); P01 = P10^T
-                ok = run([&] {
-                    for (int h = 0; h < 2; ++h)
-                        for (int kb = 0; kb < 2; ++kb) {
-                            const uint8_t* Pblk = (h == 0) ? (kb == 0 ? S0 : S1) : (kb == 0 ? S1 : S2);
-                            const bool tr = (h == 0 && kb == 1);
-                            for (int s = 0; s < 8; ++s)
-                                tc_mma(tmem + 256 * h, tr ? ms(Pblk, s) : ks(Pblk, s), mx(128 * kb + 16 * s, 0),
-                                       tr ? id_px_t : id_px, (kb | s) ? 1u : 0u);
-                        }
-                });
-                if (!ok) break;
-                const float alpha = first ? inv : 1.0f;
-                if (!last) {
-                    drain_x(0, 0, alpha);
-                    drain_x(256, 128, alpha);
-                } else {
-                    write_out(a, e, X, tlane, 0, alpha, nck);
-                    write_out(a, e, X, tlane + 256, 128, alpha, nck);
+            // X <- Q X : TMEM [0, 64 nck)
+            ok = run([&] {
+                for (int h = 0; h < 2; ++h) {
+                    const int nh = min(256, nck * 64 - 256 * h);
+                    if (nh <= 0) break;
+                    const uint32_t id = idesc_bf16(128, nh, false, true);
+                    for (int s = 0; s < 8; ++s) tc_mma(tmem + 256 * h, ks(Q, s), mx(16 * s, 4 * h), id, s > 0 ? 1u : 0u);
                 }
+            });
+            if (!ok) break;
+            const float alpha = first ? inv : 1.0f;
+            if (!last) drain_x(0, 0, alpha);
+            else write_out(a, bk, e, X, tlane, 0, alpha, nck);
+        }
+    } else {
+        constexpr uint32_t ID_WIDE = idesc_bf16(128, 256, false, false);
+        constexpr uint32_t ID_TT = idesc_bf16(128, 128, true, true);
+        constexpr uint32_t ID_KT = idesc_bf16(128, 128, false, true);
+        const uint32_t id_px = idesc_bf16(128, nck * 64, false, true);
+        const uint32_t id_px_t = idesc_bf16(128, nck * 64, true, true);
+        for (int it = 0; it < bk.nseg && ok; ++it) {
+            const bool first = (it == 0), last = (it == bk.nseg - 1);
+            const float gs = first ? inv * inv : 1.0f;
+            // A = X X^T: A00 -> TMEM [0, 128); rows 128.. (A10 | A11) -> [128, 384)
+            ok = run([&] {
+                for (int s = 0; s < nck * 4; ++s) {
+                    tc_mma(tmem, kx(0, s), kx(0, s), ID_SQ, s > 0 ? 1u : 0u);
+                    tc_mma(tmem + 128, kx(128, s), kx(0, s), ID_WIDE, s > 0 ? 1u : 0u);
+                }
+            });
+            if (!ok) break;
+            drain_store(0, S0, gs);
+            drain_store(128, S1, gs);
+            drain_store(256, S2, gs);
+            // A^2 blocks: C00 -> [0,128), C10 -> [128,256), C11 -> [256,384)
+            ok = run([&] {
+                for (int s = 0; s < 8; ++s) tc_mma(tmem, ks(S0, s), ks(S0, s), ID_SQ, s > 0 ? 1u : 0u);
+                for (int s = 0; s < 8; ++s) tc_mma(tmem, ms(S1, s), ms(S1, s), ID_TT, 1u);
+                for (int s = 0; s < 8; ++s) tc_mma(tmem + 128, ks(S1, s), ks(S0, s), ID_SQ, s > 0 ? 1u : 0u);
+                for (int s = 0; s < 8; ++s) tc_mma(tmem + 128, ks(S2, s), ms(S1, s), ID_KT, 1u);
+                for (int s = 0; s < 8; ++s) tc_mma(tmem + 256, ks(S1, s), ks(S1, s), ID_SQ, s > 0 ? 1u : 0u);
+                for (int s = 0; s < 8; ++s) tc_mma(tmem + 256, ks(S2, s), ks(S2, s), ID_SQ, 1u);
+            });
+            if (!ok) break;
+            drain_poly(0, S0, S0, true);
+            drain_poly(128, S1, S1, false);
+            drain_poly(256, S2, S2, true);
+            // X <- P X: M-half h -> TMEM [256 h, 256 h + 64 nck); P01 = P10^T
+            ok = run([&] {
+                for (int h = 0; h < 2; ++h)
+                    for (int kb = 0; kb < 2; ++kb) {
+                        const uint8_t* Pblk = (h == 0) ? (kb == 0 ? S0 : S1) : (kb == 0 ? S1 : S2);
+                        const bool tr = (h == 0 && kb == 1);
+                        for (int s = 0; s < 8; ++s)
+                            tc_mma(tmem + 256 * h, tr ? ms(Pblk, s) : ks(Pblk, s), mx(128 * kb + 16 * s, 0),
+                                   tr ? id_px_t : id_px, (kb | s) ? 1u : 0u);
+                    }
+            });
+            if (!ok) break;
+            const float alpha = first ? inv : 1.0f;
+            if (!last) {
+                drain_x(0, 0, alpha);
+                drain_x(256, 128, alpha);
+            } else {
+                write_out(a, bk, e, X, tlane, 0, alpha, nck);
+                write_out(a, bk, e, X, tlane + 256, 128, alpha, nck);
             }
         }
-        fence_async_smem();         // the next prologue refills the slots on the copy engine
-        __syncthreads();
+    }
+    fence_async_smem();         // the next prologue refills the slots on the copy engine
+    __syncthreads();
+    return ok;
+}
+
+// Item k of this CTA: its bucket and matrix index.
+__device__ __forceinline__ void item_at(const SmallArgs& a, int k, int& bi, int& b) {
+    if (a.cta_ptr) {
+        const int it = a.items[k];
+        bi = it >> 24;
+        b = it & 0xFFFFFF;
+    } else {
+        bi = 0;
+        b = blockIdx.x + k * (int)gridDim.x;
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1) small_ns_kernel(const __grid_constant__ SmallArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctx c;
+    c.X = base;
+    c.S0 = base + X_BYTES;
+    c.S1 = c.S0 + S_BYTES;
+    c.S2 = c.S1 + S_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(c.S2 + S_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);     // bar[0] products, bar[1..3] stages
+    c.red = reinterpret_cast<float*>(tmem_slot + 2);
+    c.inv_s = c.red + 8;
+    c.tid = threadIdx.x;
+    c.warp = c.tid >> 5;
+    c.lane = c.tid & 31;
+    c.hw = c.warp >> 2;
+    c.r = 32 * (c.warp & 3) + c.lane;                              // this thread's TMEM lane
+    c.barA = smem_u32(bar);
+
+    if (c.tid == 0) {
+        for (int i = 0; i < 4; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(c.barA + 8 * i) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (c.warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem = *tmem_slot;
+    c.tlane = c.tmem + ((uint32_t)(32 * (c.warp & 3)) << 16);
+    c.phase = 0;
+    c.stream = Stream{c.barA + 8, smem_u32(c.S0), stream_stages(a), 0u, 0u};
+    pdl_wait();          // the caller's matrices may come from the previous kernel
+    pdl_trigger();
+
+    int k0, k1;
+    if (a.cta_ptr) {
+        k0 = a.cta_ptr[blockIdx.x];
+        k1 = a.cta_ptr[blockIdx.x + 1];
+    } else {
+        k0 = 0;
+        k1 = (a.bk[0].batch - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    }
+    bool ok = true;
+    for (int k = k0; k < k1 && ok; ++k) {
+        int bi, b;
+        item_at(a, k, bi, b);
+        const MatEntry* nx = nullptr;
+        int64_t nx_elems = 0;
+        if (k + 1 < k1) {
+            int nbi, nb;
+            item_at(a, k + 1, nbi, nb);
+            nx = a.bk[nbi].mats + nb;
+            nx_elems = (int64_t)a.bk[nbi].m * a.bk[nbi].n;
+        }
+        const SmallBucket& bk = a.bk[bi];
+        ok = bk.m > 128 ? process<256>(a, bk, b, nx, nx_elems, c) : process<128>(a, bk, b, nx, nx_elems, c);
     }
 
     if (!ok) {
-        if (tid == 0) {
+        if (c.tid == 0) {
             atomicOr(a.status, STATUS_TIMEOUT);
-            tc_commit(barA);                // wait (bounded) for the products in flight
-            wait_limited(barA, phase);
-            for (uint32_t k = stream.consumed; k < stream.issued; ++k)      // and the staged loads
-                wait_limited(stream.bars + 8 * (k % stream.nst), (k / stream.nst) & 1u);
+            tc_commit(c.barA);              // wait (bounded) for the products in flight
+            wait_limited(c.barA, c.phase);
+            for (uint32_t k = c.stream.consumed; k < c.stream.issued; ++k)     // and the staged loads
+                wait_limited(c.stream.bars + 8 * (k % c.stream.nst), (k / c.stream.nst) & 1u);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (c.warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(c.tmem) : "memory");
     }
 }
 
 }  // namespace small
 
 bool small_ns_fits(int m, int n, int nseg, const int* segs) {
-    if (m < 1 || n < m || nseg < 1 || nseg > 16) return false;
+    if (m < 1 || n < m || nseg < 1 || nseg > 8) return false;
     if (m <= 128) {
         if (n > 512) return false;
         for (int i = 0; i < nseg; ++i)
@@ -755,18 +815,24 @@ bool small_ns_fits(int m, int n, int nseg, const int* segs) {
 }
 
 cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s) {
-    static cudaError_t attr128 = cudaFuncSetAttribute(small::small_ns_kernel<128>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, small::SMEM_BYTES);
-    static cudaError_t attr256 = cudaFuncSetAttribute(small::small_ns_kernel<256>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, small::SMEM_BYTES);
-    if (attr128 != cudaSuccess) return attr128;
-    if (attr256 != cudaSuccess) return attr256;
-    if (!small_ns_fits(a.m, a.n, a.nseg, a.segs) || a.batch < 1) return cudaErrorInvalidValue;
-    if (a.param_dtype != MUON_BF16) return cudaErrorInvalidValue;
-    const int grid = a.batch < num_sms ? a.batch : num_sms;
-    if (a.m > 128)
-        return launch_pdl(small::small_ns_kernel<256>, dim3(grid), dim3(small::NT), (size_t)small::SMEM_BYTES, s, a);
-    return launch_pdl(small::small_ns_kernel<128>, dim3(grid), dim3(small::NT), (size_t)small::SMEM_BYTES, s, a);
+    static cudaError_t attr = cudaFuncSetAttribute(small::small_ns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   small::SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    if (a.nb < 1 || a.nb > SMALL_MAX_BUCKETS || a.param_dtype != MUON_BF16) return cudaErrorInvalidValue;
+    for (int i = 0; i < a.nb; ++i) {
+        const SmallBucket& bk = a.bk[i];
+        if (!small_ns_fits(bk.m, bk.n, bk.nseg, bk.segs) || bk.batch < 1 || bk.batch >= (1 << 24))
+            return cudaErrorInvalidValue;
+    }
+    int grid;
+    if (a.cta_ptr) {
+        if (!a.items || a.grid < 1 || a.grid > num_sms) return cudaErrorInvalidValue;
+        grid = a.grid;
+    } else {
+        if (a.nb != 1) return cudaErrorInvalidValue;
+        grid = a.bk[0].batch < num_sms ? a.bk[0].batch : num_sms;
+    }
+    return launch_pdl(small::small_ns_kernel, dim3(grid), dim3(small::NT), (size_t)small::SMEM_BYTES, s, a);
 }
 
 }  // namespace muon

@@ -82,3 +82,25 @@ def test_group_validation(mg):
     with pytest.raises(mg.MuonError):
         h = mg.MuonGroup(W, G, M)
         mg.muon_group_step(h.handle, float("nan"), 0.9, 0.0, False)
+
+
+def test_group_fused_buckets_match_step(mg, monkeypatch):
+    """Five fused buckets of both forms (128-row and 256-row) in one fused
+    launch with work lists, replayed from the group's graph: bitwise the same
+    weights and momenta as muon_step on the same inputs."""
+    monkeypatch.setenv("MUON_SMALL", "1")
+    monkeypatch.setenv("MUON_GRAPH", "1")
+    shapes = [(128, 512)] * 5 + [(256, 256)] * 3 + [(192, 256), (512, 128), (256, 200), (64, 96)]
+    W1, G1, M1 = _make(shapes, torch.bfloat16, torch.bfloat16, 31)
+    W2, G2, M2 = [w.clone() for w in W1], [g.clone() for g in G1], [m.clone() for m in M1]
+    group = mg.MuonGroup(W1, G1, M1)
+    try:
+        for _ in range(3):
+            group.step(lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+            mg.muon_step(W2, G2, M2, lr=0.02, beta=0.95, wd=0.1, nesterov=False)
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+        for a, b in zip(W1 + M1, W2 + M2):
+            assert torch.equal(a, b)
+    finally:
+        group.close()
