@@ -308,6 +308,76 @@ __device__ __forceinline__ void epi_mirror_staged(const GemmArgs& a, int b, int 
     __syncwarp();
 }
 
+// Workspace products (EPI_STORE / EPI_POLY) of one warp's 32 x 32 chunk
+// (rows r0 + lane, columns c0..) through the 32 x 33 staging area: the final
+// values are staged once, then both the rows and (symmetric) the mirrored
+// rows leave as 8-column segments, four lanes per 64-byte row piece, so every
+// store transaction is a whole 32-byte sector (a lane writing 16 bytes of its
+// own row costs one half-sector transaction per lane).  Symmetric products
+// keep (r, c) with c <= r and mirror c < r to (c, r).
+__device__ __forceinline__ void epi_store_staged(const GemmArgs& a, int b, int r0, int c0, float (&v)[32], float s,
+                                                 const float (&g)[32], float (*stage)[33]) {
+    const int lane = threadIdx.x & 31;
+    const int r = r0 + lane;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= s;
+    if (a.epi == EPI_POLY) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = a.pc * v[j] + a.pb * g[j] + ((c0 + j) == r ? a.pa : 0.f);
+    }
+    if (a.round_tf32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = round_tf32(v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[lane][j] = v[j];
+    __syncwarp();
+    const int64_t cbase = (int64_t)b * a.strideC;
+    const int sg = lane & 3;
+    // rows: pass p writes rows r0 + 8p + lane / 4, columns c0 + 8 sg ..
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+        const int i = pass * 8 + (lane >> 2);
+        const int rr = r0 + i, cc = c0 + 8 * sg;
+        if (rr < a.M && cc < a.N) {
+            float w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = stage[i][8 * sg + k];
+            const int64_t off = cbase + (int64_t)rr * a.ldc + cc;
+            if (cc + 7 < a.N && (!a.symmetric || cc + 7 <= rr)) {
+                store_row_run<8>(a.C, off, w, a.c_dtype);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (cc + k < a.N && (!a.symmetric || cc + k <= rr)) st_elem(a.C, off + k, w[k], a.c_dtype);
+            }
+        }
+    }
+    // mirrored rows: pass p writes row c0 + 8p + lane / 4, columns r0 + 8 sg ..
+    if (a.symmetric && c0 < r0 + 31) {
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int i = pass * 8 + (lane >> 2);    // mirrored row c0 + i
+            const int c = c0 + i;
+            const int rb = r0 + 8 * sg;              // its columns rb .. rb+7 (rows of the chunk)
+            float w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = stage[8 * sg + k][i];
+            if (c < a.N) {
+                const int64_t off = cbase + (int64_t)c * a.ldc + rb;
+                if (c < rb && rb + 7 < a.M) {
+                    store_row_run<8>(a.C, off, w, a.c_dtype);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (rb + k < a.M && c < rb + k) st_elem(a.C, off + k, w[k], a.c_dtype);
+                }
+            }
+        }
+    }
+    __syncwarp();
+}
+
 // Convenience for callers without pipelining: scale, table entry and loads
 // for one chunk, then the epilogue.
 template <int W>

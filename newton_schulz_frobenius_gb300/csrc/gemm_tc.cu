@@ -641,8 +641,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     epi_load_chunk<32>(args, ent, b, row0 + lane, col0 + 32, gnxt);
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-                epi_row_chunk<32, false>(args, ent, b, row0 + lane, col0, v, scale, gcur);
-                if (B_KMAJOR && args.symmetric) epi_mirror_staged(args, b, row0, col0, v, mstage);
+                if (B_KMAJOR && (args.epi == EPI_STORE || args.epi == EPI_POLY)) {
+                    // workspace products: rows and mirrored rows through the staging area
+                    epi_store_staged(args, b, row0, col0, v, scale, gcur, mstage);
+                } else {
+                    epi_row_chunk<32, false>(args, ent, b, row0 + lane, col0, v, scale, gcur);
+                }
                 if (loads) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) gcur[j] = gnxt[j];
