@@ -41,6 +41,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace muon {
@@ -155,6 +157,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+
+// Tile store shared -> global on the copy engine (bulk group of this thread).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's stores may be overwritten
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's stores are complete
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -376,6 +391,58 @@ struct TileSched {
     }
 };
 
+// 16-bit workspace products (EPI_STORE / EPI_POLY): one warp's 32 x 32 chunk
+// (rows r0 + lane, columns c0..) is converted into the warp's staging area
+// (4 KB: the chunk, then its transpose, 64-byte rows) and leaves as tile stores
+// on the copy engine, so the warp issues two instructions instead of sixteen
+// row-piece stores.  Symmetric products: a chunk below the diagonal is stored
+// at (r0, c0) and transposed at (c0, r0); the diagonal chunk (c0 == r0) is
+// assembled symmetric (rows c <= r from v, the rest mirrored) and stored once,
+// so no element is written twice.  The stores clip at the matrix edge.
+__device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorMap* tmC, int b, int r0, int c0,
+                                              float (&v)[32], float s, const float (&g)[32], uint8_t* stg,
+                                              bool& pending) {
+    const int lane = threadIdx.x & 31;
+    const int r = r0 + lane;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= s;
+    if (a.epi == EPI_POLY) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = a.pc * v[j] + a.pb * g[j] + ((c0 + j) == r ? a.pa : 0.f);
+    }
+    const bool f16 = (a.c_dtype == MUON_F16);
+    if (pending) {              // the previous chunk's stores have read the staging
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+    }
+    uint8_t* nrm = stg;
+    uint8_t* trn = stg + 2048;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(nrm + lane * 64 + 16 * u) = pack8_h(v + 8 * u, f16);
+    const bool below = a.symmetric && c0 < r0;
+    const bool diag = a.symmetric && c0 == r0;
+    if (below || diag) {
+        if (diag) __syncwarp();     // the mirrored entries replace the row stores' upper part
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            // element (j, lane) of the transpose, or of the diagonal chunk's upper part
+            uint8_t* dst = (below ? trn : nrm) + j * 64 + lane * 2;
+            if (below || j < lane) {
+                if (f16) *reinterpret_cast<__half*>(dst) = __float2half_rn(v[j]);
+                else *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v[j]);
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmC, smem_u32(nrm), c0, r0, b);
+        if (below) tma_store_3d(tmC, smem_u32(trn), r0, c0, b);
+        bulk_commit();
+    }
+    pending = true;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -383,7 +450,7 @@ struct TileSched {
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ GemmArgs args, const TileSched sched) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args, const TileSched sched) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
@@ -595,6 +662,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         float (*mstage)[33] = reinterpret_cast<float (*)[33]>(mirror_stage + (warp - 2) * 32 * 33);
         const int half = (warp - 2) / 4;           // which half of the tile's columns
         constexpr int HALF_COLS = BN / 2;
+        bool tma_pending = false;                  // this warp's bulk stores may still read its staging
         int acc = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < sched.total; t += ustep) {
@@ -641,7 +709,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     epi_load_chunk<32>(args, ent, b, row0 + lane, col0 + 32, gnxt);
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-                if (B_KMAJOR && (args.epi == EPI_STORE || args.epi == EPI_POLY)) {
+                if (B_KMAJOR && args.tma_c) {
+                    // 16-bit workspace products: the chunk (and its mirror) leave on the copy engine
+                    epi_store_tma(args, &tmC, b, row0, col0, v, scale, gcur,
+                                  reinterpret_cast<uint8_t*>(&mstage[0][0]), tma_pending);
+                } else if (B_KMAJOR && (args.epi == EPI_STORE || args.epi == EPI_POLY)) {
                     // workspace products: rows and mirrored rows through the staging area
                     epi_store_staged(args, b, row0, col0, v, scale, gcur, mstage);
                 } else {
@@ -661,6 +733,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
+        if (tma_pending && lane == 0) bulk_wait0();    // the stores are complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -695,7 +769,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // matrices of `rows` x `inner` (row pitch ld, matrix pitch stride, in
 // elements), box box_inner x box_rows x 1, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t batch,
-              uint64_t ld, uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
+              uint64_t ld, uint64_t stride, uint32_t box_inner, uint32_t box_rows, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return false;
     if (batch <= 1) stride = ld * rows;
@@ -709,9 +783,17 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t inner, uint6
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, elem,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// MUON_TMA_STORE=0 routes 16-bit workspace outputs through the staged row
+// stores instead (both write the same values; the tests compare them)
+bool tma_store_enabled() {
+    const char* e = std::getenv("MUON_TMA_STORE");
+    return !(e && e[0] == '0');
 }
 
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
@@ -753,6 +835,18 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
                         : make_map(&mB, a.B, a.dtype, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.batch,
                                    (uint64_t)a.ldb, (uint64_t)a.strideB, 64, BK);
     if (!okB) return cudaErrorInvalidValue;
+    // 16-bit workspace outputs of K-major launches leave through tile stores
+    CUtensorMap mC;
+    std::memset(&mC, 0, sizeof mC);
+    GemmArgs ga = a;
+    ga.tma_c = 0;
+    const bool c16 = is_half(a.c_dtype) && !a.round_tf32;
+    const bool al = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 8 == 0) && (a.strideC % 8 == 0 || a.batch <= 1);
+    if (B_KMAJOR && (a.epi == EPI_STORE || a.epi == EPI_POLY) && c16 && al && tma_store_enabled()) {
+        if (make_map(&mC, a.C, a.c_dtype, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.ldc,
+                     (uint64_t)a.strideC, 32, 32, false))
+            ga.tma_c = 1;
+    }
 
     TileSched sc;
     sc.tiles_m = (a.M + BM - 1) / BM;
@@ -772,7 +866,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     sc.total = sc.per_batch * a.batch;
     if (!PAIR) {
         const int grid = sc.total < num_sms ? sc.total : num_sms;
-        return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, a, sc);
+        return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, mC, ga, sc);
     }
     int clusters = std::min(num_sms / 2, max_clusters);
     if (sc.total < clusters) clusters = sc.total;
@@ -790,7 +884,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, mA, mB, a, sc);
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, ga, sc);
 }
 
 }  // namespace tc

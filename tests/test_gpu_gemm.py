@@ -193,3 +193,48 @@ def test_paired_products(mg, monkeypatch, kind, M, N, K, batch):
         assert err < 2e-3, err
     else:
         _check(out[1], ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("kind,M,N,K,batch,tile", [
+    ("sym", 264, 264, 200, 2, 256), ("sym", 896, 896, 136, 1, 128), ("sym", 384, 384, 520, 1, 256),
+    ("kmajor", 200, 264, 136, 3, 256), ("kmajor", 384, 1000, 72, 1, 128), ("poly", 296, 296, 0, 2, 256)])
+def test_tile_store_epilogue(mg, monkeypatch, dtype, kind, M, N, K, batch, tile):
+    """16-bit workspace products leave the kernel as 32 x 32 tile stores (a chunk
+    below the diagonal also as its transpose, the diagonal chunk assembled
+    symmetric).  They write the same values as the staged row stores
+    (MUON_TMA_STORE=0), bit for bit, cover every element of a ragged output
+    (C starts as NaN) and keep a symmetric product exactly symmetric."""
+    poly = kind == "poly"
+    sym = kind in ("sym", "poly")
+    if poly:
+        X = _rand((batch, M, 2 * M), torch.float64, 41)
+        G = torch.matmul(X, X.transpose(1, 2))
+        A = (G / torch.linalg.matrix_norm(G, ord=2, keepdim=True)).to(dtype).contiguous()
+        B = A
+    else:
+        A = _rand((batch, M, K), dtype, 42, scale=1.0 / np.sqrt(K))
+        B = A if sym else _rand((batch, N, K), dtype, 43)
+    out = []
+    for flag in ("0", "1"):
+        monkeypatch.setenv("MUON_TMA_STORE", flag)
+        C = torch.full((batch, M, N), float("nan"), dtype=dtype, device="cuda")
+        if poly:
+            mg.muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=True, poly=(3.4445, -4.7750, 2.0315), tile_n=tile)
+        else:
+            mg.muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=sym, tile_n=tile)
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+        out.append(C)
+    assert not torch.isnan(out[1]).any()
+    assert torch.equal(out[0], out[1])
+    if sym:
+        assert torch.equal(out[1], out[1].transpose(1, 2))
+    Ad = A.double()
+    if poly:
+        a, b, c = 3.4445, -4.7750, 2.0315
+        ref = a * torch.eye(M, device="cuda", dtype=torch.float64) + b * Ad + c * torch.matmul(Ad, Ad)
+    else:
+        ref = torch.matmul(Ad, B.double().transpose(1, 2))
+    err = ((out[1].double() - ref).norm() / ref.norm()).item()
+    assert err < (1e-2 if dtype == torch.bfloat16 else 2e-3), err
