@@ -136,6 +136,8 @@ constexpr int STAGE_SLOTS = 4;
 struct Workspace {
     char* base = nullptr;
     size_t bytes = 0;
+    int* pcnt = nullptr;        // prep kernel's per-matrix arrival counters (zero between launches)
+    int pcnt_cap = 0;
     MatEntry* h_stage[STAGE_SLOTS] = {nullptr, nullptr, nullptr, nullptr};
     cudaEvent_t ev[STAGE_SLOTS] = {nullptr, nullptr, nullptr, nullptr};
     size_t stage_cap = 0;   // entries per slot
@@ -167,6 +169,34 @@ static int ws_get(int dev, cudaStream_t s, size_t need, Workspace** out) {
         logf(2, "workspace grown to %zu bytes on device %d", want, dev);
     }
     *out = &w;
+    return MUON_OK;
+}
+
+// At least B prep counters for stream s on device dev, zero (grown, never
+// shrunk; each launch leaves them at zero again).
+static int prep_counters(int dev, cudaStream_t s, int B, int** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.pcnt_cap < B) {
+        if (w.pcnt) {
+            cudaError_t e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize(counters grow)");
+            cudaFree(w.pcnt);
+            w.pcnt = nullptr;
+            w.pcnt_cap = 0;
+        }
+        const int cap = std::max(B, 4096);
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&w.pcnt), (size_t)cap * sizeof(int));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            w.pcnt = nullptr;
+            return fail(MUON_ENOMEM, "prep counters: %s", cudaGetErrorString(e));
+        }
+        e = cudaMemsetAsync(w.pcnt, 0, (size_t)cap * sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(prep counters)");
+        w.pcnt_cap = cap;
+    }
+    *out = w.pcnt;
     return MUON_OK;
 }
 
@@ -553,7 +583,7 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
 
 static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
                     const MatEntry* d_mats, int in_dtype, int mom_dtype, int x_dtype, bool with_mom, int nesterov,
-                    float beta, bool vec_ok, const float* hyper = nullptr) {
+                    float beta, bool vec_ok, int* cnt, const float* hyper = nullptr) {
     PrepArgs p;
     std::memset(&p, 0, sizeof p);
     p.mats = d_mats;
@@ -564,7 +594,7 @@ static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLay
     p.beta = beta;
     p.X = base + L.off_X; p.ldx = L.ldx; p.strideX = (int64_t)m * L.ldx;
     p.partials = reinterpret_cast<float*>(base + L.off_part);
-    p.nparts = L.nparts;
+    p.nparts = prep_grid_parts(m, n, B);       // CTAs per matrix, one partial each (<= L.nparts)
     p.vec_ok = vec_ok ? 1 : 0;
     p.hyper = hyper;
     p.write_x = 1;
@@ -574,30 +604,40 @@ static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLay
     const double bytes = in_bytes + elems * ((with_mom ? esize(mom_dtype) : 0.0) + esize(x_dtype));
     float* inv = reinterpret_cast<float*>(base + L.off_inv);
     const bool two_pass = !x_holds_u(x_dtype);
+    // with counters the (first) prep launch finalises the norm itself
+    PrepArgs pf = p;
+    if (cnt) {
+        pf.counter = cnt;
+        pf.inv = inv;
+        pf.eps = 1e-7f;
+        pf.status = dc.status;
+    }
     auto finalize = [&]() -> int {
         note_launch_begin(KC_NORM, s);
-        cudaError_t e = launch_norm_finalize(p.partials, L.nparts, B, 1e-7f, inv, dc.status, s);
-        note_launch_end(KC_NORM, (double)L.nparts * B * 4.0, s);
+        cudaError_t e = launch_norm_finalize(p.partials, p.nparts, B, 1e-7f, inv, dc.status, s);
+        note_launch_end(KC_NORM, (double)p.nparts * B * 4.0, s);
         return e == cudaSuccess ? MUON_OK : cuda_fail(e, "norm launch");
     };
     if (two_pass) {
         // fp16 X: sums of U^2 first (nothing written), then momentum and U / ||U||
-        PrepArgs p1 = p;
+        PrepArgs p1 = pf;
         p1.write_x = 0;
         p1.write_mom = 0;
         note_launch_begin(KC_PREP, s);
         cudaError_t e = launch_prep(p1, s);
         note_launch_end(KC_PREP, in_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-        int r = finalize();
-        if (r) return r;
+        if (!cnt) {
+            int r = finalize();
+            if (r) return r;
+        }
         p.x_scale = inv;
     }
     note_launch_begin(KC_PREP, s);
-    cudaError_t e = launch_prep(p, s);
+    cudaError_t e = launch_prep(two_pass ? p : pf, s);
     note_launch_end(KC_PREP, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-    return two_pass ? MUON_OK : finalize();
+    return (two_pass || cnt) ? MUON_OK : finalize();
 }
 
 }  // namespace muon
@@ -1131,7 +1171,9 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
     for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
         const int B = (int)std::min<int64_t>(chunk, batch - b0);
         const ChunkLayout LB = chunk_layout(om, on, B, nsd);
-        if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, nsd, false, 0, 0.f, vec_ok)))
+        int* pc = nullptr;
+        if ((r = prep_counters(dc.device, s, B, &pc))) return r;
+        if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, nsd, false, 0, 0.f, vec_ok, pc)))
             return r;
         FinalEpi fin{EPI_OUT, d_table + b0, dtype, 0.f, 0.f, 0.f};
         if ((r = run_ns(dc, s, cbase, LB, om, on, B, nsd, plan, x_holds_u(nsd), fin))) return r;
@@ -1260,8 +1302,10 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
             const int B = (int)std::min<size_t>(chunks[k], idx.size() - c0);
             const ChunkLayout L = chunk_layout(m, n, B, nsd);
             const MatEntry* dm = d_table + first + c0;
+            int* pc = nullptr;
+            if ((r = prep_counters(dc.device, s, B, &pc))) return r;
             if ((r = run_prep(dc, s, cbase, L, m, n, B, dm, param_dtype, mom_dtype, nsd, true, nesterov, beta,
-                              vec_ok)))
+                              vec_ok, pc)))
                 return r;
             FinalEpi fin{EPI_UPDATE, dm, param_dtype, lr, wd, scale};
             if ((r = run_ns(dc, s, cbase, L, m, n, B, nsd, plans[k], x_holds_u(nsd), fin))) return r;
@@ -1531,9 +1575,12 @@ namespace muon {
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(64) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+// the prep kernel's per-matrix arrival counters (zero between launches)
+static __device__ int g_noalloc_prep_cnt[65536];
 
 struct NoallocDev {
     char* base = nullptr;   // device address of g_noalloc_scratch on this device
+    int* pcnt = nullptr;    // device address of g_noalloc_prep_cnt
     int sms = 0;
 };
 static std::map<int, NoallocDev> g_noalloc_dev;
@@ -1559,6 +1606,11 @@ static int noalloc_setup(NoallocDev& out) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
         NoallocDev d;
         d.base = static_cast<char*>(p);
+        e = cudaGetSymbolAddress(&p, g_noalloc_prep_cnt);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(counters)");
+        d.pcnt = static_cast<int*>(p);
+        e = cudaMemset(d.pcnt, 0, sizeof(g_noalloc_prep_cnt));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counters)");
         d.sms = sms;
         it = g_noalloc_dev.emplace(dev, d).first;
     }
@@ -1623,7 +1675,8 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
     std::vector<int> segs(segments, segments + num_segments);
     NsPlan plan = make_plan(coeffs, steps, segs, path, 256, om, on);
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
-    if ((r = run_prep(dc, s, cbase, L, om, on, (int)batch, d_table, dtype, dtype, nsd, false, 0, 0.f, vec_ok)))
+    if ((r = run_prep(dc, s, cbase, L, om, on, (int)batch, d_table, dtype, dtype, nsd, false, 0, 0.f, vec_ok,
+                      nd.pcnt)))
         return r;
     FinalEpi fin{EPI_OUT, d_table, dtype, 0.f, 0.f, 0.f};
     return run_ns(dc, s, cbase, L, om, on, (int)batch, nsd, plan, x_holds_u(nsd), fin);
@@ -1653,6 +1706,7 @@ struct muon_group {
     std::vector<int> chunks;
     char* ws = nullptr;
     size_t ws_bytes = 0;
+    int* pcnt = nullptr;                            // prep counters at the end of ws (zero between launches)
     MatEntry* d_table = nullptr;
     float* d_hyper = nullptr;
     char* cbase = nullptr;
@@ -1688,7 +1742,7 @@ static int group_enqueue(muon_group* g, cudaStream_t s) {
             const ChunkLayout L = chunk_layout(m, n, B, g->ns_dtype);
             const MatEntry* dm = g->d_table + first + c0;
             if ((r = run_prep(g->dc, s, g->cbase, L, m, n, B, dm, g->param_dtype, g->mom_dtype, g->ns_dtype, true,
-                              0, 0.f, g->vec_ok[k] != 0, g->d_hyper)))
+                              0, 0.f, g->vec_ok[k] != 0, g->pcnt, g->d_hyper)))
                 return r;
             FinalEpi fin{EPI_UPDATE, dm, g->param_dtype, 0.f, 0.f, scale, g->d_hyper};
             if ((r = run_ns(g->dc, s, g->cbase, L, m, n, B, g->ns_dtype, plan, x_holds_u(g->ns_dtype), fin))) return r;
@@ -1733,7 +1787,8 @@ static int group_plan(muon_group* g, cudaStream_t s) {
     size_t work_bytes = 0;
     g->fused = plan_fused(g->dc, g->plans, g->keys, g->bucket_size, g->ns_dtype, &work_bytes);
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)g->count, 256);
-    const size_t need = table_bytes + 256 + work_bytes + chunk_need;
+    const size_t cnt_off = align_up(table_bytes + 256 + work_bytes + chunk_need, 256);
+    const size_t need = cnt_off + sizeof(int) * (size_t)g->count;
     if (g->ws_bytes < need) {
         MUON_CUDA(cudaStreamSynchronize(s));
         group_drop_graph(g);
@@ -1760,6 +1815,9 @@ static int group_plan(muon_group* g, cudaStream_t s) {
         MUON_CUDA(cudaStreamSynchronize(s));
         MUON_CUDA(cudaMemcpy(g->d_work, blk.data(), work_bytes, cudaMemcpyHostToDevice));
     }
+    // the prep counters after the chunks (they move with them): zeroed
+    g->pcnt = reinterpret_cast<int*>(g->ws + cnt_off);
+    MUON_CUDA(cudaMemsetAsync(g->pcnt, 0, sizeof(int) * (size_t)g->count, s));
     group_drop_graph(g);
     g->direct_done = false;
     g->version = version;

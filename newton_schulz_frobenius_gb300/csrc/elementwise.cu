@@ -22,6 +22,8 @@ namespace muon {
 namespace {
 
 constexpr int PT = 64;          // tile edge
+
+__host__ __device__ __forceinline__ int prep_tiles(int m, int n) { return ((m + PT - 1) / PT) * ((n + PT - 1) / PT); }
 constexpr int PTHREADS = 256;   // 64 rows x 4 segments of 16 elements
 
 __device__ __forceinline__ void load16(const void* p, int dtype, int64_t off, int valid, bool vec,
@@ -70,24 +72,41 @@ __device__ __forceinline__ void store16(void* p, int dtype, int64_t off, int val
         if (j < valid) st_elem(p, off + j, v[j], dtype);
 }
 
-__global__ void __launch_bounds__(PTHREADS)
-prep_kernel(const __grid_constant__ PrepArgs a) {
-    __shared__ float tile[PT][PT + 1];
-    __shared__ float red[PTHREADS / 32];
+// Sum of one matrix's nparts partial sums of squares by a 256-thread block, in
+// double and in a fixed order (eight independent loads in flight per thread,
+// then warp and block sums); the total is returned to thread 0.
+__device__ double sum_partials_256(const float* pb, int nparts, double* red) {
+    double s = 0.0;
+    for (int i0 = threadIdx.x; i0 < nparts; i0 += 256 * 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + 256 * u;
+            v[u] = i < nparts ? __ldcg(pb + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += (double)v[u];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < 8; ++w) t += red[w];
+    return t;
+}
 
-    pdl_wait();
-    pdl_trigger();
-    const int b = blockIdx.y;
+// One 64 x 64 tile of the oriented matrix b: momentum, U into X, and this
+// thread's sum of squares of U added to ss.
+__device__ __forceinline__ void prep_tile(const PrepArgs& a, const MatEntry& e, int b, int tile_idx, float beta,
+                                          int nesterov, float (*tile)[PT + 1], float& ss) {
     const int tiles_c = (a.n + PT - 1) / PT;
-    const int tr = blockIdx.x / tiles_c;
-    const int tc = blockIdx.x % tiles_c;
-    const MatEntry e = a.mats[b];
-    const float beta = a.hyper ? a.hyper[1] : a.beta;
-    const int nesterov = a.hyper ? (a.hyper[3] != 0.f) : a.nesterov;
+    const int tr = tile_idx / tiles_c;
+    const int tc = tile_idx % tiles_c;
     const int lr = threadIdx.x >> 2;          // row within the tile
     const int seg = (threadIdx.x & 3) * 16;   // first of 16 columns
     const bool vec = a.vec_ok != 0;
-
     // Raw (caller) coordinates of this thread's 16 elements.
     int raw_r, raw_c0, raw_rows, raw_cols;
     if (!e.trans) {
@@ -102,7 +121,6 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
     const int64_t off = (int64_t)raw_r * raw_cols + raw_c0;
 
     float u[16];
-    float ss = 0.f;
     if (valid > 0) {
         float g[16];
         load16(e.grad, a.in_dtype, off, valid, vec, g);
@@ -152,8 +170,28 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = tile[seg + j][lr];
+        __syncthreads();        // the tile is read before the next one overwrites it
         if (ovalid > 0) store16(a.X, a.x_dtype, xb + (int64_t)orow * a.ldx + ocol0, ovalid, xvec, x);
     }
+}
+
+
+// Grid (parts, batch): CTA p of matrix b takes the tiles p, p + parts, ... and
+// writes one partial sum of squares.
+__global__ void __launch_bounds__(PTHREADS)
+prep_kernel(const __grid_constant__ PrepArgs a) {
+    __shared__ float tile[PT][PT + 1];
+    __shared__ float red[PTHREADS / 32];
+
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.y;
+    const MatEntry e = a.mats[b];
+    const float beta = a.hyper ? a.hyper[1] : a.beta;
+    const int nesterov = a.hyper ? (a.hyper[3] != 0.f) : a.nesterov;
+    const int ntiles = prep_tiles(a.m, a.n);
+    float ss = 0.f;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) prep_tile(a, e, b, t, beta, nesterov, tile, ss);
 
     // Block sum of squares -> one partial per tile.
 #pragma unroll
@@ -166,6 +204,25 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
         for (int w = 0; w < PTHREADS / 32; ++w) t += red[w];
         a.partials[(int64_t)b * a.nparts + blockIdx.x] = t;
     }
+    if (!a.counter) return;
+    // The CTA that completes matrix b's count turns its partials into the
+    // scale 1/(||U||_F + eps) (the same sum, in the same order, as
+    // norm_finalize_kernel) and resets the count for the next launch.
+    __shared__ int s_last;
+    __shared__ double dred[PTHREADS / 32];
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(a.counter + b, 1) == a.nparts - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const double t = sum_partials_256(a.partials + (int64_t)b * a.nparts, a.nparts, dred);
+    if (threadIdx.x == 0) {
+        if (!isfinite(t)) atomicOr(a.status, STATUS_NONFINITE);
+        a.inv[b] = (float)(1.0 / (sqrt(t) + (double)a.eps));
+        a.counter[b] = 0;
+    }
 }
 
 __global__ void __launch_bounds__(256)
@@ -175,26 +232,8 @@ norm_finalize_kernel(const float* __restrict__ partials, int nparts, float eps,
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x;
-    const float* pb = partials + (int64_t)b * nparts;
-    // eight independent loads in flight per thread, summed in double
-    double s = 0.0;
-    for (int i0 = threadIdx.x; i0 < nparts; i0 += 256 * 8) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + 256 * u;
-            v[u] = i < nparts ? pb[i] : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) s += (double)v[u];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-    __syncthreads();
+    const double t = sum_partials_256(partials + (int64_t)b * nparts, nparts, red);
     if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < 8; ++w) t += red[w];
         if (!isfinite(t)) atomicOr(status, STATUS_NONFINITE);
         inv[b] = (float)(1.0 / (sqrt(t) + (double)eps));
     }
@@ -218,12 +257,18 @@ __global__ void fill_synthetic_kernel(void* X, int64_t count, int dtype, float s
 
 }  // namespace
 
-int prep_num_parts(int m, int n) {
-    return ((m + PT - 1) / PT) * ((n + PT - 1) / PT);
+int prep_num_parts(int m, int n) { return prep_tiles(m, n); }
+
+int prep_grid_parts(int m, int n, int batch) {
+    // about 2048 CTAs per launch: a few tiles each, so that the per-matrix
+    // partial sums (and the finalising count) stay short
+    const int t = prep_tiles(m, n);
+    const int want = (2048 + batch - 1) / batch;
+    return t < want ? t : (want < 1 ? 1 : want);
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-    dim3 grid(prep_num_parts(a.m, a.n), a.batch);
+    dim3 grid(a.nparts, a.batch);
     return launch_pdl(prep_kernel, grid, dim3(PTHREADS), 0, s, a);
 }
 

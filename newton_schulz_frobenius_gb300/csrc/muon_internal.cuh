@@ -94,14 +94,22 @@ struct PrepArgs {
     float beta;
     void* X; int64_t ldx; int64_t strideX;
     float* partials;        // [batch][nparts]
-    int nparts;
+    int nparts;             // CTAs per matrix (the grid's x), each writing one partial
     int vec_ok;             // caller rows are 16-byte aligned for vector access
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides beta, nesterov
     int write_x;            // store U (times x_scale) into X
     int write_mom;          // store M' (0: a first pass that only sums U^2)
     const float* x_scale;   // optional per-matrix factor applied to U before it is stored
+    // Optional in-kernel finalisation: per-matrix arrival counters (zero
+    // before the launch, zero again after it); the last CTA of matrix b
+    // writes inv[b] = 1/(||U||_F + eps) and flags a non-finite sum in status.
+    int* counter;
+    float* inv;
+    float eps;
+    int* status;
 };
-int prep_num_parts(int m, int n);
+int prep_num_parts(int m, int n);              // 64 x 64 tiles of one matrix (partials capacity)
+int prep_grid_parts(int m, int n, int batch);   // CTAs (partials) per matrix of one launch
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
 // Whole update of small matrices, one CTA per matrix (see small_ns.cu): the
