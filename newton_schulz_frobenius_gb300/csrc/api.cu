@@ -604,20 +604,13 @@ static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLay
     const double bytes = in_bytes + elems * ((with_mom ? esize(mom_dtype) : 0.0) + esize(x_dtype));
     float* inv = reinterpret_cast<float*>(base + L.off_inv);
     const bool two_pass = !x_holds_u(x_dtype);
-    // with counters the (first) prep launch finalises the norm itself
+    // the (first) prep launch finalises the norm itself: its last CTA per
+    // matrix writes inv (cnt: zero per-matrix counters, left at zero)
     PrepArgs pf = p;
-    if (cnt) {
-        pf.counter = cnt;
-        pf.inv = inv;
-        pf.eps = 1e-7f;
-        pf.status = dc.status;
-    }
-    auto finalize = [&]() -> int {
-        note_launch_begin(KC_NORM, s);
-        cudaError_t e = launch_norm_finalize(p.partials, p.nparts, B, 1e-7f, inv, dc.status, s);
-        note_launch_end(KC_NORM, (double)p.nparts * B * 4.0, s);
-        return e == cudaSuccess ? MUON_OK : cuda_fail(e, "norm launch");
-    };
+    pf.counter = cnt;
+    pf.inv = inv;
+    pf.eps = 1e-7f;
+    pf.status = dc.status;
     if (two_pass) {
         // fp16 X: sums of U^2 first (nothing written), then momentum and U / ||U||
         PrepArgs p1 = pf;
@@ -627,17 +620,13 @@ static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLay
         cudaError_t e = launch_prep(p1, s);
         note_launch_end(KC_PREP, in_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-        if (!cnt) {
-            int r = finalize();
-            if (r) return r;
-        }
         p.x_scale = inv;
     }
     note_launch_begin(KC_PREP, s);
     cudaError_t e = launch_prep(two_pass ? p : pf, s);
     note_launch_end(KC_PREP, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-    return (two_pass || cnt) ? MUON_OK : finalize();
+    return MUON_OK;
 }
 
 }  // namespace muon

@@ -1,5 +1,6 @@
 // Elementwise kernels of the Muon update: momentum (+Nesterov), orientation
-// into the workspace, Frobenius partial sums, and the norm finalisation.
+// into the workspace, Frobenius partial sums, and the norm finalisation (by
+// the last CTA to finish each matrix).
 //
 // Momentum smooths the gradient before Newton-Schulz ("MuonX" page, section 2);
 // the Frobenius normalisation places every singular value at or below 1 before
@@ -206,8 +207,8 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
     }
     if (!a.counter) return;
     // The CTA that completes matrix b's count turns its partials into the
-    // scale 1/(||U||_F + eps) (the same sum, in the same order, as
-    // norm_finalize_kernel) and resets the count for the next launch.
+    // scale 1/(||U||_F + eps) (summed in double in a fixed order) and resets
+    // the count for the next launch.
     __shared__ int s_last;
     __shared__ double dred[PTHREADS / 32];
     if (threadIdx.x == 0) {
@@ -222,20 +223,6 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
         if (!isfinite(t)) atomicOr(a.status, STATUS_NONFINITE);
         a.inv[b] = (float)(1.0 / (sqrt(t) + (double)a.eps));
         a.counter[b] = 0;
-    }
-}
-
-__global__ void __launch_bounds__(256)
-norm_finalize_kernel(const float* __restrict__ partials, int nparts, float eps,
-                     float* __restrict__ inv, int* status) {
-    __shared__ double red[8];
-    pdl_wait();
-    pdl_trigger();
-    const int b = blockIdx.x;
-    const double t = sum_partials_256(partials + (int64_t)b * nparts, nparts, red);
-    if (threadIdx.x == 0) {
-        if (!isfinite(t)) atomicOr(status, STATUS_NONFINITE);
-        inv[b] = (float)(1.0 / (sqrt(t) + (double)eps));
     }
 }
 
@@ -270,11 +257,6 @@ int prep_grid_parts(int m, int n, int batch) {
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
     dim3 grid(a.nparts, a.batch);
     return launch_pdl(prep_kernel, grid, dim3(PTHREADS), 0, s, a);
-}
-
-cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
-                                 float* inv, int* status, cudaStream_t s) {
-    return launch_pdl(norm_finalize_kernel, dim3(batch), dim3(256), 0, s, partials, nparts, eps, inv, status);
 }
 
 cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale, uint32_t seed,

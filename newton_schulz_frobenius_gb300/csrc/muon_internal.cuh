@@ -171,10 +171,6 @@ struct AdamArgs {
 };
 cudaError_t launch_adamw(const AdamArgs& a, int nchunks, cudaStream_t s);
 
-// inv[b] = 1 / (sqrt(sum(partials[b][:])) + eps); flags a non-finite sum.
-cudaError_t launch_norm_finalize(const float* partials, int nparts, int batch, float eps,
-                                 float* inv, int* status, cudaStream_t s);
-
 // Fills `count` elements of a workspace buffer with bounded pseudo-random values
 // (autotune input only; never touches caller data).
 cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale,
@@ -209,7 +205,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Kernel-class bookkeeping for launch counting and optional event timing.
 enum KernelClass : int {
-    KC_PREP = 0, KC_NORM = 1, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
+    KC_PREP = 0, KC_NORM = 1 /* no longer launched: prep finalises */, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
     KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_ADAMW = 9, KC_COUNT = 10
 };
 void note_launch_begin(int kclass, cudaStream_t s);
