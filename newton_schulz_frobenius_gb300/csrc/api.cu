@@ -730,11 +730,72 @@ static SmallWork small_work(const std::vector<int>& counts, const std::vector<do
     std::vector<std::vector<int>> lists((size_t)w.grid);
     std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<>> heap;
     for (int c = 0; c < w.grid; ++c) heap.push({0.0, c});
+    std::vector<double> load((size_t)w.grid, 0.0);
+    std::vector<std::vector<double>> lcost((size_t)w.grid);
     for (const auto& it : order) {
         auto top = heap.top();
         heap.pop();
         lists[(size_t)top.second].push_back(it.second);
+        lcost[(size_t)top.second].push_back(it.first);
+        load[(size_t)top.second] = top.first + it.first;
         heap.push({top.first + it.first, top.second});
+    }
+    // Improve the makespan: move one item out of the most loaded CTA, or swap
+    // it for a cheaper one of another CTA, while that lowers the maximum of
+    // the two loads below the current makespan (a few sweeps; LPT leaves the
+    // last CTAs one item over when the items are few and coarse).
+    const int sweeps = total <= 8 * w.grid ? 4 * w.grid : 0;   // fine-grained lists are near the bound already
+    for (int sweep = 0; sweep < sweeps; ++sweep) {
+        const size_t cm = (size_t)(std::max_element(load.begin(), load.end()) - load.begin());
+        const double top = load[cm];
+        double best = top;
+        size_t bi = 0, bc = 0, bj = 0;
+        bool bswap = false;
+        for (size_t i = 0; i < lists[cm].size(); ++i) {
+            const double ci = lcost[cm][i];
+            for (size_t c = 0; c < (size_t)w.grid; ++c) {
+                if (c == cm) continue;
+                const double mv = std::max(top - ci, load[c] + ci);
+                if (mv < best - 1e-12) { best = mv; bi = i; bc = c; bswap = false; }
+                for (size_t j = 0; j < lists[c].size(); ++j) {
+                    const double cj = lcost[c][j];
+                    if (cj >= ci) continue;
+                    const double sw = std::max(top - ci + cj, load[c] - cj + ci);
+                    if (sw < best - 1e-12) { best = sw; bi = i; bc = c; bj = j; bswap = true; }
+                }
+            }
+        }
+        if (best >= top - 1e-12) break;
+        const int item = lists[cm][bi];
+        const double ci = lcost[cm][bi];
+        lists[cm].erase(lists[cm].begin() + (long)bi);
+        lcost[cm].erase(lcost[cm].begin() + (long)bi);
+        load[cm] -= ci;
+        if (bswap) {
+            const int other = lists[bc][bj];
+            const double cj = lcost[bc][bj];
+            lists[bc][bj] = item;
+            lcost[bc][bj] = ci;
+            load[bc] += ci - cj;
+            lists[cm].push_back(other);
+            lcost[cm].push_back(cj);
+            load[cm] += cj;
+        } else {
+            lists[bc].push_back(item);
+            lcost[bc].push_back(ci);
+            load[bc] += ci;
+        }
+    }
+    // within a CTA, the costliest items first (the next one's inputs are
+    // prefetched while the current one runs)
+    for (int c = 0; c < w.grid; ++c) {
+        std::vector<size_t> idx(lists[(size_t)c].size());
+        for (size_t i = 0; i < idx.size(); ++i) idx[i] = i;
+        std::stable_sort(idx.begin(), idx.end(),
+                         [&](size_t x, size_t y) { return lcost[(size_t)c][x] > lcost[(size_t)c][y]; });
+        std::vector<int> l2;
+        for (size_t i : idx) l2.push_back(lists[(size_t)c][i]);
+        lists[(size_t)c] = l2;
     }
     w.ptr.assign((size_t)w.grid + 1, 0);
     for (int c = 0; c < w.grid; ++c) {
