@@ -228,6 +228,26 @@ __device__ __forceinline__ uint32_t stream_stages(const SmallArgs& a) {
     return min(3u, (uint32_t)STAGE_AREA / (PIECE * (2u + msz)));
 }
 
+// Piece p of matrix e (total elements; gradient then, for a Muon step,
+// momentum) as piece k of the launch: stage k % nst, its barrier expecting
+// the bytes.  Thread 0 only; the stage must be free.
+__device__ __forceinline__ void issue_piece(const SmallArgs& a, const MatEntry& e, int total, uint32_t k, int p,
+                                            const Stream& st) {
+    const bool step = (a.mode == 0);
+    const uint32_t msz = step ? (a.mom_dtype == MUON_F32 ? 4u : 2u) : 0u;
+    const uint32_t gbytes = PIECE * 2;
+    const uint32_t sbytes = gbytes + PIECE * msz;
+    const uint32_t s = k % st.nst;
+    const uint32_t bar = st.bars + 8 * s;
+    const uint32_t elems = (uint32_t)min(PIECE, total - p * PIECE);
+    mbar_expect_tx(bar, elems * (2 + msz));
+    bulk_g2s(st.stage + s * sbytes, reinterpret_cast<const __nv_bfloat16*>(e.grad) + (int64_t)p * PIECE, elems * 2,
+             bar);
+    if (step)
+        bulk_g2s(st.stage + s * sbytes + gbytes, reinterpret_cast<const char*>(e.mom) + (int64_t)p * PIECE * msz,
+                 elems * msz, bar);
+}
+
 // U of one matrix (momentum update when a.mode == 0) into X; returns this
 // thread's sum of squares of U.  Aligned inputs stream through the slot area
 // in pieces of 8192 elements on the bulk-copy engine (two or three pieces in
@@ -277,19 +297,7 @@ __device__ float prologue(const SmallArgs& a, const SmallBucket& bk, const MatEn
     const uint32_t nst = st.nst;
     const int npieces = (total + PIECE - 1) / PIECE;
     const uint32_t first = st.consumed;
-    auto issue = [&](int p) {
-        const uint32_t k = first + (uint32_t)p;
-        const uint32_t s = k % nst;
-        const uint32_t bar = st.bars + 8 * s;
-        const uint32_t elems = (uint32_t)min(PIECE, total - p * PIECE);
-        mbar_expect_tx(bar, elems * (2 + msz));
-        bulk_g2s(st.stage + s * sbytes, reinterpret_cast<const __nv_bfloat16*>(e.grad) + (int64_t)p * PIECE, elems * 2,
-                 bar);
-        if (step)
-            bulk_g2s(st.stage + s * sbytes + gbytes,
-                     reinterpret_cast<const char*>(e.mom) + (int64_t)p * PIECE * msz, elems * msz, bar);
-        st.issued = k + 1;
-    };
+    auto issue = [&](int p) { issue_piece(a, e, total, first + (uint32_t)p, p, st); };
     if (tid == 0) {
         fence_async_smem();         // earlier generic accesses of the stage area come first
         for (int p = 0; p < npieces && p < (int)nst; ++p) issue(p);
@@ -348,9 +356,12 @@ __device__ float prologue(const SmallArgs& a, const SmallBucket& bk, const MatEn
 // Output of one M-half of O: rows row0 .. row0+127 in TMEM lanes, columns in
 // TMEM [tl + c) for c < 64 nck, scaled by alpha; written to the caller as O
 // (mode 1) or applied to W (mode 0).  Blocks of 256 columns pass through
-// shared memory as fp32 (row pitch 1040 B) so that the caller's rows are read
-// and written whole by a warp, not one row per lane.
-constexpr int OPITCH = 256 * 4 + 16;
+// shared memory as fp32 so that the caller's rows are read and written whole
+// by a warp, not one row per lane.  The stage fills X exactly (128 rows of
+// 1024 B, not a byte past it): the 16-byte piece index of float column c of
+// row i is XOR-ed with i & 7, so eight lanes writing one column to eight rows
+// hit eight bank groups.
+__device__ __forceinline__ int so_off(int i, int c) { return i * 1024 + ((((c >> 2) ^ (i & 7)) << 4) | ((c & 3) << 2)); }
 
 __device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk, const MatEntry& e, uint8_t* stage,
                                        uint32_t tl, int row0, float alpha, int nck) {
@@ -366,18 +377,17 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk
         const int bc = min(256, nck * 64 - col0);
         // TMEM -> stage: this thread's row r, 32-column chunks [k0, k1) of the block
         const int per = bc / 64, k0 = hw * per, k1 = k0 + per;
-        float* srow = reinterpret_cast<float*>(stage + r * OPITCH);
         for (int k = k0; k < k1; k += 2) {
             float v0[32], v1[32];
             tmem_ld64(tl + col0 + 32 * k, tl + col0 + 32 * (k + 1), v0, v1);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<float4*>(srow + 32 * k + 4 * u) =
+                *reinterpret_cast<float4*>(stage + so_off(r, 32 * k + 4 * u)) =
                     make_float4(v0[4 * u] * alpha, v0[4 * u + 1] * alpha, v0[4 * u + 2] * alpha, v0[4 * u + 3] * alpha);
             if (k + 1 < k1) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<float4*>(srow + 32 * (k + 1) + 4 * u) = make_float4(
+                    *reinterpret_cast<float4*>(stage + so_off(r, 32 * (k + 1) + 4 * u)) = make_float4(
                         v1[4 * u] * alpha, v1[4 * u + 1] * alpha, v1[4 * u + 2] * alpha, v1[4 * u + 3] * alpha);
             }
         }
@@ -400,9 +410,8 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk
                     for (int t = 0; t < 16; ++t) {
                         const int i = warp + 8 * t, row = row0 + i;
                         if (row >= bk.m) continue;
-                        const float* so = reinterpret_cast<const float*>(stage + i * OPITCH) + c;
-                        const float4 o0 = *reinterpret_cast<const float4*>(so);
-                        const float4 o1 = *reinterpret_cast<const float4*>(so + 4);
+                        const float4 o0 = *reinterpret_cast<const float4*>(stage + so_off(i, c));
+                        const float4 o1 = *reinterpret_cast<const float4*>(stage + so_off(i, c + 4));
                         float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
                         if (upd) {
                             float wf[8];
@@ -415,9 +424,8 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk
                 } else {
                     for (int i = warp; i < 128 && row0 + i < bk.m; i += 8) {
                         const int64_t off = (int64_t)(row0 + i) * bk.n + col;
-                        const float* so = reinterpret_cast<const float*>(stage + i * OPITCH) + c;
                         for (int j = 0; j < 8 && col + j < bk.n; ++j) {
-                            float o = so[j];
+                            float o = *reinterpret_cast<const float*>(stage + so_off(i, c + j));
                             if (upd) {
                                 const float w = ld_elem(e.w, off + j, od);
                                 o = w - fmaf(lrwd, w, stepc * o);
@@ -436,7 +444,7 @@ __device__ __noinline__ void write_out(const SmallArgs& a, const SmallBucket& bk
                 for (int t = 0; t < 4; ++t) {
                     const int i = lane + 32 * t, row = row0 + i;
                     if (row >= bk.m) continue;
-                    float o = reinterpret_cast<const float*>(stage + i * OPITCH)[jj];
+                    float o = *reinterpret_cast<const float*>(stage + so_off(i, jj));
                     if (upd) {
                         const float w = ld_elem(e.w, rbase + row, od);
                         o = w - fmaf(lrwd, w, stepc * o);

@@ -272,3 +272,15 @@ def test_symmetric_products_both_forms(mg, monkeypatch, dense, path):
                                       9500, 0.02, steps=2):
         assert err <= TOL["bf16"] + q, (err, q)
         assert m_ok
+
+
+def test_fused_many_matrices_per_cta(mg, monkeypatch):
+    """More matrices than CTAs in one fused launch (both kernel forms): each
+    CTA runs several in turn through the same shared memory (the write-out
+    stage, the prologue's staged pieces, the slots); every matrix matches the
+    oracle."""
+    monkeypatch.setenv("MUON_SMALL", "1")
+    shapes = [(128, 512)] * 160 + [(256, 256)] * 160
+    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", mg.MUON_PATH_AUTO, True, 8800, 0.0316):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
