@@ -482,19 +482,8 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
         if (feeds_apply) { g.c_dtype = MUON_BF16; g.round_tf32 = 0; }
         else { g.c_dtype = MUON_F32; g.round_tf32 = 1; }
     };
-    // The Gram-space matrices as lower 256-blocks: when every product of the
-    // run is a 2-SM product on 256-wide tiles in a 16-bit type, the symmetric
-    // outputs skip their mirrored halves and every reader fetches those
-    // blocks transposed from the stored ones (MUON_LOWER=0: mirrored, full).
-    const char* pe = std::getenv("MUON_PAIR");
-    const char* le = std::getenv("MUON_LOWER");
-    const bool lower = !tf && is_half(dtype) && !plan.sym_dense && plan.sym_tile_n == 256 && plan.tile_n == 256 &&
-                       !(pe && pe[0] != '1') && !(le && le[0] == '0');
     auto sym = [&](const void* A, const void* Bm, void* C, bool feeds_apply) {
         GemmArgs g = gemm_base(sq_dtype, dc.status);
-        g.sym_lower_out = lower ? 1 : 0;
-        g.a_lower = lower ? 1 : 0;
-        g.b_lower = lower ? 1 : 0;
         g.A = A; g.lda = L.ldm; g.strideA = strideM;
         g.B = Bm; g.ldb = L.ldm; g.strideB = strideM;
         g.M = m; g.N = m; g.K = m; g.batch = B;
@@ -522,7 +511,6 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
             g.epi = EPI_STORE;
             g.C = G; g.ldc = L.ldm; g.strideC = strideM;
             g.tile_n = plan.sym_tile_n;
-            g.sym_lower_out = lower ? 1 : 0;
             gram_out(g, false);
             if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 1; }
             int r = run_gemm(dc, s, g, KC_SYRK);
@@ -573,7 +561,6 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
         g.B = X; g.ldb = L.ldx; g.strideB = strideX; g.b_kmajor = 0;
         g.M = m; g.N = n; g.K = m; g.batch = B;
         g.tile_n = plan.tile_n;
-        g.a_lower = lower ? 1 : 0;
         if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 0; }
         int kc = KC_APPLY;
         if (!last || fin.kind == EPI_STORE) {
@@ -1076,10 +1063,6 @@ static int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype
     *plan = make_plan(cfg.coeffs, cfg.steps, cfg.segments, path, tile_n, m, n, sym_tile_n, sym_dense);
     if (const char* f = std::getenv("MUON_SYM_DENSE")) {    // override for tests: 0 triangle, 1 all tiles
         if (f[0] == '0' || f[0] == '1') plan->sym_dense = f[0] - '0';
-    }
-    if (const char* f = std::getenv("MUON_SYM_TILE")) {     // override for tests: 128 or 256
-        const int t = std::atoi(f);
-        if (t == 128 || t == 256) plan->sym_tile_n = t;
     }
     // the fused small-matrix kernel: as measured, else whenever it applies
     const bool measured = have && ent.path == path;

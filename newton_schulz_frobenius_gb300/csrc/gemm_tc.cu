@@ -419,9 +419,8 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
     uint8_t* trn = stg + 2048;
 #pragma unroll
     for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(nrm + lane * 64 + 16 * u) = pack8_h(v + 8 * u, f16);
-    // lower-block output: every chunk as computed, nothing mirrored
-    const bool below = a.symmetric && !a.sym_lower_out && c0 < r0;
-    const bool diag = a.symmetric && !a.sym_lower_out && c0 == r0;
+    const bool below = a.symmetric && c0 < r0;
+    const bool diag = a.symmetric && c0 == r0;
     if (below || diag) {
         if (diag) __syncwarp();     // the mirrored entries replace the row stores' upper part
 #pragma unroll
@@ -451,8 +450,7 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmAt,
-               const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ GemmArgs args, const TileSched sched) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args, const TileSched sched) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
@@ -460,13 +458,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     constexpr int MM = PAIR ? 2 * BM : BM;      // rows of one product instruction
     const uint32_t IDESC = TF32 ? idesc_tf32(MM, BN) : idesc_f16kind(MM, BN, !B_KMAJOR, args.dtype == MUON_F16);
     constexpr int KE = TF32 ? 32 : 64;    // elements per 128-byte k-block
-    // Operands stored as their lower 256-blocks (a symmetric matrix whose
-    // blocks above the 256 x 256 diagonal blocks were never written): the
-    // k-block kb of an operand whose rows lie in 256-block r is read
-    // transposed from the stored block (kb, r) when it lies above the
-    // diagonal block.  Both CTAs of a pair share r, so they agree.
-    const bool LOWER_OK = PAIR && !TF32 && BN == 256;
-    auto upper = [&](int kb, int rblk) { return (kb * KE) >= (rblk + 1) * 256; };
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -548,23 +539,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, C::STAGE_BYTES);
-                    if (LOWER_OK && args.a_lower && upper(kb, tm >> 1)) {
-                        // A rows tm * 128 .. from the stored block below: MN-major, two 64-column boxes
-#pragma unroll
-                        for (int q = 0; q < 2; ++q)
-                            tma_load_3d(smem_u32(sA + stage * C::A_BYTES + q * (BK * 128)), &tmAt, fb,
-                                        tm * BM + q * 64, kb * KE, b);
-                    } else {
-                        tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
-                    }
+                    tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
                     if (PAIR) {
                         // this CTA's half of B: rows (K-major) or columns (MN-major) rank * BN / 2 ..
-                        if (B_KMAJOR && LOWER_OK && args.b_lower && upper(kb, tn)) {
-#pragma unroll
-                            for (int q = 0; q < 2; ++q)
-                                tma_load_3d(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmBt, fb,
-                                            tn * BN + rank * (BN / 2) + q * 64, kb * KE, b);
-                        } else if (B_KMAJOR) {
+                        if (B_KMAJOR) {
                             tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN + rank * (BN / 2),
                                         b);
                         } else {
@@ -634,8 +612,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-                int mb = 0, mtm = 0, mtn = 0;
-                if (LOWER_OK && (args.a_lower || args.b_lower)) sched.decode(t, mb, mtm, mtn, rank);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, args.status)) {
                         ok = false;
@@ -644,20 +620,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
                     const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
-                    const bool a_t = LOWER_OK && args.a_lower && upper(kb, mtm >> 1);
-                    const bool b_t = !B_KMAJOR || (LOWER_OK && args.b_lower && upper(kb, mtn));
-                    const uint32_t idesc = IDESC | (a_t ? (1u << 15) : 0u) | (b_t ? (1u << 16) : 0u);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // one instruction consumes 32 bytes of K (16 bf16 or 8 TF32)
-                        const uint64_t ad = a_t ? sdesc(a_base + kk * 2048, BK * 128, 1024)
-                                                : sdesc(a_base + kk * 32, 16, 1024);
-                        const uint64_t bd = b_t ? sdesc(b_base + kk * 2048, BK * 128, 1024)
-                                                : sdesc(b_base + kk * 32, 16, 1024);
+                        const uint64_t ad = sdesc(a_base + kk * 32, 16, 1024);
+                        const uint64_t bd = B_KMAJOR ? sdesc(b_base + kk * 32, 16, 1024)
+                                                     : sdesc(b_base + kk * 2048, BK * 128, 1024);
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
                         if (PAIR) {
                             if (TF32) tc_mma2_tf32(d, ad, bd, IDESC, accum);
-                            else tc_mma2_bf16(d, ad, bd, idesc, accum);
+                            else tc_mma2_bf16(d, ad, bd, IDESC, accum);
                         } else {
                             if (TF32) tc_mma_tf32(d, ad, bd, IDESC, accum);
                             else tc_mma_bf16(d, ad, bd, IDESC, accum);
@@ -732,7 +704,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int ch = ch_beg; ch < ch_end; ++ch) {
                 const int col0 = tn * BN + ch * 32;
                 if (col0 >= args.N) break;
-                if (args.symmetric && !args.sym_lower_out && col0 > warp_row_max) continue;
+                if (args.symmetric && col0 > warp_row_max) continue;
                 if (loads && ch + 1 < ch_end)      // next chunk's loads fly while this one is processed
                     epi_load_chunk<32>(args, ent, b, row0 + lane, col0 + 32, gnxt);
                 float v[32];
@@ -876,23 +848,6 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
             ga.tma_c = 1;
     }
 
-    // lower-block operands: the same matrices as 64 x 64 boxes for transposed reads;
-    // lower-block output only through the tile stores of 2-SM 256-wide tiles
-    CUtensorMap mAt, mBt;
-    std::memset(&mAt, 0, sizeof mAt);
-    std::memset(&mBt, 0, sizeof mBt);
-    constexpr bool LOWER_OK = PAIR && !TF32 && BN == 256;
-    if (a.a_lower || a.b_lower) {
-        if (!LOWER_OK || a.M != a.K || (a.b_lower && (!B_KMAJOR || a.N != a.K))) return cudaErrorInvalidValue;
-        if (a.a_lower && !make_map(&mAt, a.A, a.dtype, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch,
-                                   (uint64_t)a.lda, (uint64_t)a.strideA, 64, 64))
-            return cudaErrorInvalidValue;
-        if (a.b_lower && !make_map(&mBt, a.B, a.dtype, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
-                                   (uint64_t)a.ldb, (uint64_t)a.strideB, 64, 64))
-            return cudaErrorInvalidValue;
-    }
-    if (!(LOWER_OK && ga.tma_c && a.symmetric)) ga.sym_lower_out = 0;     // full storage serves every reader
-
     TileSched sc;
     sc.tiles_m = (a.M + BM - 1) / BM;
     sc.tiles_n = (a.N + BN - 1) / BN;
@@ -911,7 +866,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     sc.total = sc.per_batch * a.batch;
     if (!PAIR) {
         const int grid = sc.total < num_sms ? sc.total : num_sms;
-        return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, mC, mAt, mBt, ga, sc);
+        return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, mC, ga, sc);
     }
     int clusters = std::min(num_sms / 2, max_clusters);
     if (sc.total < clusters) clusters = sc.total;
@@ -929,7 +884,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mAt, mBt, ga, sc);
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, ga, sc);
 }
 
 }  // namespace tc

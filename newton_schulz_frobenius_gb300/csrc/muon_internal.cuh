@@ -74,12 +74,6 @@ struct GemmArgs {
     int tile_n;             // tensor-core tile N extent (128 or 256)
     int pair;               // tile_n 256 as 2-SM products on 2-CTA clusters: 0 off, otherwise on
     int tma_c;              // set by the launcher: 16-bit workspace output written by tile stores
-    // Symmetric Gram-space matrices as lower 256-blocks (2-SM 256-wide tiles
-    // only): the output's tiles stored as computed, nothing mirrored (the
-    // blocks above the diagonal 256 x 256 blocks stay unwritten); operands in
-    // that form read those blocks transposed from the stored ones.
-    int sym_lower_out;
-    int a_lower, b_lower;
     int* status;            // device status word
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd
 };

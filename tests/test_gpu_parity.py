@@ -284,21 +284,3 @@ def test_fused_many_matrices_per_cta(mg, monkeypatch):
     for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", mg.MUON_PATH_AUTO, True, 8800, 0.0316):
         assert err <= TOL["bf16"] + q, (err, q)
         assert m_ok
-
-
-@pytest.mark.parametrize("lower", ["0", "1"])
-@pytest.mark.parametrize("path", ["plain", "gram"])
-def test_gram_space_lower_blocks(mg, monkeypatch, path, lower):
-    """Gram-space matrices stored as lower 256-blocks (the symmetric products
-    store their tiles as computed and mirror nothing; their readers fetch the
-    blocks above the diagonal 256-blocks transposed) or mirrored in full: both
-    match the oracle, on shapes with several pair rows, ragged edges and a
-    transposed caller matrix."""
-    monkeypatch.setenv("MUON_SMALL", "0")
-    monkeypatch.setenv("MUON_SYM_TILE", "256")
-    monkeypatch.setenv("MUON_LOWER", lower)
-    code = mg.MUON_PATH_PLAIN if path == "plain" else mg.MUON_PATH_GRAM
-    shapes = [(768, 1536), (1000, 1280), (1536, 600), (520, 520)]
-    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", code, True, 9700, 0.02, steps=2):
-        assert err <= TOL["bf16"] + q, (err, q)
-        assert m_ok
