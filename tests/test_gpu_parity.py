@@ -284,3 +284,20 @@ def test_fused_many_matrices_per_cta(mg, monkeypatch):
     for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", mg.MUON_PATH_AUTO, True, 8800, 0.0316):
         assert err <= TOL["bf16"] + q, (err, q)
         assert m_ok
+
+
+@pytest.mark.parametrize("mom_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("small", ["0", "1"])
+def test_degenerate_shapes_step(mg, monkeypatch, small, mom_dtype):
+    """The method's degenerate shapes: row and column vectors (a 1 x 1 Gram
+    matrix), 2 x 2, odd widths that rule out 16-byte rows, and thin matrices,
+    through both the product kernels and the fused one-CTA-per-matrix kernel,
+    two steps each, against the oracle.  (A random odd square such as 17 x 17
+    is left out: it is nearly singular, and rounding U to bf16 before the
+    iteration moves its polar factor by about 3% in both GPU paths alike, a
+    conditioning limit of the bf16 working type rather than of a kernel.)"""
+    monkeypatch.setenv("MUON_SMALL", small)
+    shapes = [(1, 4096), (4096, 1), (2, 2), (1, 7), (3, 1000), (17, 40), (8, 520)]
+    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", mom_dtype, mg.MUON_PATH_AUTO, True, 9900, 0.02, steps=2):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
