@@ -180,6 +180,8 @@ def bench_reference(args):
         return 0
     if args.workload == ADAMW_WORKLOAD:
         return bench_reference_adamw(args)
+    if args.workload == PACK_WORKLOAD:
+        return bench_reference_pack(args)
     from oracle import muon_oracle as orc
     from workloads import WORKLOADS, gen_matrix, zeros_matrix
     wl = WORKLOADS[args.workload]
@@ -321,6 +323,159 @@ def bench_reference_adamw(args):
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"AdamW over {n} bf16 parameters per step (numpy fp64)"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+PACK_WORKLOAD = "pack_7b_bf16"
+PACK_RANKS = 8
+
+
+def _pack_setup():
+    """The 7B stack's 224 bf16 gradient matrices, owners for PACK_RANKS ranks
+    by the owner planner, and the packed layout (16-byte starts)."""
+    from workloads import WORKLOADS
+    wl = WORKLOADS["stack_32L_7b_bf16_f32mom"]
+    shapes = [(r, c) for _, r, c in wl.matrices()]
+    return shapes
+
+
+def pack_cpu_baseline(shapes, offsets, max_seconds=20.0):
+    """The packing oracle (numpy) on the host cores, on a bounded sample: the
+    first matrices of the layout, about 256 M elements per pass."""
+    import numpy as np
+    from oracle import pack_oracle as po
+    take, n = [], 0
+    for i, (m, c) in enumerate(shapes):
+        if n + m * c > (1 << 28):
+            break
+        take.append(i)
+        n += m * c
+    mats = [np.zeros((shapes[i][0], shapes[i][1]), np.uint16) + np.uint16(i) for i in take]
+    base = min(offsets[i] for i in take)
+    end = max(offsets[i] + mats[k].size for k, i in enumerate(take))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        po.pack(mats, [offsets[i] - base for i in take], end - base)
+        done += 1
+        el = time.perf_counter() - t0
+        if el * (done + 1) / done > max_seconds or done >= 5:
+            break
+    return {"value": 4.0 * n * done / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} pack(s) of the first {len(take)} matrices ({n} bf16 elements, read + write "
+                      f"4 bytes per element) with the numpy packing oracle", "seconds": el}
+
+
+def bench_reference_pack(args):
+    """--impl reference for the pack workload: the numpy packing oracle on the
+    bounded sample, one pack per step.  The layout is the oracle's, with
+    owners round-robin (the owner choice moves the bytes, not their number)."""
+    from oracle import pack_oracle as po
+    shapes = _pack_setup()
+    owners = [i % PACK_RANKS for i in range(len(shapes))]
+    offsets, seg = po.layout(shapes, owners, PACK_RANKS, 8)
+    cb = pack_cpu_baseline(shapes, offsets, max_seconds=5.0 * max(1, args.steps))
+    value = cb["value"]
+    line = {"impl": "reference", "metric": "packed exchange buffers: pack + unpack of the gradients (GB/s)",
+            "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * cb["seconds"] / max(1, args.steps), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": PACK_WORKLOAD, "matrices": len(shapes), "ranks": PACK_RANKS},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_pack(args):
+    """Packed exchange buffers for an 8-rank owner-centric step of the 7B
+    stack: all 224 bf16 gradient matrices into the packed layout and back out,
+    one launch each way.  HBM-bound: algorithmic bytes per element = 2 B read
+    + 2 B written per direction = 8 B per step."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as mg
+    shapes = _pack_setup()
+    owners, _, _, _ = mg.muon_owner_plan(shapes, PACK_RANKS)
+    offsets, seg = mg.muon_pack_plan(shapes, owners, PACK_RANKS, 8)
+    g = torch.Generator(device="cuda").manual_seed(777)
+    mats = [torch.randn(s, generator=g, device="cuda").to(torch.bfloat16) for s in shapes]
+    packed = torch.empty(PACK_RANKS * seg, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    elems = sum(m * n for m, n in shapes)
+    nbytes = 8.0 * elems
+
+    def step():
+        mg.muon_pack(mats, offsets, packed, to_packed=True)
+        mg.muon_pack(mats, offsets, packed, to_packed=False)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(0)
+    clk.start()
+    n0 = mg.muon_launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    launches = mg.muon_launch_count() - n0
+    clocks = clk.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+
+    mg.muon_kernel_timing_read()
+    mg.muon_set_kernel_timing(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    mg.muon_set_kernel_timing(False)
+    kl, kms, work = mg.muon_kernel_timing_read()["pack"]
+    achieved = work / (kms * 1e-3) / 1e9
+
+    # end to end: one rank's owned gradients H2D from pinned host, the two
+    # launches, the same matrices D2H to pinned host
+    mine = [i for i in range(len(shapes)) if owners[i] == 0]
+    host = [mats[i].cpu().pin_memory() for i in mine]
+    back = [torch.empty_like(h).pin_memory() for h in host]
+    e2e_steps = max(3, min(args.steps, 10))
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        eev[i][0].record()
+        for k, j in enumerate(mine):
+            mats[j].copy_(host[k], non_blocking=True)
+        step()
+        for k, j in enumerate(mine):
+            back[k].copy_(mats[j], non_blocking=True)
+        eev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
+    hbytes = sum(h.numel() * h.element_size() for h in host)
+
+    peaks = _peaks()
+    line = {"metric": "packed exchange buffers: pack + unpack of the gradients (GB/s)",
+            "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic: seeded torch device RNG",
+            "config": {"workload": PACK_WORKLOAD, "matrices": len(shapes), "elements": elems, "ranks": PACK_RANKS,
+                       "segment_elements": seg, "bytes_per_element": 8,
+                       "l2": "flushed between timed steps (256 MiB device write outside the step events)"},
+            "roofline": {"kernel": "pack_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None, "launches": kl,
+                         "peak_source": f"{peaks['source']} hbm_gbs"},
+            "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": hbytes,
+                    "d2h_bytes_per_step": hbytes, "ms_per_step": e2e_ms,
+                    "what": "rank 0's owned gradients H2D from pinned host, pack + unpack, the same D2H"},
+            "gpu_launches": launches,
+            "clocks": clocks}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in pack_cpu_baseline(shapes, offsets).items() if k != "seconds"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -625,6 +780,8 @@ def main():
         return bench_reference(args)
     if args.workload == ADAMW_WORKLOAD:
         return bench_adamw(args)
+    if args.workload == PACK_WORKLOAD:
+        return bench_pack(args)
     return bench_gpu(args)
 
 

@@ -258,6 +258,36 @@ int muon_adamw_step(void* const* params, const void* const* grads, void* const* 
 int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, int ranks,
                     int* owner_out, double* load_out, double* makespan_out, int* measured_out);
 
+/*
+ * Packed exchange layout ("DMuon" summary, section 2.1: gradients are reduced
+ * into owner-contiguous buffers before the orthogonalisation and the updated
+ * parameters are published from them afterwards).  One buffer of
+ * ranks x seg elements: rank r's segment [r seg, (r+1) seg) holds the matrices
+ * it owns (owner[i], e.g. from muon_owner_plan) in ascending index, each
+ * starting on a multiple of align_elems within the segment (pass 8 for
+ * 16-byte starts of 16-bit elements); every segment is padded to the longest,
+ * so that one reduce-scatter of the buffer hands each owner its summed
+ * gradients and one all-gather hands every rank the owners' updated
+ * parameters.  Host-only and deterministic (every rank computes the same
+ * layout); each matrix at most 2^31 elements.
+ *   offset_out    count entries: element offset of matrix i in the buffer
+ *   seg_elems_out the segment length in elements
+ */
+int muon_pack_plan(const int64_t* ms, const int64_t* ns, const int* owner, int64_t count, int ranks,
+                   int64_t align_elems, int64_t* offset_out, int64_t* seg_elems_out);
+
+/*
+ * Moves `count` row-major device matrices (mats[i], ms[i] x ns[i] elements of
+ * dtype) to (to_packed != 0) or from (to_packed == 0) a packed device buffer,
+ * matrix i at element offset offsets[i] (from muon_pack_plan), in one launch
+ * on `stream`.  Elements between the matrices are neither read nor written.
+ * The caller owns every buffer; regions must not overlap.  16-byte vector
+ * copies where a matrix pointer, the buffer and offsets[i] * element size are
+ * all 16-byte aligned, element copies otherwise.
+ */
+int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns, const int64_t* offsets,
+              int64_t count, int dtype, void* packed, int to_packed, void* stream);
+
 /* ---- diagnostics (not part of the method) ---------------------------------- */
 
 /* Total kernels this library has launched in this process. */

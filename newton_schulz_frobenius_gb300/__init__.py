@@ -40,6 +40,7 @@ EXPORTS = (
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
     "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan", "muon_adamw_step",
+    "muon_pack_plan", "muon_pack",
 )
 
 _lib = None
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         "muon_owner_plan": (i32, [i64p, i64p, i64, i32, i32, ip, dp, dp, ip]),
         "muon_adamw_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   i64p, i64, i32, i32, f32, f32, f32, f32, f32, i64, vp]),
+        "muon_pack_plan": (i32, [i64p, i64p, ip, i64, i32, i64, i64p, i64p]),
+        "muon_pack": (i32, [ctypes.POINTER(vp), i64p, i64p, i64p, i64, i32, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -367,6 +370,47 @@ def muon_owner_plan(shapes, ranks: int, dtype: int = MUON_BF16):
     _check(lib().muon_owner_plan(I64(*[s[0] for s in shapes]), I64(*[s[1] for s in shapes]), k, dtype, ranks,
                                  owners, loads, ctypes.byref(mk), ctypes.byref(meas)), "muon_owner_plan")
     return list(owners)[:k], list(loads)[:ranks], mk.value, bool(meas.value)
+
+
+def muon_pack_plan(shapes, owners, ranks: int, align_elems: int = 8):
+    """Packed exchange layout: (element offset per matrix, segment length);
+    rank r's owned matrices fill segment [r seg, (r+1) seg)."""
+    shapes, owners = list(shapes), list(owners)
+    k = len(shapes)
+    if len(owners) != k:
+        raise ValueError("one owner per matrix")
+    I64 = ctypes.c_int64 * max(1, k)
+    off = I64()
+    seg = ctypes.c_int64()
+    _check(lib().muon_pack_plan(I64(*[s[0] for s in shapes]), I64(*[s[1] for s in shapes]),
+                                (ctypes.c_int * max(1, k))(*owners), k, int(ranks), int(align_elems), off,
+                                ctypes.byref(seg)), "muon_pack_plan")
+    return list(off)[:k], seg.value
+
+
+def muon_pack(mats, offsets, packed, to_packed: bool = True, stream=None):
+    """Copies CUDA matrices into (to_packed) or out of a packed CUDA buffer of
+    the same dtype, matrix i at element offset offsets[i]."""
+    k = len(mats)
+    if len(offsets) != k:
+        raise ValueError("one offset per matrix")
+    if k == 0:
+        return
+    dt = _dtype_code(packed)
+    _cuda_contig(packed, "packed")
+    for i, t in enumerate(mats):
+        _cuda_contig(t, f"matrix {i}")
+        if _dtype_code(t) != dt:
+            raise TypeError(f"matrix {i}: dtype differs from the packed buffer")
+        if offsets[i] < 0 or offsets[i] + t.numel() > packed.numel():
+            raise ValueError(f"matrix {i} does not fit the packed buffer at offset {offsets[i]}")
+    shp = [(t.shape[0], t.numel() // t.shape[0]) if t.dim() >= 1 and t.shape[0] > 0 else (1, t.numel())
+           for t in mats]
+    VP = ctypes.c_void_p * k
+    I64 = ctypes.c_int64 * k
+    _check(lib().muon_pack(VP(*[t.data_ptr() for t in mats]), I64(*[s[0] for s in shp]), I64(*[s[1] for s in shp]),
+                           I64(*offsets), k, dt, packed.data_ptr(), 1 if to_packed else 0, _stream_ptr(stream)),
+           "muon_pack")
 
 
 def muon_adamw_step(params, grads, exp_avgs, exp_avg_sqs, lr: float, beta1: float = 0.9, beta2: float = 0.999,

@@ -252,7 +252,7 @@ static thread_local int t_open = -1;   // index of the launch being recorded
 static const char* kclass_name(int k) {
     static const char* names[KC_COUNT] = {"prep_momentum_norm", "norm_finalize", "gemm_tc_syrk",
                                           "gemm_tc_square", "gemm_tc_apply", "gemm_tc_apply_update",
-                                          "gemm_fp32", "other", "small_ns_fused", "adamw"};
+                                          "gemm_fp32", "other", "small_ns_fused", "adamw", "pack"};
     return (k >= 0 && k < KC_COUNT) ? names[k] : "other";
 }
 
@@ -2084,6 +2084,85 @@ extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t cou
         for (int rk = 0; rk < ranks; ++rk) load_out[rk] = load[(size_t)rk];
     if (makespan_out) *makespan_out = mk;
     if (measured_out) *measured_out = measured ? 1 : 0;
+    return MUON_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Packed exchange buffers ("DMuon" summary, sections 2.1 and 2.3): each rank's
+// owned matrices contiguous in one segment, segments of equal length so that
+// one reduce-scatter (gradients to their owners) or all-gather (updated
+// parameters from their owners) moves the whole buffer.
+// ---------------------------------------------------------------------------
+
+extern "C" int muon_pack_plan(const int64_t* ms, const int64_t* ns, const int* owner, int64_t count, int ranks,
+                              int64_t align_elems, int64_t* offset_out, int64_t* seg_elems_out) {
+    if (count < 0 || ranks < 1 || align_elems < 1) return fail(MUON_EINVAL, "count < 0, ranks < 1 or align < 1");
+    if (!seg_elems_out || (count > 0 && (!ms || !ns || !owner || !offset_out)))
+        return fail(MUON_EINVAL, "NULL array argument");
+    for (int64_t i = 0; i < count; ++i) {
+        if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "matrix %lld has a zero side", (long long)i);
+        if (owner[i] < 0 || owner[i] >= ranks) return fail(MUON_EINVAL, "owner of matrix %lld out of range", (long long)i);
+        if (ms[i] > ((int64_t)1 << 31) / ns[i]) return fail(MUON_EINVAL, "matrix %lld above 2^31 elements", (long long)i);
+    }
+    auto up = [&](int64_t x) { return (x + align_elems - 1) / align_elems * align_elems; };
+    std::vector<int64_t> cur((size_t)ranks, 0);
+    for (int64_t i = 0; i < count; ++i) {       // ascending index within each rank
+        int64_t& c = cur[(size_t)owner[i]];
+        offset_out[i] = up(c);
+        c = offset_out[i] + ms[i] * ns[i];
+    }
+    int64_t seg = 0;
+    for (int64_t c : cur) seg = std::max(seg, up(c));
+    for (int64_t i = 0; i < count; ++i) offset_out[i] += (int64_t)owner[i] * seg;
+    *seg_elems_out = seg;
+    return MUON_OK;
+}
+
+extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns, const int64_t* offsets,
+                         int64_t count, int dtype, void* packed, int to_packed, void* stream) {
+    if (count < 0) return fail(MUON_EINVAL, "count < 0");
+    if (count == 0) return MUON_OK;
+    if (!mats || !ms || !ns || !offsets || !packed) return fail(MUON_EINVAL, "NULL argument");
+    if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    const int es = (int)esize(dtype);
+    const bool pk16 = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
+    std::vector<PackMat> pm((size_t)count);
+    std::vector<PackChunk> chunks;
+    for (int64_t i = 0; i < count; ++i) {
+        if (!mats[i]) return fail(MUON_EINVAL, "NULL matrix pointer at %lld", (long long)i);
+        if (ms[i] < 1 || ns[i] < 1 || offsets[i] < 0) return fail(MUON_EINVAL, "bad size or offset at %lld", (long long)i);
+        const int64_t numel = ms[i] * ns[i];
+        const bool v = pk16 && (reinterpret_cast<uintptr_t>(mats[i]) & 15) == 0 && (offsets[i] * es) % 16 == 0;
+        pm[(size_t)i] = PackMat{mats[i], offsets[i], v ? 1 : 0, 0};
+        for (int64_t s0 = 0; s0 < numel; s0 += PACK_CHUNK_ELEMS)
+            chunks.push_back(PackChunk{s0, (int)i, (int)std::min<int64_t>(PACK_CHUNK_ELEMS, numel - s0)});
+    }
+    if (chunks.size() > (size_t)INT32_MAX) return fail(MUON_EINVAL, "too many elements");
+    int r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tb = align_up(sizeof(PackMat) * pm.size(), 256);
+    const size_t cb = align_up(sizeof(PackChunk) * chunks.size(), 256);
+    Workspace* w = nullptr;
+    if ((r = ws_get(dc.device, s, tb + cb, &w))) return r;
+    static_assert(256 % sizeof(MatEntry) == 0, "ring rows tile 256 bytes");
+    std::vector<MatEntry> rows((tb + cb) / sizeof(MatEntry));
+    std::memcpy(rows.data(), pm.data(), sizeof(PackMat) * pm.size());
+    std::memcpy(reinterpret_cast<char*>(rows.data()) + tb, chunks.data(), sizeof(PackChunk) * chunks.size());
+    if ((r = upload_table(*w, rows, reinterpret_cast<MatEntry*>(w->base), s))) return r;
+    PackArgs a;
+    a.mats = reinterpret_cast<const PackMat*>(w->base);
+    a.chunks = reinterpret_cast<const PackChunk*>(w->base + tb);
+    a.packed = packed;
+    a.esize = es;
+    a.to_packed = to_packed ? 1 : 0;
+    double bytes = 0;
+    for (int64_t i = 0; i < count; ++i) bytes += 2.0 * (double)(ms[i] * ns[i]) * es;
+    note_launch_begin(KC_PACK, s);
+    cudaError_t e = launch_pack(a, (int)chunks.size(), s);
+    note_launch_end(KC_PACK, bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return MUON_OK;
 }
 

@@ -171,6 +171,30 @@ struct AdamArgs {
 };
 cudaError_t launch_adamw(const AdamArgs& a, int nchunks, cudaStream_t s);
 
+// Packed exchange buffers (see pack.cu): chunk k moves elements
+// [start, start + len) of matrix `mat` between the caller's storage and the
+// packed buffer at element offset mats[mat].off + start.
+constexpr int PACK_CHUNK_ELEMS = 32768;
+struct PackMat {
+    void* p;                // caller storage, row-major
+    int64_t off;            // element offset in the packed buffer
+    int vec_ok;             // both sides 16-byte aligned at every chunk start
+    int pad;
+};
+struct PackChunk {
+    int64_t start;
+    int mat;
+    int len;
+};
+struct PackArgs {
+    const PackMat* mats;
+    const PackChunk* chunks;
+    void* packed;
+    int esize;              // bytes per element
+    int to_packed;          // 1: matrices -> packed buffer, 0: packed buffer -> matrices
+};
+cudaError_t launch_pack(const PackArgs& a, int nchunks, cudaStream_t s);
+
 // Fills `count` elements of a workspace buffer with bounded pseudo-random values
 // (autotune input only; never touches caller data).
 cudaError_t launch_fill_synthetic(void* X, int64_t count, int dtype, float scale,
@@ -206,7 +230,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Kernel-class bookkeeping for launch counting and optional event timing.
 enum KernelClass : int {
     KC_PREP = 0, KC_NORM = 1 /* no longer launched: prep finalises */, KC_SYRK = 2, KC_SQUARE = 3, KC_APPLY = 4,
-    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_ADAMW = 9, KC_COUNT = 10
+    KC_APPLY_UPDATE = 5, KC_SIMT = 6, KC_OTHER = 7, KC_SMALL = 8, KC_ADAMW = 9, KC_PACK = 10, KC_COUNT = 11
 };
 void note_launch_begin(int kclass, cudaStream_t s);
 void note_launch_end(int kclass, double work, cudaStream_t s);

@@ -1,0 +1,133 @@
+"""The packed exchange layout (host-only, so it runs without a GPU): each
+owner's matrices contiguous in its segment, segments of equal length, and a
+two-rank gloo exchange over buffers in that layout hands every owner the sum
+of its matrices' gradients (all-reduce, then each rank reads its segment:
+what one reduce-scatter of the buffer delivers)."""
+import os
+import socket
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist          # noqa: E402
+import torch.multiprocessing as mp        # noqa: E402
+
+SHAPES = [(2048, 2048), (1024, 4096), (7, 13), (4096, 1), (128, 512), (3, 3), (640, 200), (1, 9)]
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_frobenius_gb300 as pkg
+    return pkg
+
+
+@pytest.mark.parametrize("ranks,align", [(1, 8), (2, 8), (3, 1), (4, 32), (8, 8)])
+def test_layout_invariants(mg, ranks, align):
+    owners, _, _, _ = mg.muon_owner_plan(SHAPES, ranks)
+    off, seg = mg.muon_pack_plan(SHAPES, owners, ranks, align)
+    assert seg % align == 0
+    sizes = [m * n for m, n in SHAPES]
+    for r in range(ranks):
+        mine = [i for i in range(len(SHAPES)) if owners[i] == r]
+        # ascending index, aligned, inside the segment, disjoint and in order
+        prev_end = r * seg
+        for i in mine:
+            assert (off[i] - r * seg) % align == 0
+            assert off[i] >= prev_end and off[i] + sizes[i] <= (r + 1) * seg
+            prev_end = off[i] + sizes[i]
+    # the longest segment is tight: its last matrix ends within align of it
+    longest = max((max((off[i] + sizes[i] - owners[i] * seg for i in range(len(SHAPES)) if owners[i] == r),
+                       default=0)) for r in range(ranks))
+    assert seg - longest < align
+    # deterministic
+    assert mg.muon_pack_plan(SHAPES, owners, ranks, align) == (off, seg)
+
+
+def test_layout_rejects_bad_arguments(mg):
+    with pytest.raises(mg.MuonError):
+        mg.muon_pack_plan([(4, 4)], [2], 2)          # owner out of range
+    with pytest.raises(mg.MuonError):
+        mg.muon_pack_plan([(0, 4)], [0], 1)          # zero side
+    with pytest.raises(mg.MuonError):
+        mg.muon_pack_plan([(4, 4)], [0], 0)          # no ranks
+    with pytest.raises(mg.MuonError):
+        mg.muon_pack_plan([(4, 4)], [0], 1, 0)       # alignment
+    assert mg.muon_pack_plan([], [], 3) == ([], 0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import newton_schulz_frobenius_gb300 as mg
+    shapes = SHAPES[2:]                       # small enough for CPU buffers
+    owners, _, _, _ = mg.muon_owner_plan(shapes, world)
+    off, seg = mg.muon_pack_plan(shapes, owners, world, 8)
+    # this rank's gradients (a rank-dependent seed), packed by the layout
+    g = torch.Generator().manual_seed(100 + rank)
+    grads = [torch.randn(m * n, generator=g, dtype=torch.float64) for m, n in shapes]
+    buf = torch.zeros(world * seg, dtype=torch.float64)
+    for i, t in enumerate(grads):
+        buf[off[i]:off[i] + t.numel()] = t
+    dist.all_reduce(buf)
+    mine = buf[rank * seg:(rank + 1) * seg].clone()
+    out[rank] = (owners, off, seg, mine.numpy().tolist())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_exchange_over_the_layout():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
+    shapes = SHAPES[2:]
+    owners, off, seg, _ = out[0]
+    assert out[1][:3] == (owners, off, seg)       # both ranks computed the same layout
+    # regenerate each rank's gradients and sum them per matrix
+    per_rank = []
+    for r in range(2):
+        g = torch.Generator().manual_seed(100 + r)
+        per_rank.append([torch.randn(m * n, generator=g, dtype=torch.float64) for m, n in shapes])
+    for r in range(2):
+        mine = np.array(out[r][3])
+        for i in range(len(shapes)):
+            if owners[i] != r:
+                continue
+            lo = off[i] - r * seg
+            np.testing.assert_array_equal(mine[lo:lo + shapes[i][0] * shapes[i][1]],
+                                          (per_rank[0][i] + per_rank[1][i]).numpy())
+
+
+@pytest.mark.parametrize("ranks,align", [(1, 1), (2, 8), (3, 4), (8, 32)])
+def test_layout_matches_oracle(mg, ranks, align):
+    """The library's planner against the oracle's plain restatement of the
+    layout, on owners from the owner planner and on a skewed hand-made
+    assignment (every matrix on the last rank but one)."""
+    from oracle import pack_oracle as po
+    owners, _, _, _ = mg.muon_owner_plan(SHAPES, ranks)
+    assert mg.muon_pack_plan(SHAPES, owners, ranks, align) == tuple(po.layout(SHAPES, owners, ranks, align))
+    skew = [ranks - 1] * len(SHAPES)
+    skew[0] = 0
+    assert mg.muon_pack_plan(SHAPES, skew, ranks, align) == tuple(po.layout(SHAPES, skew, ranks, align))
+
+
+def test_oracle_pack_places_every_element():
+    from oracle import pack_oracle as po
+    shapes, owners = [(2, 3), (1, 5), (3, 1)], [1, 0, 1]
+    off, seg = po.layout(shapes, owners, 2, 4)
+    # rank 0: matrix 1 at 0, ends at 5 (8 with alignment); rank 1: matrix 0 at 0,
+    # ends at 6, matrix 2 at 8, ends at 11 (12): segments of 12
+    assert (off, seg) == ([12, 0, 20], 12)
+    mats = [np.arange(m * n, dtype=np.float64).reshape(m, n) + 10 * i for i, (m, n) in enumerate(shapes)]
+    buf = po.pack(mats, off, 2 * seg, fill=-1)
+    for a, o in zip(mats, off):
+        np.testing.assert_array_equal(buf[o:o + a.size], a.reshape(-1))
+    assert (buf == -1).sum() == 2 * seg - sum(a.size for a in mats)
