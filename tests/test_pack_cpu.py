@@ -131,3 +131,57 @@ def test_oracle_pack_places_every_element():
     for a, o in zip(mats, off):
         np.testing.assert_array_equal(buf[o:o + a.size], a.reshape(-1))
     assert (buf == -1).sum() == 2 * seg - sum(a.size for a in mats)
+
+
+def _owner_step_worker(rank, world, port, out):
+    """One owner-centric Muon step over CPU ranks: gradients summed into the
+    packed layout, each owner updating its matrices (the fp64 oracle stands in
+    for the per-owner GPU update), updated parameters published through the
+    same layout."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import newton_schulz_frobenius_gb300 as mg
+    from oracle import muon_oracle as orc
+    shapes = [(16, 48), (40, 24), (8, 8), (24, 72)]
+    owners, _, _, _ = mg.muon_owner_plan(shapes, world, mg.MUON_F32)
+    off, seg = mg.muon_pack_plan(shapes, owners, world, 4)
+    W = [np.random.default_rng(7 + i).standard_normal(s).astype(np.float32) * 0.02 for i, s in enumerate(shapes)]
+    G = [np.random.default_rng(100 * rank + i).standard_normal(s).astype(np.float32) * 0.01
+         for i, s in enumerate(shapes)]
+    # 1. gradients summed into their owners' segments (one reduction of the buffer)
+    gbuf = torch.zeros(world * seg, dtype=torch.float32)
+    for i, g in enumerate(G):
+        gbuf[off[i]:off[i] + g.size] = torch.from_numpy(g.reshape(-1))
+    dist.all_reduce(gbuf)
+    # 2. each owner updates its matrices; 3. published through the same layout
+    pbuf = torch.zeros(world * seg, dtype=torch.float32)
+    for i, (m, n) in enumerate(shapes):
+        if owners[i] != rank:
+            continue
+        gsum = gbuf[off[i]:off[i] + m * n].numpy().reshape(m, n)
+        r = orc.muon_step(W[i], np.zeros((m, n), np.float32), gsum, lr=0.02, beta=0.95, wd=0.1, nesterov=False,
+                          path="gram" if m != n else "plain", param_dtype="f32", mom_dtype="f32")
+        pbuf[off[i]:off[i] + m * n] = torch.from_numpy(np.asarray(r["W_new"], np.float32).reshape(-1))
+    dist.all_reduce(pbuf)                     # every segment filled by its owner alone
+    out[rank] = [pbuf[off[i]:off[i] + m * n].numpy().reshape(m, n).tolist() for i, (m, n) in enumerate(shapes)]
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_owner_centric_step_over_two_ranks():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    world = 2
+    mp.start_processes(_owner_step_worker, args=(world, _free_port(), out), nprocs=world, join=True,
+                       start_method="spawn")
+    from oracle import muon_oracle as orc
+    shapes = [(16, 48), (40, 24), (8, 8), (24, 72)]
+    for i, (m, n) in enumerate(shapes):
+        a, b = np.array(out[0][i]), np.array(out[1][i])
+        np.testing.assert_array_equal(a, b)             # every rank holds the same parameters
+        W = np.random.default_rng(7 + i).standard_normal((m, n)).astype(np.float32) * 0.02
+        gsum = sum(np.random.default_rng(100 * r + i).standard_normal((m, n)).astype(np.float32) * 0.01
+                   for r in range(world)).astype(np.float32)
+        ref = orc.muon_step(W, np.zeros((m, n), np.float32), gsum, lr=0.02, beta=0.95, wd=0.1, nesterov=False,
+                            path="gram" if m != n else "plain", param_dtype="f32", mom_dtype="f32")
+        np.testing.assert_array_equal(a, np.asarray(ref["W_new"], np.float32))
