@@ -163,6 +163,35 @@ __device__ __forceinline__ void load_row_run(const void* base, int64_t off, floa
     }
 }
 
+// A tall caller matrix (stored n x m, oriented (r, c) at c m + r) is read and
+// written a caller row per lane: the warp's 32 x 32 chunk (rows r0.., columns
+// c0..) is handled in its transpose, lane j owning caller row c0 + j, elements
+// r0 .. r0+31, as 64 contiguous bytes.  Only for whole chunks whose rows start
+// on 16 bytes (the condition is the same for every lane of the warp).
+__device__ __forceinline__ bool trans_vec_chunk(const GemmArgs& a, const MatEntry& e, int r0, int c0) {
+    const int es = a.out_dtype == MUON_F32 ? 4 : 2;
+    return e.trans && r0 + 32 <= a.M && c0 + 32 <= a.N && ((int64_t)a.M * es) % 16 == 0 &&
+           (reinterpret_cast<uintptr_t>(e.w) & 15) == 0;
+}
+
+// In-register transpose of a warp's 32 x 32 tile (lane i holds row i on entry,
+// column i on return): five rounds of exchanges with the lane whose index
+// differs in bit k, swapping the k-wide blocks that are out of place.
+__device__ __forceinline__ void warp_transpose32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool up = (lane & k) != 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j & k) continue;
+            const float x = __shfl_xor_sync(0xffffffffu, up ? v[j] : v[j + k], k);
+            if (up) v[j] = x;
+            else v[j + k] = x;
+        }
+    }
+}
+
 // Loads, for one thread's row r and columns c0 .. c0+W-1, the values the
 // epilogue will combine with the product: G for EPI_POLY, the caller's W for
 // EPI_UPDATE (nothing otherwise).  Split from epi_row_chunk so a caller can
@@ -191,6 +220,10 @@ __device__ __forceinline__ void epi_load_chunk(const GemmArgs& a, const MatEntry
 #pragma unroll
                 for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(e.w, off + j, od) : 0.f;
             }
+        } else if (W == 32 && trans_vec_chunk(a, e, r - (threadIdx.x & 31), c0)) {
+            // transposed chunk: this lane's caller row c0 + lane, elements r0 .. r0+31
+            const int lane = threadIdx.x & 31;
+            load_row_run<W>(e.w, (int64_t)(c0 + lane) * a.M + (r - lane), g, od);
         } else {
 #pragma unroll
             for (int j = 0; j < W; ++j) g[j] = (j < nvalid) ? ld_elem(e.w, (int64_t)(c0 + j) * a.M + r, od) : 0.f;
@@ -247,6 +280,20 @@ __device__ __forceinline__ void epi_row_chunk(const GemmArgs& a, const MatEntry&
     const float wd = a.hyper ? a.hyper[2] : a.wd;
     const float lrwd = lr * wd;
     const float step = lr * a.scale;
+    if constexpr (W == 32) {
+        if (trans_vec_chunk(a, e, r - (threadIdx.x & 31), c0)) {
+            // tall caller matrix, whole chunk: transposed in registers, then one
+            // caller row per lane (g was loaded in that layout by epi_load_chunk)
+            const int lane = threadIdx.x & 31;
+            warp_transpose32(v);
+            if (a.epi == EPI_UPDATE) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = g[j] - fmaf(lrwd, g[j], step * v[j]);
+            }
+            store_row_run<32>(e.w, (int64_t)(c0 + lane) * a.M + (r - lane), v, od);
+            return;
+        }
+    }
     if (a.epi == EPI_UPDATE) {
         // W - (lr wd W + step O): the decrement is formed first and subtracted
         // once, so an fp32-rounded factor (1 - lr wd) never scales every W
