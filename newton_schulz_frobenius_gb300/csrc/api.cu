@@ -1,5 +1,5 @@
 // Host runtime of the Muon update library: argument validation, per-device
-// state, workspace, shape bucketing, the Newton-Schulz driver (plain and Gram
+// state, workspace, shape bucketing, the Newton-Schulz orchestration (plain and Gram
 // with segment restarts), the measured-cost autotune with its persistent cache,
 // and the C ABI declared in include/muon.h.
 //
@@ -320,7 +320,7 @@ static int validate_segments(int steps, const int* segs, int nseg) {
 }
 
 // A resolved NS plan: the segment lengths actually run.  The plain path is
-// the Gram driver with unit segments (per step: XX^T, P = aI + bA + cA^2,
+// the Gram orchestration with unit segments (per step: XX^T, P = aI + bA + cA^2,
 // X <- P X), which performs the plain algorithm's products one for one.
 struct NsPlan {
     float a, b, c;
