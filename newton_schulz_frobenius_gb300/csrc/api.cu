@@ -10,6 +10,8 @@
 // section 3.2.
 #include "muon_internal.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -28,6 +30,28 @@
 #include <vector>
 
 namespace muon {
+
+// NVTX ranges around the host steps (a step, a bucket, its prologue and NS
+// run, the fused small-matrix launches): free when no tool is attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Device allocations of the library's own storage (workspaces, counters,
+// groups) go through here.  MUON_FAIL_ALLOC=1 makes every one of them fail, so
+// that the allocation-failure paths can be exercised without exhausting a GPU.
+static cudaError_t dev_alloc(void** p, size_t bytes) {
+    const char* f = std::getenv("MUON_FAIL_ALLOC");
+    if (f && f[0] == '1') {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
 
 // ---------------------------------------------------------------------------
 // logging and errors
@@ -160,7 +184,7 @@ static int ws_get(int dev, cudaStream_t s, size_t need, Workspace** out) {
             w.bytes = 0;
         }
         size_t want = align_up(need + need / 4, 1 << 20);
-        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&w.base), want);
+        cudaError_t e = dev_alloc(reinterpret_cast<void**>(&w.base), want);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(MUON_ENOMEM, "workspace allocation of %zu bytes failed: %s", want, cudaGetErrorString(e));
@@ -186,7 +210,7 @@ static int prep_counters(int dev, cudaStream_t s, int B, int** out) {
             w.pcnt_cap = 0;
         }
         const int cap = std::max(B, 4096);
-        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&w.pcnt), (size_t)cap * sizeof(int));
+        cudaError_t e = dev_alloc(reinterpret_cast<void**>(&w.pcnt), (size_t)cap * sizeof(int));
         if (e != cudaSuccess) {
             cudaGetLastError();
             w.pcnt = nullptr;
@@ -463,6 +487,9 @@ struct FinalEpi {
 // TF32 tensor path, with the transform applied to X rounded to bf16.
 static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
                   int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin) {
+    char nvname[64];
+    std::snprintf(nvname, sizeof nvname, "ns %dx%d x%d", m, n, B);
+    NvtxRange nvr(nvname);
     char* X = base + L.off_X;
     char* Xn = base + L.off_X2;
     char* G = base + L.off_G;
@@ -584,6 +611,9 @@ static int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayou
 static int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
                     const MatEntry* d_mats, int in_dtype, int mom_dtype, int x_dtype, bool with_mom, int nesterov,
                     float beta, bool vec_ok, int* cnt, const float* hyper = nullptr) {
+    char nvname[64];
+    std::snprintf(nvname, sizeof nvname, "prep %dx%d x%d", m, n, B);
+    NvtxRange nvr(nvname);
     PrepArgs p;
     std::memset(&p, 0, sizeof p);
     p.mats = d_mats;
@@ -819,6 +849,7 @@ static double plan_alg_flops(const NsPlan& p, int m, int n) {
 }
 
 static int run_small(const DevCtx& dc, cudaStream_t s, const SmallArgs& a, double alg_flops) {
+    NvtxRange nvr("fused small-matrix launch");
     note_launch_begin(KC_SMALL, s);
     cudaError_t e = launch_small_ns(a, dc.sms, s);
     note_launch_end(KC_SMALL, alg_flops, s);
@@ -1156,6 +1187,7 @@ int muon_set_ns_precision(int dtype) {
 
 int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype, const float coeffs[3],
                           int steps, const int* segments, int num_segments, void* stream) {
+    muon::NvtxRange nvr("muon_ns_orthogonalize");
     if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
     if (m < 1 || n < 1 || batch < 1) return fail(MUON_EINVAL, "m, n, batch must be >= 1");
     if (m > (1 << 20) || n > (1 << 20)) return fail(MUON_EINVAL, "matrix side above 2^20");
@@ -1238,6 +1270,7 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
 int muon_step(void* const* params, const void* const* grads, void* const* moms, const int64_t* ms,
               const int64_t* ns, int64_t count, int param_dtype, int mom_dtype, float lr, float beta, float wd,
               int nesterov, void* stream) {
+    muon::NvtxRange nvr("muon_step");
     if (count < 0) return fail(MUON_EINVAL, "count < 0");
     if (count == 0) return MUON_OK;
     if (!params || !grads || !moms || !ms || !ns) return fail(MUON_EINVAL, "NULL array argument");
@@ -1774,6 +1807,7 @@ struct muon_group {
 namespace muon {
 
 static int group_enqueue(muon_group* g, cudaStream_t s) {
+    NvtxRange nvr("muon_group_step");
     int r;
     for (const auto& f : g->fused) {
         const SmallArgs sa = fused_args(f, g->d_work, g->plans, g->keys, g->bucket_size, g->vec_ok,
@@ -1845,7 +1879,7 @@ static int group_plan(muon_group* g, cudaStream_t s) {
         if (g->ws) cudaFree(g->ws);
         g->ws = nullptr;
         g->ws_bytes = 0;
-        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&g->ws), need);
+        cudaError_t e = dev_alloc(reinterpret_cast<void**>(&g->ws), need);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(MUON_ENOMEM, "group workspace of %zu bytes: %s", need, cudaGetErrorString(e));
