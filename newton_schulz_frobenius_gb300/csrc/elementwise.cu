@@ -196,7 +196,7 @@ prep_kernel(const __grid_constant__ PrepArgs a) {
     float ss = 0.f;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) prep_tile(a, e, b, t, beta, nesterov, tile, ss);
 
-    // Block sum of squares -> one partial per tile.
+    // Block sum of squares -> one partial per CTA.
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
