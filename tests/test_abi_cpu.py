@@ -38,6 +38,23 @@ def test_library_exports_every_declared_symbol(mg):
         assert hasattr(L, name), name
 
 
+def test_plain_c_caller(mg, tmp_path):
+    """The header compiles as strict C99 and a C program linked against the
+    library runs its host-only entry points (tests/c_abi_host.c)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(mg.LIB_PATH)
+    exe = str(tmp_path / "c_abi_host")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_host.c"),
+                    "-L", libdir, "-lmuon_gb300", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout + r.stderr
+
+
 def test_no_fallback_when_library_missing(monkeypatch):
     import newton_schulz_frobenius_gb300 as pkg
     monkeypatch.setattr(pkg, "_lib", None)
