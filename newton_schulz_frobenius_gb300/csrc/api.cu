@@ -2158,6 +2158,7 @@ extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns
     if (count == 0) return MUON_OK;
     if (!mats || !ms || !ns || !offsets || !packed) return fail(MUON_EINVAL, "NULL argument");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if (count > INT32_MAX) return fail(MUON_EINVAL, "more than 2^31 - 1 matrices");
     const int es = (int)esize(dtype);
     const bool pk16 = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
     std::vector<PackMat> pm((size_t)count);
@@ -2165,6 +2166,8 @@ extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns
     for (int64_t i = 0; i < count; ++i) {
         if (!mats[i]) return fail(MUON_EINVAL, "NULL matrix pointer at %lld", (long long)i);
         if (ms[i] < 1 || ns[i] < 1 || offsets[i] < 0) return fail(MUON_EINVAL, "bad size or offset at %lld", (long long)i);
+        if (ms[i] > (INT64_MAX / 16) / ns[i] || offsets[i] > INT64_MAX / 16 - ms[i] * ns[i])
+            return fail(MUON_EINVAL, "matrix %lld: size or offset overflows the byte range", (long long)i);
         const int64_t numel = ms[i] * ns[i];
         const bool v = pk16 && (reinterpret_cast<uintptr_t>(mats[i]) & 15) == 0 && (offsets[i] * es) % 16 == 0;
         pm[(size_t)i] = PackMat{mats[i], offsets[i], v ? 1 : 0, 0};

@@ -58,6 +58,24 @@ def test_layout_rejects_bad_arguments(mg):
     assert mg.muon_pack_plan([], [], 3) == ([], 0)
 
 
+def test_pack_rejects_overflowing_sizes(mg):
+    """Sizes whose byte range overflows int64 are rejected before any device
+    use.  The matrix and buffer pointers are placeholders, so this runs only
+    where no CUDA device is present: a validation bug then fails with a
+    missing-device status instead of reaching a kernel."""
+    import ctypes
+    if torch.cuda.is_available():
+        pytest.skip("placeholder pointers: host-only check")
+    L = mg.lib()
+    fake = ctypes.c_void_p(4096)
+    big = (1 << 62)
+    for m, n, off in ((big, 4, 0), (1 << 31, 1 << 31, 0), (4, 4, (1 << 63) - 8)):
+        r = L.muon_pack((ctypes.c_void_p * 1)(fake), (ctypes.c_int64 * 1)(m), (ctypes.c_int64 * 1)(n),
+                        (ctypes.c_int64 * 1)(off), 1, mg.MUON_BF16, fake, 1, None)
+        assert r == mg.MUON_EINVAL, (m, n, off, r)
+        assert "overflow" in mg.last_error_message()
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
