@@ -28,7 +28,8 @@
  *   - Host-detectable errors return a negative muon_status and enqueue nothing.
  *     Device-detected errors (non-finite norm, a bounded wait that gave up) are
  *     recorded in a per-device status word read by muon_sync_status().
- *   - No C++ exception crosses the ABI; no call aborts the process.
+ *   - No C++ exception crosses the ABI; no call aborts the process.  A failed
+ *     host allocation (tables sized by the arguments) returns MUON_ENOMEM.
  *   - The library keeps a workspace per (device, stream) that only grows; the
  *     first call of a new shape set may allocate and therefore must not be made
  *     while the stream is being captured into a CUDA graph.
@@ -80,7 +81,8 @@ typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muo
  *              these segment lengths (each >= 1, sum == steps): per segment
  *              G = XX^T, then P = aI + bG + cG^2, Q <- P (first) or PQ,
  *              G <- PGP (not after the last), then X <- QX.
- * Returns MUON_EINVAL for NULL ptr, m/n/batch < 1, steps < 1 or bad segments.
+ * Returns MUON_EINVAL for NULL ptr, m/n/batch < 1, a side above 2^20, a batch
+ * above 2^31 - 1 or whose byte range overflows, steps < 1 or bad segments.
  */
 int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype,
                           const float coeffs[3], int steps, const int* segments,

@@ -22,6 +22,9 @@
 #include <fstream>
 #include <functional>
 #include <map>
+#include <memory>
+#include <new>
+#include <stdexcept>
 #include <mutex>
 #include <queue>
 #include <sstream>
@@ -99,6 +102,15 @@ static int fail(int status, const char* fmt, ...) {
 static int cuda_fail(cudaError_t e, const char* what) {
     return fail(MUON_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+// Host containers sized by the caller's arguments can fail to allocate; every
+// entry point that builds them ends in these handlers, so that no C++
+// exception crosses the C boundary.
+#define MUON_CATCH_ALL                                                                        \
+    catch (const std::bad_alloc&) { return fail(MUON_ENOMEM, "host allocation failed"); }      \
+    catch (const std::length_error&) { return fail(MUON_ENOMEM, "host allocation too large"); } \
+    catch (const std::exception& ex_) { return fail(MUON_EINVAL, "internal error: %s", ex_.what()); } \
+    catch (...) { return fail(MUON_EINVAL, "internal error"); }
 
 #define MUON_CUDA(call)                                   \
     do {                                                  \
@@ -1160,7 +1172,7 @@ const char* muon_status_str(int status) {
 
 const char* muon_last_error_message(void) { return t_last_error.c_str(); }
 
-int muon_set_ns_config(const float coeffs[3], int steps, const int* segments, int num_segments, int path) {
+int muon_set_ns_config(const float coeffs[3], int steps, const int* segments, int num_segments, int path) try {
     int r = validate_segments(steps, segments, num_segments);
     if (r) return r;
     if (path != MUON_PATH_AUTO && path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM)
@@ -1174,7 +1186,7 @@ int muon_set_ns_config(const float coeffs[3], int steps, const int* segments, in
     g_cfg.path = path;
     g_cfg_version.fetch_add(1);
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 int muon_set_ns_precision(int dtype) {
     if (dtype != -1 && dtype != MUON_BF16 && dtype != MUON_F16)
@@ -1186,11 +1198,13 @@ int muon_set_ns_precision(int dtype) {
 }
 
 int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype, const float coeffs[3],
-                          int steps, const int* segments, int num_segments, void* stream) {
+                          int steps, const int* segments, int num_segments, void* stream) try {
     muon::NvtxRange nvr("muon_ns_orthogonalize");
     if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
     if (m < 1 || n < 1 || batch < 1) return fail(MUON_EINVAL, "m, n, batch must be >= 1");
     if (m > (1 << 20) || n > (1 << 20)) return fail(MUON_EINVAL, "matrix side above 2^20");
+    if (batch > INT32_MAX || batch > (INT64_MAX / 8) / (m * n))
+        return fail(MUON_EINVAL, "batch x m x n overflows the byte range");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
     if (!coeffs || !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
         return fail(MUON_EINVAL, "coeffs missing or non-finite");
@@ -1265,11 +1279,11 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
         g_last_path[{om, on, dtype}] = path;
     }
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 int muon_step(void* const* params, const void* const* grads, void* const* moms, const int64_t* ms,
               const int64_t* ns, int64_t count, int param_dtype, int mom_dtype, float lr, float beta, float wd,
-              int nesterov, void* stream) {
+              int nesterov, void* stream) try {
     muon::NvtxRange nvr("muon_step");
     if (count < 0) return fail(MUON_EINVAL, "count < 0");
     if (count == 0) return MUON_OK;
@@ -1398,9 +1412,9 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
         g_last_path[{m, n, param_dtype}] = plans[k].path;
     }
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
-int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream) {
+int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream) try {
     if (count < 0 || (count > 0 && (!ms || !ns))) return fail(MUON_EINVAL, "bad shape arrays");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
     int r;
@@ -1428,15 +1442,15 @@ int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype
     if (const char* p = std::getenv("MUON_TUNE_CACHE")) save_tune_file(p);
     g_cfg_version.fetch_add(1);
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
-int muon_tune_save(const char* path) {
+int muon_tune_save(const char* path) try {
     if (!path) return fail(MUON_EINVAL, "path is NULL");
     int r = save_tune_file(path);
     return r < 0 ? r : MUON_OK;
-}
+} MUON_CATCH_ALL
 
-int muon_tune_load(const char* path) {
+int muon_tune_load(const char* path) try {
     if (!path) return fail(MUON_EINVAL, "path is NULL");
     std::ifstream f(path);
     if (!f) return 0;
@@ -1477,7 +1491,7 @@ int muon_tune_load(const char* path) {
         }
     }
     return loaded;
-}
+} MUON_CATCH_ALL
 
 int muon_last_path(int64_t m, int64_t n, int dtype, int* path_out) {
     if (!path_out) return fail(MUON_EINVAL, "path_out is NULL");
@@ -1555,7 +1569,7 @@ int muon_set_kernel_timing(int enable) {
     return MUON_OK;
 }
 
-int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms, double* work, int max_classes) {
+int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms, double* work, int max_classes) try {
     if (max_classes < 0) return fail(MUON_EINVAL, "max_classes < 0");
     std::vector<TimedLaunch> recs;
     {
@@ -1591,11 +1605,11 @@ int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms, do
         if (work) work[k] = work_acc[k];
     }
     return n;
-}
+} MUON_CATCH_ALL
 
 int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t batch,
                     int dtype, int b_kmajor, int symmetric, int poly, float alpha, float pa, float pb, float pc,
-                    int tile_n, void* stream) {
+                    int tile_n, void* stream) try {
     if (!A || !B || !C) return fail(MUON_EINVAL, "NULL operand");
     if (M < 1 || N < 1 || K < 1 || batch < 1) return fail(MUON_EINVAL, "bad sizes");
     if (M > (1 << 20) || N > (1 << 20) || K > (1 << 20)) return fail(MUON_EINVAL, "size above 2^20");
@@ -1628,7 +1642,7 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
         g.pa = pa; g.pb = pb; g.pc = pc;
     }
     return run_gemm(dc, reinterpret_cast<cudaStream_t>(stream), g, KC_OTHER);
-}
+} MUON_CATCH_ALL
 
 }  // extern "C"
 
@@ -1713,7 +1727,7 @@ __global__ void noalloc_table_kernel(MatEntry* t, char* base, int64_t stride_byt
 
 extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype,
                                              const float coeffs[3], int steps, const int* segments,
-                                             int num_segments, void* stream) {
+                                             int num_segments, void* stream) try {
     if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
     if (m < 1 || n < 1 || batch < 1) return fail(MUON_EINVAL, "m, n, batch must be >= 1");
     if (m > (1 << 20) || n > (1 << 20) || batch > 65535) return fail(MUON_EINVAL, "size out of range");
@@ -1763,7 +1777,7 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
         return r;
     FinalEpi fin{EPI_OUT, d_table, dtype, 0.f, 0.f, 0.f};
     return run_ns(dc, s, cbase, L, om, on, (int)batch, nsd, plan, x_holds_u(nsd), fin);
-}
+} MUON_CATCH_ALL
 
 // ---------------------------------------------------------------------------
 // Persistent groups: a fixed set of matrices stepped many times (the optimizer
@@ -1913,7 +1927,7 @@ static int group_plan(muon_group* g, cudaStream_t s) {
 extern "C" {
 
 int muon_group_create(void* const* params, const void* const* grads, void* const* moms, const int64_t* ms,
-                      const int64_t* ns, int64_t count, int param_dtype, int mom_dtype, muon_group** out) {
+                      const int64_t* ns, int64_t count, int param_dtype, int mom_dtype, muon_group** out) try {
     if (!out) return fail(MUON_EINVAL, "out is NULL");
     *out = nullptr;
     if (count < 1) return fail(MUON_EINVAL, "a group needs at least one matrix");
@@ -1931,6 +1945,8 @@ int muon_group_create(void* const* params, const void* const* grads, void* const
     if ((r = get_dev(dc))) return r;
     muon_group* g = new (std::nothrow) muon_group();
     if (!g) return fail(MUON_ENOMEM, "group allocation");
+    // released to the caller on success; destroyed on every early return or throw
+    std::unique_ptr<muon_group, int (*)(muon_group*)> holder(g, muon_group_destroy);
     g->device = dc.device;
     g->dc = dc;
     g->count = count;
@@ -1959,15 +1975,12 @@ int muon_group_create(void* const* params, const void* const* grads, void* const
         e = cudaMallocHost(reinterpret_cast<void**>(&g->h_hyper[i]), 4 * sizeof(float));
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->hev[i], cudaEventDisableTiming);
     }
-    if (e != cudaSuccess) {
-        muon_group_destroy(g);
-        return cuda_fail(e, "group stream/event/pinned setup");
-    }
-    *out = g;
+    if (e != cudaSuccess) return cuda_fail(e, "group stream/event/pinned setup");
+    *out = holder.release();
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
-int muon_group_step(muon_group* g, float lr, float beta, float wd, int nesterov, void* stream) {
+int muon_group_step(muon_group* g, float lr, float beta, float wd, int nesterov, void* stream) try {
     if (!g) return fail(MUON_EINVAL, "group is NULL");
     if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(wd))
         return fail(MUON_EINVAL, "non-finite hyper-parameter");
@@ -2028,7 +2041,7 @@ done:
             g_last_path[{g->keys[k].first, g->keys[k].second, g->param_dtype}] = g->plans[k].path;
     }
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 int muon_group_destroy(muon_group* g) {
     if (!g) return MUON_OK;
@@ -2061,7 +2074,7 @@ int muon_group_destroy(muon_group* g) {
 // ---------------------------------------------------------------------------
 
 extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, int ranks,
-                               int* owner_out, double* load_out, double* makespan_out, int* measured_out) {
+                               int* owner_out, double* load_out, double* makespan_out, int* measured_out) try {
     if (count < 0 || ranks < 1) return fail(MUON_EINVAL, "count < 0 or ranks < 1");
     if (count > 0 && (!ms || !ns || !owner_out)) return fail(MUON_EINVAL, "NULL array argument");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
@@ -2119,7 +2132,7 @@ extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t cou
     if (makespan_out) *makespan_out = mk;
     if (measured_out) *measured_out = measured ? 1 : 0;
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 // ---------------------------------------------------------------------------
 // Packed exchange buffers ("DMuon" summary, sections 2.1 and 2.3): each rank's
@@ -2129,7 +2142,7 @@ extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t cou
 // ---------------------------------------------------------------------------
 
 extern "C" int muon_pack_plan(const int64_t* ms, const int64_t* ns, const int* owner, int64_t count, int ranks,
-                              int64_t align_elems, int64_t* offset_out, int64_t* seg_elems_out) {
+                              int64_t align_elems, int64_t* offset_out, int64_t* seg_elems_out) try {
     if (count < 0 || ranks < 1 || align_elems < 1) return fail(MUON_EINVAL, "count < 0, ranks < 1 or align < 1");
     if (!seg_elems_out || (count > 0 && (!ms || !ns || !owner || !offset_out)))
         return fail(MUON_EINVAL, "NULL array argument");
@@ -2150,10 +2163,10 @@ extern "C" int muon_pack_plan(const int64_t* ms, const int64_t* ns, const int* o
     for (int64_t i = 0; i < count; ++i) offset_out[i] += (int64_t)owner[i] * seg;
     *seg_elems_out = seg;
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns, const int64_t* offsets,
-                         int64_t count, int dtype, void* packed, int to_packed, void* stream) {
+                         int64_t count, int dtype, void* packed, int to_packed, void* stream) try {
     if (count < 0) return fail(MUON_EINVAL, "count < 0");
     if (count == 0) return MUON_OK;
     if (!mats || !ms || !ns || !offsets || !packed) return fail(MUON_EINVAL, "NULL argument");
@@ -2201,7 +2214,7 @@ extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns
     note_launch_end(KC_PACK, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return MUON_OK;
-}
+} MUON_CATCH_ALL
 
 // ---------------------------------------------------------------------------
 // AdamW for the non-matrix parameters ("MuonX" page, section 2)
@@ -2210,7 +2223,7 @@ extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns
 extern "C" int muon_adamw_step(void* const* params, const void* const* grads, void* const* exp_avg,
                                void* const* exp_avg_sq, const int64_t* numels, int64_t count, int param_dtype,
                                int state_dtype, float lr, float beta1, float beta2, float eps, float wd,
-                               int64_t step, void* stream) {
+                               int64_t step, void* stream) try {
     if (count < 0) return fail(MUON_EINVAL, "count < 0");
     if (count == 0) return MUON_OK;
     if (!params || !grads || !exp_avg || !exp_avg_sq || !numels) return fail(MUON_EINVAL, "NULL array argument");
@@ -2267,4 +2280,4 @@ extern "C" int muon_adamw_step(void* const* params, const void* const* grads, vo
     note_launch_end(KC_ADAMW, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "adamw launch");
     return MUON_OK;
-}
+} MUON_CATCH_ALL

@@ -132,6 +132,10 @@ def test_step_and_orthogonalize_validation_before_any_device_use(mg):
     assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 5, c, 5, segs, 3, None) == mg.MUON_EDTYPE
     assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 1, c, 4, segs, 3, None) == mg.MUON_EINVAL
     assert L.muon_ns_orthogonalize(0x1000, 4, 8, 1, 1, None, 5, segs, 3, None) == mg.MUON_EINVAL
+    # a batch whose byte range overflows, or beyond the matrix table's index range
+    assert L.muon_ns_orthogonalize(0x1000, 1 << 20, 1 << 20, 1 << 21, 1, c, 5, segs, 3, None) == mg.MUON_EINVAL
+    assert "overflows" in mg.last_error_message()
+    assert L.muon_ns_orthogonalize(0x1000, 1, 1, 1 << 31, 1, c, 5, segs, 3, None) == mg.MUON_EINVAL
 
 
 def test_debug_gemm_validation(mg):
