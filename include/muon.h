@@ -33,6 +33,10 @@
  *   - The library keeps a workspace per (device, stream) that only grows; the
  *     first call of a new shape set may allocate and therefore must not be made
  *     while the stream is being captured into a CUDA graph.
+ *   - Host threads may call the library concurrently on different streams.
+ *     Calls on one stream from several host threads must be serialised by the
+ *     caller (a growing workspace is freed once the stream drains, while
+ *     another thread's call on that stream may still be using it).
  *   - There is no CPU fallback: every step runs in the library's CUDA kernels.
  */
 #ifndef MUON_GB300_H
