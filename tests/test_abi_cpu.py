@@ -23,7 +23,8 @@ def mg():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    with open(os.path.join(ROOT, "include", "muon.h")) as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(muon_[a-z0-9_]+)\s*\(", src)))
 

@@ -428,7 +428,8 @@ def test_f16_rounding_matches_ieee():
     x = np.concatenate([
         rng.standard_normal(200000) * np.exp2(rng.uniform(-30, 17, 200000)),
         (rng.integers(-2048, 2048, 20000) + 0.5) * np.exp2(rng.integers(-24, 5, 20000)).astype(np.float64)])
-    want = x.astype(np.float16).astype(np.float64)
+    with np.errstate(over="ignore"):                                # values past 65520 become inf
+        want = x.astype(np.float16).astype(np.float64)
     got = r(x)
     same = (got == want) | (np.isinf(got) & np.isinf(want) & (np.sign(got) == np.sign(want)))
     assert same.all(), x[~same][:5]
