@@ -255,7 +255,8 @@ int muon_adamw_step(void* const* params, const void* const* grads, void* const* 
  * picks without measurements (*measured_out = 0).  Greedy longest-processing-
  * time first, the pages' fallback to their MILP: matrices in decreasing cost
  * (stable in index), each to the least-loaded rank (ties to the lower rank).
- * Host-only and deterministic, so every rank computes the same plan.
+ * Host-only and deterministic, so every rank computes the same plan.  Sides
+ * must lie in [1, 2^20] (the limit of muon_step), else MUON_EINVAL.
  *   owner_out     count entries (required when count > 0)
  *   load_out      ranks entries or NULL: predicted cost per rank
  *   makespan_out  NULL or the largest per-rank cost

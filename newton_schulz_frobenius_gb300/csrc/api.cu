@@ -1478,6 +1478,7 @@ int muon_tune_load(const char* path) try {
             if (sym_dense != 0 && sym_dense != 1) continue;
             if (fused != 0 && fused != 1) continue;
             if (sym_tile != 128 && sym_tile != 256) continue;
+            if (!std::isfinite(ms) || ms < 0.0) continue;     // costs feed the owner planner's sort
             if (cols[0] != dc.name || sms != dc.sms || cuv != cv) continue;          // stale: other device/runtime
             if (m < 1 || n < m || !valid_dtype(dt)) continue;
             if (path != MUON_PATH_PLAIN && path != MUON_PATH_GRAM) continue;
@@ -2078,8 +2079,10 @@ extern "C" int muon_owner_plan(const int64_t* ms, const int64_t* ns, int64_t cou
     if (count < 0 || ranks < 1) return fail(MUON_EINVAL, "count < 0 or ranks < 1");
     if (count > 0 && (!ms || !ns || !owner_out)) return fail(MUON_EINVAL, "NULL array argument");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
-    for (int64_t i = 0; i < count; ++i)
+    for (int64_t i = 0; i < count; ++i) {
         if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "matrix %lld has a zero side", (long long)i);
+        if (ms[i] > (1 << 20) || ns[i] > (1 << 20)) return fail(MUON_EINVAL, "matrix %lld: side above 2^20", (long long)i);
+    }
     NsConfig cfg;
     {
         std::lock_guard<std::mutex> lk(g_mu);

@@ -83,6 +83,10 @@ def test_degenerate_inputs(mg):
     assert owners == [0]
     with pytest.raises(mg.MuonError):
         mg.muon_owner_plan([(10, 10)], 0)
+    with pytest.raises(mg.MuonError):
+        mg.muon_owner_plan([(10, (1 << 20) + 1)], 2)      # beyond the library's side limit
+    owners, _, _, _ = mg.muon_owner_plan([(1 << 20, 1 << 20)], 2)
+    assert owners == [0]
 
 
 def _free_port():
