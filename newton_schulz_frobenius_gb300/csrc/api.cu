@@ -2177,20 +2177,25 @@ extern "C" int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns
     if (count > INT32_MAX) return fail(MUON_EINVAL, "more than 2^31 - 1 matrices");
     const int es = (int)esize(dtype);
     const bool pk16 = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
-    std::vector<PackMat> pm((size_t)count);
-    std::vector<PackChunk> chunks;
+    int64_t nchunks = 0;                        // checked before any table is built
     for (int64_t i = 0; i < count; ++i) {
         if (!mats[i]) return fail(MUON_EINVAL, "NULL matrix pointer at %lld", (long long)i);
         if (ms[i] < 1 || ns[i] < 1 || offsets[i] < 0) return fail(MUON_EINVAL, "bad size or offset at %lld", (long long)i);
         if (ms[i] > (INT64_MAX / 16) / ns[i] || offsets[i] > INT64_MAX / 16 - ms[i] * ns[i])
             return fail(MUON_EINVAL, "matrix %lld: size or offset overflows the byte range", (long long)i);
+        nchunks += (ms[i] * ns[i] + PACK_CHUNK_ELEMS - 1) / PACK_CHUNK_ELEMS;
+        if (nchunks > INT32_MAX) return fail(MUON_EINVAL, "too many elements");
+    }
+    std::vector<PackMat> pm((size_t)count);
+    std::vector<PackChunk> chunks;
+    chunks.reserve((size_t)nchunks);
+    for (int64_t i = 0; i < count; ++i) {
         const int64_t numel = ms[i] * ns[i];
         const bool v = pk16 && (reinterpret_cast<uintptr_t>(mats[i]) & 15) == 0 && (offsets[i] * es) % 16 == 0;
         pm[(size_t)i] = PackMat{mats[i], offsets[i], v ? 1 : 0, 0};
         for (int64_t s0 = 0; s0 < numel; s0 += PACK_CHUNK_ELEMS)
             chunks.push_back(PackChunk{s0, (int)i, (int)std::min<int64_t>(PACK_CHUNK_ELEMS, numel - s0)});
     }
-    if (chunks.size() > (size_t)INT32_MAX) return fail(MUON_EINVAL, "too many elements");
     int r;
     DevCtx dc;
     if ((r = get_dev(dc))) return r;
@@ -2236,12 +2241,19 @@ extern "C" int muon_adamw_step(void* const* params, const void* const* grads, vo
     if (!std::isfinite(lr) || !std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(eps) ||
         !std::isfinite(wd) || beta1 < 0.f || beta1 >= 1.f || beta2 < 0.f || beta2 >= 1.f || eps < 0.f)
         return fail(MUON_EINVAL, "bad hyper-parameter");
-    std::vector<AdamTensor> tens((size_t)count);
-    std::vector<AdamChunk> chunks;
+    if (count > INT32_MAX) return fail(MUON_EINVAL, "more than 2^31 - 1 tensors");
+    int64_t nchunks = 0;                        // checked before any table is built
     for (int64_t i = 0; i < count; ++i) {
         if (!params[i] || !grads[i] || !exp_avg[i] || !exp_avg_sq[i])
             return fail(MUON_EINVAL, "NULL tensor pointer at %lld", (long long)i);
-        if (numels[i] < 0) return fail(MUON_EINVAL, "negative size at %lld", (long long)i);
+        if (numels[i] < 0 || numels[i] > INT64_MAX / 16) return fail(MUON_EINVAL, "bad size at %lld", (long long)i);
+        nchunks += (numels[i] + ADAM_CHUNK_ELEMS - 1) / ADAM_CHUNK_ELEMS;
+        if (nchunks > INT32_MAX) return fail(MUON_EINVAL, "too many elements");
+    }
+    std::vector<AdamTensor> tens((size_t)count);
+    std::vector<AdamChunk> chunks;
+    chunks.reserve((size_t)nchunks);
+    for (int64_t i = 0; i < count; ++i) {
         auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
         tens[(size_t)i] = AdamTensor{params[i], grads[i], exp_avg[i], exp_avg_sq[i],
                                      (a16(params[i]) && a16(grads[i]) && a16(exp_avg[i]) && a16(exp_avg_sq[i])) ? 1 : 0, 0};
@@ -2249,7 +2261,6 @@ extern "C" int muon_adamw_step(void* const* params, const void* const* grads, vo
             chunks.push_back(AdamChunk{s0, (int)i, (int)std::min<int64_t>(ADAM_CHUNK_ELEMS, numels[i] - s0)});
     }
     if (chunks.empty()) return MUON_OK;
-    if (chunks.size() > (size_t)INT32_MAX) return fail(MUON_EINVAL, "too many elements");
     int r;
     DevCtx dc;
     if ((r = get_dev(dc))) return r;

@@ -139,6 +139,26 @@ def test_step_and_orthogonalize_validation_before_any_device_use(mg):
     assert L.muon_ns_orthogonalize(0x1000, 1, 1, 1 << 31, 1, c, 5, segs, 3, None) == mg.MUON_EINVAL
 
 
+def test_adamw_rejects_oversized_tables_before_device_use(mg):
+    """Sizes whose chunk table would not fit the launch (or the byte range)
+    are rejected before any table is built or any device is touched.  The
+    pointers are placeholders, so this runs only without a CUDA device."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("placeholder pointers: host-only check")
+    L = mg.lib()
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    fake = (vp * 1)(0x1000)
+    for numel in (1 << 62, 1 << 50):
+        r = L.muon_adamw_step(fake, fake, fake, fake, (i64 * 1)(numel), 1, mg.MUON_BF16, mg.MUON_F32,
+                              1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None)
+        assert r == mg.MUON_EINVAL, (numel, r)
+    # a size within range gets past validation and stops at the missing device
+    r = L.muon_adamw_step(fake, fake, fake, fake, (i64 * 1)(1024), 1, mg.MUON_BF16, mg.MUON_F32,
+                          1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None)
+    assert r not in (mg.MUON_OK, mg.MUON_EINVAL)
+
+
 def test_debug_gemm_validation(mg):
     L = mg.lib()
     assert L.muon_debug_gemm(None, None, None, 4, 4, 4, 1, 1, 1, 0, 0, 1.0, 0, 0, 0, 0, None) == mg.MUON_EINVAL
