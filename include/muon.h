@@ -190,6 +190,7 @@ int muon_set_ns_precision(int dtype);
  * the plain and the Gram path (and the tile choices of the long products) on
  * synthetic data in the workspace with CUDA events (median of several runs)
  * and caches the fastest.  Synchronises `stream`.  Never touches caller data.
+ * Sides must lie in [1, 2^20], else MUON_EINVAL before any device work.
  */
 int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream);
 

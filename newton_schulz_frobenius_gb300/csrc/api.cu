@@ -1417,6 +1417,9 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
 int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype, void* stream) try {
     if (count < 0 || (count > 0 && (!ms || !ns))) return fail(MUON_EINVAL, "bad shape arrays");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    for (int64_t i = 0; i < count; ++i)
+        if (ms[i] < 1 || ns[i] < 1 || ms[i] > (1 << 20) || ns[i] > (1 << 20))
+            return fail(MUON_EINVAL, "shape %lld: sides must lie in [1, 2^20]", (long long)i);
     int r;
     DevCtx dc;
     if ((r = get_dev(dc))) return r;
@@ -1428,7 +1431,6 @@ int muon_autotune(const int64_t* ms, const int64_t* ns, int64_t count, int dtype
     }
     std::map<std::pair<int, int>, int> shapes;
     for (int64_t i = 0; i < count; ++i) {
-        if (ms[i] < 1 || ns[i] < 1) return fail(MUON_EINVAL, "bad shape at %lld", (long long)i);
         shapes[{(int)std::min(ms[i], ns[i]), (int)std::max(ms[i], ns[i])}] += 1;
     }
     const int nsd = ns_dtype(dtype, cfg);

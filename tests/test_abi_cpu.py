@@ -159,6 +159,16 @@ def test_adamw_rejects_oversized_tables_before_device_use(mg):
     assert r not in (mg.MUON_OK, mg.MUON_EINVAL)
 
 
+def test_autotune_validation_before_any_device_use(mg):
+    L = mg.lib()
+    i64 = ctypes.c_int64
+    assert L.muon_autotune(None, None, -1, mg.MUON_BF16, None) == mg.MUON_EINVAL
+    assert L.muon_autotune((i64 * 1)(4), (i64 * 1)(8), 1, 9, None) == mg.MUON_EDTYPE
+    for m, n in ((0, 8), (8, (1 << 20) + 1), ((1 << 31) + 5, 8)):
+        assert L.muon_autotune((i64 * 1)(m), (i64 * 1)(n), 1, mg.MUON_BF16, None) == mg.MUON_EINVAL, (m, n)
+        assert "2^20" in mg.last_error_message()
+
+
 def test_debug_gemm_validation(mg):
     L = mg.lib()
     assert L.muon_debug_gemm(None, None, None, 4, 4, 4, 1, 1, 1, 0, 0, 1.0, 0, 0, 0, 0, None) == mg.MUON_EINVAL
