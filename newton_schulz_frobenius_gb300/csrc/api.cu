@@ -349,7 +349,9 @@ static int validate_segments(int steps, const int* segs, int nseg) {
     int sum = 0;
     for (int i = 0; i < nseg; ++i) {
         if (segs[i] < 1) return fail(MUON_EINVAL, "segment %d has length %d < 1", i, segs[i]);
+        if (segs[i] > steps) return fail(MUON_EINVAL, "segment %d longer than steps (%d)", i, steps);
         sum += segs[i];
+        if (sum > steps) break;                   // reported below; keeps the sum in range
     }
     if (sum != steps) return fail(MUON_EINVAL, "segments sum to %d, steps is %d", sum, steps);
     return MUON_OK;

@@ -102,6 +102,10 @@ def test_set_ns_config_validation(mg):
     assert L.muon_set_ns_config(c, 5, bad, 3, 0) == mg.MUON_EINVAL        # sums to 6
     zero = (ctypes.c_int * 2)(5, 0)
     assert L.muon_set_ns_config(c, 5, zero, 2, 0) == mg.MUON_EINVAL       # empty segment
+    huge = (ctypes.c_int * 2)(2 ** 31 - 1, 2 ** 31 - 1)
+    assert L.muon_set_ns_config(c, 5, huge, 2, 0) == mg.MUON_EINVAL       # no int overflow in the sum
+    over = (ctypes.c_int * 4)(3, 3, 3, -8)
+    assert L.muon_set_ns_config(c, 5, over, 4, 0) == mg.MUON_EINVAL       # running sum past steps
     assert L.muon_set_ns_config(c, 0, None, 0, 0) == mg.MUON_EINVAL       # no steps
     assert L.muon_set_ns_config(c, 5, None, 0, 9) == mg.MUON_EINVAL       # bad path
     nanc = (ctypes.c_float * 3)(float("nan"), 0, 0)
