@@ -222,6 +222,8 @@ const char* muon_last_error_message(void);
  * 1.443 -> 1.134 TFLOPs for 2560 x 9728); algorithmic counts products with a
  * symmetric result (XX^T and products of polynomials in the same Gram matrix)
  * as half.  path is MUON_PATH_PLAIN or MUON_PATH_GRAM (segments required).
+ * At most 64 segments, each of length 1..64 (for the plain path they only
+ * give the step count); MUON_EINVAL otherwise.
  */
 int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_segments,
                   double* nominal, double* algorithmic);

@@ -1533,8 +1533,11 @@ int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_s
     if (path == MUON_PATH_PLAIN) {
         int steps = 0;
         if (num_segments > 0) {
-            if (!segments) return fail(MUON_EINVAL, "segments NULL");
-            for (int i = 0; i < num_segments; ++i) steps += segments[i];
+            if (!segments || num_segments > 64) return fail(MUON_EINVAL, "segments NULL or more than 64");
+            for (int i = 0; i < num_segments; ++i) {
+                if (segments[i] < 1 || segments[i] > 64) return fail(MUON_EINVAL, "segment length outside [1, 64]");
+                steps += segments[i];
+            }
         } else {
             steps = 5;
         }
@@ -1545,9 +1548,10 @@ int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_s
         }
     } else if (path == MUON_PATH_GRAM) {
         if (num_segments < 1 || !segments) return fail(MUON_EINVAL, "Gram path needs segments");
+        if (num_segments > 64) return fail(MUON_EINVAL, "more than 64 segments");
         for (int si = 0; si < num_segments; ++si) {
             const int L = segments[si];
-            if (L < 1) return fail(MUON_EINVAL, "segment < 1");
+            if (L < 1 || L > 64) return fail(MUON_EINVAL, "segment length outside [1, 64]");
             prod(M, M, N, true);    // G = X X^T
             for (int j = 1; j <= L; ++j) {
                 prod(M, M, M, true);                 // G^2

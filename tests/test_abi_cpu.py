@@ -93,6 +93,11 @@ def test_flops_rejects_bad_arguments(mg):
     assert L.muon_ns_flops(0, 5, 1, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
     assert L.muon_ns_flops(5, 5, 2, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
     assert L.muon_ns_flops(5, 5, 7, None, 0, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
+    huge = (ctypes.c_int * 2)(2 ** 31 - 1, 2 ** 31 - 1)
+    for path in (1, 2):                                 # no overflowing step count, no endless loop
+        assert L.muon_ns_flops(5, 9, path, huge, 2, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
+    neg = (ctypes.c_int * 2)(3, -1)
+    assert L.muon_ns_flops(5, 9, 1, neg, 2, ctypes.byref(d), ctypes.byref(d)) == mg.MUON_EINVAL
 
 
 def test_set_ns_config_validation(mg):
