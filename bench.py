@@ -149,6 +149,27 @@ def _gen_inputs(torch, wl, device):
     return params, grads, moms, host_grads
 
 
+def _blas_threads():
+    """Threads of numpy's BLAS pool, where the oracle's matrix products run."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d["num_threads"] for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        try:
+            return max(1, int(os.environ[var]))
+        except (KeyError, ValueError):
+            pass
+    return os.cpu_count()
+
+
+# numpy's elementwise operations and copies run on one thread
+ELEMENTWISE_THREADS = 1
+
+
 def run_cpu_baseline(wl, max_seconds=30.0):
     """The fp64 oracle as it stands, timed on the host cores on a bounded sample."""
     from oracle import muon_oracle as orc
@@ -168,7 +189,7 @@ def run_cpu_baseline(wl, max_seconds=30.0):
         el = time.perf_counter() - t0
         if el * (done + 1) / done > max_seconds or done >= 3:
             break
-    return {"value": done / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": done / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{done} full Muon step(s) of one {r}x{c} {wl.param_dtype} matrix, {path} NS, "
                       f"numpy fp64 (BLAS threads = host cores)", "seconds": el}
 
@@ -209,7 +230,7 @@ def bench_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": args.workload, "matrices": wl.count, "shape": [r, c], "ns_path": path},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                              "sample": f"one full Muon step of the workload's first matrix ({r}x{c}) "
                                        f"per step (numpy fp64)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -283,7 +304,7 @@ def adamw_cpu_baseline(max_seconds=20.0):
         el = time.perf_counter() - t0
         if el * (done + 1) / done > max_seconds or done >= 8:
             break
-    return {"value": 22.0 * n * done / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": 22.0 * n * done / el / 1e9, "unit": "GB/s", "cores": ELEMENTWISE_THREADS, "kind": "oracle",
             "sample": f"{done} AdamW step(s) over {n} bf16 parameters with fp32 moments (numpy fp64), "
                       f"22 algorithmic bytes per element", "seconds": el}
 
@@ -320,7 +341,7 @@ def bench_reference_adamw(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": ADAMW_WORKLOAD, "elements_per_step": n, "param_dtype": "bf16",
                        "state_dtype": "f32", "bytes_per_element": 22},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": ELEMENTWISE_THREADS, "kind": "oracle",
                              "sample": f"AdamW over {n} bf16 parameters per step (numpy fp64)"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -361,7 +382,7 @@ def pack_cpu_baseline(shapes, offsets, max_seconds=20.0):
         el = time.perf_counter() - t0
         if el * (done + 1) / done > max_seconds or done >= 5:
             break
-    return {"value": 4.0 * n * done / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": 4.0 * n * done / el / 1e9, "unit": "GB/s", "cores": ELEMENTWISE_THREADS, "kind": "oracle",
             "sample": f"{done} pack(s) of the first {len(take)} matrices ({n} bf16 elements, read + write "
                       f"4 bytes per element) with the numpy packing oracle", "seconds": el}
 
