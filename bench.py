@@ -1,13 +1,21 @@
 """Benchmark of the Muon update hot path on GB300.
 
-One step = one full Muon update (momentum + Nesterov, Frobenius normalisation,
+One step = one full Muon update (momentum, Frobenius normalisation,
 Newton-Schulz with the path chosen by the measured-cost autotune, shape-scaled
-decoupled-decay update) of the 2560 x 9728 bf16 matrix, through the C ABI's
+decoupled-decay update) of every matrix of the workload, through the C ABI's
 persistent group (muon_group_step, the optimizer object of a training loop),
 with parameters, momentum and gradient resident in HBM.  L2 is flushed (256 MiB
 write) between timed steps, outside the per-step CUDA events.
 
+The default workload is the largest one that fits one GPU: the 32-layer
+7B-class stack (hidden 4096, FFN 14336, 8 KV heads of dim 128; 224 bf16
+matrices, fp32 momentum, about 7e9 parameters).  --workload selects another
+(the single 2560x9728 matrix, the 512-matrix small bucket, the 24-layer stack,
+the fp32 and fp16 cases, AdamW, packing); --slice D keeps 1/D of every shape
+of a stack (for profiling runs that must stay small).
+
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                        [--workload NAME] [--slice D] [--no-cpu-baseline]
 Under torchrun each rank runs its own replica of the workload (the matrices
 are independent units; no collective on the data path) and rank 0 prints one
 JSON line with the whole-job throughput.
@@ -29,7 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "Muon-step matrices/s and NS TFLOP/s (fraction of GB300 dense BF16 peak)"
 UNIT = "matrices/s"
-WORKLOAD = "single_2560x9728_bf16"
+WORKLOAD = "stack_32L_7b_bf16_f32mom"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -170,32 +178,92 @@ def _blas_threads():
 ELEMENTWISE_THREADS = 1
 
 
-def run_cpu_baseline(wl, max_seconds=30.0):
-    """The fp64 oracle as it stands, timed on the host cores on a bounded sample."""
-    from oracle import muon_oracle as orc
-    from workloads import gen_matrix, zeros_matrix
-    idx, r, c = next(wl.matrices())
-    seed = wl.seed(idx)
-    W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
-    G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
-    M = zeros_matrix(r, c, wl.mom_dtype)
-    path = "gram" if max(r, c) > min(r, c) else "plain"
-    done, t0 = 0, time.perf_counter()
-    while True:
-        orc.muon_step(W.data, M.data, G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov,
-                      path=path, param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype,
+def _oracle_path(r, c, paths=None):
+    """NS path the oracle runs for a caller shape: the one the GPU run chose
+    (paths from muon_last_path), else Gram for rectangular and plain for
+    square shapes (what the autotune picks for every workload shape)."""
+    m, n = min(r, c), max(r, c)
+    if paths and f"{m}x{n}" in paths:
+        return paths[f"{m}x{n}"]
+    return "gram" if n > m else "plain"
+
+
+def _distinct_shapes(wl):
+    """One entry per distinct caller shape of the workload, in parameter
+    order: (index of its first matrix, rows, cols, matrices of that shape)."""
+    out = {}
+    for idx, r, c in wl.matrices():
+        if (r, c) not in out:
+            out[(r, c)] = [idx, 0]
+        out[(r, c)][1] += 1
+    return [(v[0], r, c, v[1]) for (r, c), v in out.items()]
+
+
+class _OracleCase:
+    """Generator bytes of one matrix of the workload and one full Muon step of
+    the fp64 oracle on them (inputs made once, outside any timing)."""
+
+    def __init__(self, wl, idx, r, c, path):
+        from workloads import gen_matrix, zeros_matrix
+        seed = wl.seed(idx)
+        self.wl, self.r, self.c, self.path = wl, r, c, path
+        self.W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
+        self.G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
+        self.M = zeros_matrix(r, c, wl.mom_dtype)
+
+    def step(self):
+        from oracle import muon_oracle as orc
+        wl = self.wl
+        t0 = time.perf_counter()
+        orc.muon_step(self.W.data, self.M.data, self.G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd,
+                      nesterov=wl.nesterov, path=self.path, param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype,
                       segments=tuple(wl.extra.get("segments", (2, 2, 1))))
-        done += 1
-        el = time.perf_counter() - t0
-        if el * (done + 1) / done > max_seconds or done >= 3:
-            break
-    return {"value": done / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} full Muon step(s) of one {r}x{c} {wl.param_dtype} matrix, {path} NS, "
-                      f"numpy fp64 (BLAS threads = host cores)", "seconds": el}
+        return time.perf_counter() - t0
+
+
+def run_cpu_baseline(wl, paths=None, max_seconds=30.0):
+    """The fp64 oracle as it stands, timed on the host cores on a bounded sample.
+
+    One-shape workloads: full Muon steps of the workload's first matrix, as
+    many as fit in about max_seconds (at most three).  Workloads of several
+    shapes (the transformer stacks): one full Muon step of one matrix of every
+    distinct shape, extrapolated to the workload by its per-shape counts."""
+    shapes = _distinct_shapes(wl)
+    if len(shapes) == 1:
+        idx, r, c, _ = shapes[0]
+        case = _OracleCase(wl, idx, r, c, _oracle_path(r, c, paths))
+        done, el = 0, 0.0
+        while True:
+            el += case.step()
+            done += 1
+            if el * (done + 1) / done > max_seconds or done >= 3:
+                break
+        return {"value": wl.count * done / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                "sample": f"{done} full Muon step(s) of one {r}x{c} {wl.param_dtype} matrix, {case.path} NS, "
+                          f"numpy fp64 (BLAS threads = host cores)", "seconds": el}
+    parts, total_s, el = [], 0.0, 0.0
+    for idx, r, c, k in shapes:
+        case = _OracleCase(wl, idx, r, c, _oracle_path(r, c, paths))
+        t = case.step()
+        el += t
+        total_s += k * t
+        parts.append(f"{k} x {r}x{c} {case.path} {t:.2f} s")
+    return {"value": wl.count / total_s, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "extrapolated": True,
+            "sample": "extrapolated: one full Muon step of one matrix of every distinct shape "
+                      f"(numpy fp64, BLAS threads = host cores), times the workload's counts: {'; '.join(parts)}; "
+                      f"projected {total_s:.1f} s for all {wl.count} matrices",
+            "seconds": el}
 
 
 def bench_reference(args):
-    """--impl reference: the oracle as it stands on the host cores, same metric."""
+    """--impl reference: the oracle as it stands on the host cores, same metric.
+
+    A step is one full Muon update of one matrix by the fp64 oracle.  The
+    timed steps cycle through the workload's distinct shapes (every shape at
+    least once, even when --steps is smaller), and the value extrapolates the
+    mean time per shape to the whole workload by its per-shape counts.  The
+    warm-up steps run the cheapest shape."""
     world, rank, _ = _dist()
     if rank != 0:
         return 0
@@ -203,39 +271,53 @@ def bench_reference(args):
         return bench_reference_adamw(args)
     if args.workload == PACK_WORKLOAD:
         return bench_reference_pack(args)
-    from oracle import muon_oracle as orc
-    from workloads import WORKLOADS, gen_matrix, zeros_matrix
-    wl = WORKLOADS[args.workload]
-    idx, r, c = next(wl.matrices())
-    seed = wl.seed(idx)
-    W = gen_matrix(seed, 1, r, c, wl.weight_std, wl.param_dtype)
-    G = gen_matrix(seed, 0, r, c, wl.grad_std, wl.param_dtype)
-    M = zeros_matrix(r, c, wl.mom_dtype)
-
-    def step():
-        orc.muon_step(W.data, M.data, G.data, lr=wl.lr, beta=wl.beta, wd=wl.wd, nesterov=wl.nesterov,
-                      path=path, param_dtype=wl.param_dtype, mom_dtype=wl.mom_dtype,
-                      segments=tuple(wl.extra.get("segments", (2, 2, 1))))
-
-    path = "gram" if max(r, c) > min(r, c) else "plain"
+    from workloads import WORKLOADS
+    wl = _sliced(WORKLOADS[args.workload], args.slice)
+    shapes = _distinct_shapes(wl)
+    cases = [_OracleCase(wl, idx, r, c, _oracle_path(r, c)) for idx, r, c, _ in shapes]
+    cheapest = min(range(len(cases)), key=lambda i: cases[i].r * cases[i].c)
     for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    el = time.perf_counter() - t0
-    value = args.steps / el              # one matrix per step
+        cases[cheapest].step()
+    nsteps = max(args.steps, len(cases))
+    times = [[] for _ in cases]
+    el = 0.0
+    for i in range(nsteps):
+        t = cases[i % len(cases)].step()
+        times[i % len(cases)].append(t)
+        el += t
+    per_shape = [sum(ts) / len(ts) for ts in times]
+    total_s = sum(k * t for (_, _, _, k), t in zip(shapes, per_shape))
+    value = wl.count / total_s
+    if len(cases) == 1:
+        sample = (f"one full Muon step of one {cases[0].r}x{cases[0].c} matrix per step ({cases[0].path} NS, "
+                  f"numpy fp64), scaled to the workload's {wl.count} matrices")
+    else:
+        sample = ("one full Muon step of one matrix per step, cycling through the distinct shapes "
+                  + "; ".join(f"{k} x {r}x{c} {cs.path} {t:.2f} s" for (_, r, c, k), cs, t in
+                              zip(shapes, cases, per_shape))
+                  + f" (mean per step); extrapolated to all {wl.count} matrices by the per-shape counts")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "steps": nsteps, "warmup": args.warmup, "ms_per_step": 1e3 * el / nsteps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": args.workload, "matrices": wl.count, "shape": [r, c], "ns_path": path},
+            "data": "synthetic: seeded SplitMix64/Box-Muller generator bytes (workloads.py)",
+            "config": {"workload": wl.name, "matrices": wl.count,
+                       "shapes": [[r, c, k] for _, r, c, k in shapes],
+                       "ns_paths": {f"{min(cs.r, cs.c)}x{max(cs.r, cs.c)}": cs.path for cs in cases}},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-                             "sample": f"one full Muon step of the workload's first matrix ({r}x{c}) "
-                                       f"per step (numpy fp64)"},
+                             "extrapolated": len(cases) > 1, "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _sliced(wl, div):
+    """The workload with every shape's count divided by div (at least one
+    matrix each), for profiling runs that must hold only a few GB."""
+    if not div or div <= 1:
+        return wl
+    import dataclasses
+    shapes = [(r, c, max(1, k // div)) for r, c, k in wl.shapes]
+    return dataclasses.replace(wl, shapes=shapes, name=f"{wl.name}/slice{div}")
 
 
 def _kernel_hash():
@@ -247,16 +329,36 @@ def _kernel_hash():
     return h.hexdigest()[:16]
 
 
-def _measured_traffic(kernel_key):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
-    or None when absent or taken on a different kernel source."""
+def _instance_of(kernel_key):
+    """Short name of a kernel instance group, as profiles/ncu_traffic.json keys it."""
+    for prefix, name in (("gemm_tc_kernel symmetric", "symmetric"), ("gemm_tc_kernel long apply", "apply"),
+                         ("small_ns_kernel", "small"), ("gemm_simt_kernel", "simt"), ("adamw", "adamw")):
+        if kernel_key.startswith(prefix):
+            return name
+    return kernel_key
+
+
+def _measured_traffic(kernel_key, launches_per_step=None):
+    """Per-launch DRAM bytes (read + write) of the dominant kernel instance from
+    the committed ncu summary, or None when absent or taken on different
+    kernel sources.  An entry measured on a slice of the workload (1/D of
+    every shape) holds the instance's DRAM bytes per step of the slice; the
+    full workload's per-launch figure is that times D over the instance's
+    launches per step here (traffic taken to grow with the matrices processed)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get("symmetric_products" if kernel_key.startswith("gemm_tc_kernel symmetric") else kernel_key)
-        if e and e.get("kernel_hash") == _kernel_hash() and e.get("workload") == WORKLOAD_SEL[0]:
-            return float(e["dram_bytes_per_launch"])
+        inst = _instance_of(kernel_key)
+        for e in d.get("entries", []):
+            if e.get("instance") != inst or e.get("workload") != WORKLOAD_SEL[0]:
+                continue
+            if e.get("kernel_hash") != _kernel_hash():
+                return None
+            if "dram_bytes_per_launch" in e:
+                return float(e["dram_bytes_per_launch"])
+            if launches_per_step:
+                return float(e["dram_bytes_per_step_of_slice"]) * float(e["slice"]) / float(launches_per_step)
     except Exception:
         pass
     return None
@@ -613,8 +715,8 @@ def bench_gpu(args):
         dist.barrier()
     import newton_schulz_frobenius_gb300 as mg
     from workloads import WORKLOADS
-    wl = WORKLOADS[args.workload]
-    WORKLOAD_SEL[0] = args.workload
+    wl = _sliced(WORKLOADS[args.workload], args.slice)
+    WORKLOAD_SEL[0] = wl.name
     segs = tuple(wl.extra.get("segments", (2, 2, 1)))
     mg.muon_set_ns_config(mg.QUINTIC, 5, segs, mg.MUON_PATH_AUTO)
     total_elems = sum(r * c for _, r, c in wl.matrices())
@@ -739,7 +841,7 @@ def bench_gpu(args):
         roofline = {"kernel": best, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "launches": best_n, "avg_launch_ms": best_ms / best_n,
                     "work_per_launch_flop": best_work / best_n,
-                    "traffic": _measured_traffic(best), "peak_source": src}
+                    "traffic": _measured_traffic(best, best_n / args.steps), "peak_source": src}
     step_total_kernel_ms = sum(v[1] for v in ktimes.values()) / args.steps
     ns_tflops = alg_per_step * world / (ms * 1e-3) / 1e12
 
@@ -747,7 +849,7 @@ def bench_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.param_dtype, "data": data,
-        "config": {"workload": args.workload, "matrices": wl.count,
+        "config": {"workload": wl.name, "matrices": wl.count,
                    "shapes": [[r, c, k] for r, c, k in wl.shapes], "param_dtype": wl.param_dtype,
                    "mom_dtype": wl.mom_dtype, "ns_paths": paths, "segments": "+".join(str(x) for x in segs), "steps_ns": 5,
                    "lr": wl.lr, "beta": wl.beta, "wd": wl.wd, "nesterov": wl.nesterov,
@@ -774,7 +876,7 @@ def bench_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = run_cpu_baseline(wl)
+        line["cpu_baseline"] = run_cpu_baseline(wl, paths)
     elif rank == 0 and world == 1:
         line["cpu_baseline"] = None
     group.close()
@@ -794,6 +896,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slice", type=int, default=1,
+                    help="keep 1/D of every shape of the workload (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

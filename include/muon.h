@@ -104,21 +104,33 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
  * cudaMalloc, cudaFree, cudaMallocHost or other allocating routine.
  *   - The status word, the matrix table and the NS buffers of the whole batch
  *     must fit in the 64 MiB: one 1024 x 4096 bf16 matrix, 31 of 256 x 1024
- *     bf16, 127 of 128 x 512 bf16 (2048 x 2048 does not fit).  A call that
- *     does not fit returns
+ *     bf16, 127 of 128 x 512 bf16 (2048 x 2048 does not fit); batch at most
+ *     65535.  A call that does not fit returns
  *     MUON_EINVAL (see muon_last_error_message) and enqueues nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
  *   - Every call reuses the same array, which keeps the last call's contents;
  *     calls that overlap on the GPU (two streams, or two host threads) race.
- *   - Device-detected errors go to a status word inside the array, not to the
- *     one muon_sync_status reads; a non-finite input gives a non-finite output.
+ *     Each call first clears, on `stream`, the counters it relies on, so a
+ *     call that follows a race starts clean.
+ *   - Device-detected errors (a non-finite norm, a bounded wait that gave
+ *     up) accumulate in a status word inside the array, not in the one
+ *     muon_sync_status reads: read and clear them with
+ *     muon_noalloc_sync_status.  A non-finite input gives a non-finite output.
  *   - With muon_set_kernel_timing(1) the timing records create CUDA events.
  */
 int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, int64_t batch, int dtype,
                                   const float coeffs[3], int steps, const int* segments,
                                   int num_segments, void* stream);
+
+/* Companion of muon_ns_orthogonalize_noalloc, equally free of allocation:
+ * synchronise `stream`, then read and clear the status word inside the fixed
+ * array on the current device: MUON_OK, MUON_ENONFINITE or MUON_ETIMEOUT for
+ * the no-alloc calls since the last read (MUON_ECUDA if the sync failed).
+ * The first call on a device looks up the array's address, like the first
+ * muon_ns_orthogonalize_noalloc. */
+int muon_noalloc_sync_status(void* stream);
 
 /*
  * One Muon step over `count` matrices (the optimizer call the pages' drop-in
@@ -302,6 +314,22 @@ int muon_pack(void* const* mats, const int64_t* ms, const int64_t* ns, const int
 
 /* Total kernels this library has launched in this process. */
 int64_t muon_launch_count(void);
+
+/*
+ * Test hook of the kernels' bounded waits (not part of the method).  Arms a
+ * one-shot stall that the next launch of one kernel takes: its CTA 0 issues
+ * no copy for one pipeline stage, so the consumer's bounded wait for that
+ * stage runs out (after about two seconds); the kernel then raises
+ * MUON_ETIMEOUT in the status word, waits (bounded) for what it has in
+ * flight, frees its tensor memory and returns, leaving the device usable.
+ *   kernel 1  the tensor-core product kernel, unpaired launches (128-column
+ *             tiles or pairing off): k-block `stage` of CTA 0's first tile
+ *   kernel 2  the fused small-matrix kernel: prologue piece `stage` of CTA 0
+ *             (16-byte aligned matrices)
+ *   kernel 0  disarm.
+ * MUON_EINVAL for another kernel or a stage outside [0, 2^20].
+ */
+int muon_debug_arm_stall(int kernel, int stage);
 
 /* Enable (1) or disable (0) per-launch CUDA-event timing of the library's
  * kernels, recorded on the launching stream.  Reading resets the record. */

@@ -34,11 +34,12 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 
 #: every entry point include/muon.h declares
 EXPORTS = (
-    "muon_ns_orthogonalize", "muon_ns_orthogonalize_noalloc", "muon_step", "muon_set_ns_config",
+    "muon_ns_orthogonalize", "muon_ns_orthogonalize_noalloc", "muon_noalloc_sync_status", "muon_step",
+    "muon_set_ns_config",
     "muon_set_ns_precision", "muon_autotune",
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
-    "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm",
+    "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm", "muon_debug_arm_stall",
     "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan", "muon_adamw_step",
     "muon_pack_plan", "muon_pack",
 )
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "muon_ns_orthogonalize": (i32, [vp, i64, i64, i64, i32, f3, i32, ip, i32, vp]),
         "muon_ns_orthogonalize_noalloc": (i32, [vp, i64, i64, i64, i32, f3, i32, ip, i32, vp]),
+        "muon_noalloc_sync_status": (i32, [vp]),
         "muon_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), i64p, i64p, i64,
                             i32, i32, f32, f32, f32, i32, vp]),
         "muon_set_ns_config": (i32, [f3, i32, ip, i32, i32]),
@@ -81,6 +83,7 @@ def lib() -> ctypes.CDLL:
         "muon_last_error_message": (ctypes.c_char_p, []),
         "muon_ns_flops": (i32, [i64, i64, i32, ip, i32, dp, dp]),
         "muon_launch_count": (i64, []),
+        "muon_debug_arm_stall": (i32, [i32, i32]),
         "muon_set_kernel_timing": (i32, [i32]),
         "muon_kernel_timing_read": (i32, [ctypes.c_char_p, i64p, dp, dp, i32]),
         "muon_debug_gemm": (i32, [vp, vp, vp, i64, i64, i64, i64, i32, i32, i32, i32,
@@ -304,6 +307,11 @@ def muon_sync_status(stream=None) -> int:
     return lib().muon_sync_status(_stream_ptr(stream))
 
 
+def muon_noalloc_sync_status(stream=None) -> int:
+    """Status word of the allocation-free calls (read and cleared; allocates nothing)."""
+    return lib().muon_noalloc_sync_status(_stream_ptr(stream))
+
+
 def muon_ns_flops(m: int, n: int, path: int, segments=(2, 2, 1)):
     segs, nseg = _ints(segments)
     nom, alg = ctypes.c_double(), ctypes.c_double()
@@ -313,6 +321,17 @@ def muon_ns_flops(m: int, n: int, path: int, segments=(2, 2, 1)):
 
 def muon_launch_count() -> int:
     return lib().muon_launch_count()
+
+
+#: kernels the bounded-wait test hook can stall
+STALL_PRODUCT = 1
+STALL_SMALL = 2
+
+
+def muon_debug_arm_stall(kernel: int, stage: int = 0) -> None:
+    """Test hook: the next launch of `kernel` leaves one stage unfilled, so its
+    bounded wait runs out and muon_sync_status reports MUON_ETIMEOUT."""
+    _check(lib().muon_debug_arm_stall(int(kernel), int(stage)), "muon_debug_arm_stall")
 
 
 def muon_set_kernel_timing(enable: bool):

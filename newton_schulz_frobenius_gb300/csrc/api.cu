@@ -324,6 +324,18 @@ void note_launch_end(int kclass, double work, cudaStream_t s) {
     t_open = -1;
 }
 
+// One-shot stall of the bounded-wait test hook: kind and stage + 1 packed in
+// one word so that arming and taking are single atomic operations.
+static std::atomic<int> g_stall{0};
+
+int take_stall(int kind) {
+    int v = g_stall.load();
+    while (v != 0 && (v & 0xFF) == kind) {
+        if (g_stall.compare_exchange_weak(v, 0)) return v >> 8;
+    }
+    return 0;
+}
+
 }  // namespace muon
 
 namespace muon {
@@ -428,8 +440,10 @@ static int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kcl
     const double work = a.symmetric ? mnk : 2.0 * mnk;
     const bool tc = (is_half(a.dtype) || a.dtype == DT_TF32);
     const int kc = tc ? kclass : KC_SIMT;
+    GemmArgs ga = a;
+    if (tc) ga.stall = take_stall(STALL_PRODUCT);
     note_launch_begin(kc, s);
-    cudaError_t e = tc ? launch_gemm_tc(a, dc.sms, s) : launch_gemm_simt(a, s);
+    cudaError_t e = tc ? launch_gemm_tc(ga, dc.sms, s) : launch_gemm_simt(a, s);
     note_launch_end(kc, work, s);
     if (e != cudaSuccess) return cuda_fail(e, "product launch");
     return MUON_OK;
@@ -864,8 +878,10 @@ static double plan_alg_flops(const NsPlan& p, int m, int n) {
 
 static int run_small(const DevCtx& dc, cudaStream_t s, const SmallArgs& a, double alg_flops) {
     NvtxRange nvr("fused small-matrix launch");
+    SmallArgs sa = a;
+    sa.stall = take_stall(STALL_SMALL);
     note_launch_begin(KC_SMALL, s);
-    cudaError_t e = launch_small_ns(a, dc.sms, s);
+    cudaError_t e = launch_small_ns(sa, dc.sms, s);
     note_launch_end(KC_SMALL, alg_flops, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused small-matrix launch");
     return MUON_OK;
@@ -1573,6 +1589,17 @@ int muon_ns_flops(int64_t m, int64_t n, int path, const int* segments, int num_s
 
 int64_t muon_launch_count(void) { return g_launches.load(); }
 
+int muon_debug_arm_stall(int kernel, int stage) {
+    if (kernel == STALL_NONE) {
+        g_stall.store(0);
+        return MUON_OK;
+    }
+    if ((kernel != STALL_PRODUCT && kernel != STALL_SMALL) || stage < 0 || stage > (1 << 20))
+        return fail(MUON_EINVAL, "kernel must be 0, 1 or 2 and stage in [0, 2^20]");
+    g_stall.store(((stage + 1) << 8) | kernel);
+    return MUON_OK;
+}
+
 int muon_set_kernel_timing(int enable) {
     g_timing.store(enable ? 1 : 0);
     return MUON_OK;
@@ -1670,10 +1697,15 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
 // holds it until the process exits.  It holds, in order, a status word, the
 // matrix table, and the NS buffers of the whole batch (no chunking), so a call
 // whose batch does not fit is rejected with MUON_EINVAL.  All calls share the
-// array and it keeps the last call's contents: the status word is cleared at
-// the start of every call and every other byte a call reads is written by that
-// call first.  Two calls that overlap on the GPU (different streams, or
-// different host threads) race on the array.
+// array and it keeps the last call's contents: the prep kernel's arrival
+// counters are cleared on the caller's stream at the start of every call, and
+// every other byte a call reads, except the status word, is written by that
+// call first.
+// Two calls that overlap on the GPU (different streams, or different host
+// threads) race on the array; the next call after such a race starts clean.
+// Device-detected errors of these calls (a bounded wait that gave up, a
+// non-finite norm) accumulate in the array's status word (zero at load),
+// which muon_noalloc_sync_status reads and clears without allocating.
 // ---------------------------------------------------------------------------
 
 namespace muon {
@@ -1681,8 +1713,9 @@ namespace muon {
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(64) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
-// the prep kernel's per-matrix arrival counters (zero between launches)
-static __device__ int g_noalloc_prep_cnt[65536];
+// the prep kernel's per-matrix arrival counters (cleared by every call)
+constexpr int NOALLOC_MAX_BATCH = 65535;
+static __device__ int g_noalloc_prep_cnt[NOALLOC_MAX_BATCH + 1];
 
 struct NoallocDev {
     char* base = nullptr;   // device address of g_noalloc_scratch on this device
@@ -1715,8 +1748,6 @@ static int noalloc_setup(NoallocDev& out) {
         e = cudaGetSymbolAddress(&p, g_noalloc_prep_cnt);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(counters)");
         d.pcnt = static_cast<int*>(p);
-        e = cudaMemset(d.pcnt, 0, sizeof(g_noalloc_prep_cnt));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counters)");
         d.sms = sms;
         it = g_noalloc_dev.emplace(dev, d).first;
     }
@@ -1739,7 +1770,7 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
                                              int num_segments, void* stream) try {
     if (!ptr) return fail(MUON_EINVAL, "ptr is NULL");
     if (m < 1 || n < 1 || batch < 1) return fail(MUON_EINVAL, "m, n, batch must be >= 1");
-    if (m > (1 << 20) || n > (1 << 20) || batch > 65535) return fail(MUON_EINVAL, "size out of range");
+    if (m > (1 << 20) || n > (1 << 20) || batch > NOALLOC_MAX_BATCH) return fail(MUON_EINVAL, "size out of range");
     if (!valid_dtype(dtype)) return fail(MUON_EDTYPE, "dtype %d", dtype);
     if (!coeffs || !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
         return fail(MUON_EINVAL, "coeffs missing or non-finite");
@@ -1766,7 +1797,10 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
     DevCtx dc;
     dc.sms = nd.sms;
     dc.status = reinterpret_cast<int*>(nd.base);
-    MUON_CUDA(cudaMemsetAsync(dc.status, 0, sizeof(int), s));   // the status word starts at zero
+    // the arrival counters start at zero: a call that raced with another one
+    // (or was cut short) may have left them non-zero.  The status word is not
+    // cleared here: it keeps every call's errors until it is read.
+    MUON_CUDA(cudaMemsetAsync(nd.pcnt, 0, sizeof(int) * (size_t)batch, s));
 
     MatEntry* d_table = reinterpret_cast<MatEntry*>(nd.base + status_bytes);
     char* cbase = nd.base + status_bytes + table_bytes;
@@ -1786,6 +1820,20 @@ extern "C" int muon_ns_orthogonalize_noalloc(void* ptr, int64_t m, int64_t n, in
         return r;
     FinalEpi fin{EPI_OUT, d_table, dtype, 0.f, 0.f, 0.f};
     return run_ns(dc, s, cbase, L, om, on, (int)batch, nsd, plan, x_holds_u(nsd), fin);
+} MUON_CATCH_ALL
+
+extern "C" int muon_noalloc_sync_status(void* stream) try {
+    NoallocDev nd;
+    int r = noalloc_setup(nd);
+    if (r) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MUON_CUDA(cudaStreamSynchronize(s));
+    int v = 0;
+    MUON_CUDA(cudaMemcpy(&v, nd.base, sizeof v, cudaMemcpyDeviceToHost));
+    if (v) MUON_CUDA(cudaMemset(nd.base, 0, sizeof v));
+    if (v & STATUS_TIMEOUT) return MUON_ETIMEOUT;
+    if (v & STATUS_NONFINITE) return MUON_ENONFINITE;
+    return MUON_OK;
 } MUON_CATCH_ALL
 
 // ---------------------------------------------------------------------------

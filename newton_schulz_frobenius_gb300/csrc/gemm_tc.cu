@@ -537,6 +537,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ok = false;
                         break;
                     }
+                    if (args.stall && kb == args.stall - 1 && t == unit0 && blockIdx.x == 0) {
+                        // test hook: this stage is never filled, so the MMA
+                        // issuer's bounded wait for it runs out; nothing is
+                        // in flight for it (issued[] keeps its older phase)
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
@@ -566,12 +576,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             }
-            if (!ok) {
-                // wait (bounded) for this CTA's copies still in flight
+            // wait (bounded) for this CTA's copies still in flight: after an
+            // abort the MMA issuer no longer consumes them, and even when this
+            // loop ended normally the issuer may still give up on a stage
+            // before the last copies land.  Without an abort the copies are
+            // the issuer's next operands and land at once.
 #pragma unroll
-                for (int s = 0; s < S; ++s)
-                    if (issued[s] >= 0) wait_drain(full0 + 8 * s, (uint32_t)issued[s]);
-            }
+            for (int s = 0; s < S; ++s)
+                if (issued[s] >= 0) wait_drain(full0 + 8 * s, (uint32_t)issued[s]);
         }
         __syncwarp();
     } else if (warp == 1 && PAIR && rank == 1) {
@@ -840,6 +852,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     std::memset(&mC, 0, sizeof mC);
     GemmArgs ga = a;
     ga.tma_c = 0;
+    if (PAIR) ga.stall = 0;     // the wait test hook runs on unpaired launches only
     const bool c16 = is_half(a.c_dtype) && !a.round_tf32;
     const bool al = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 8 == 0) && (a.strideC % 8 == 0 || a.batch <= 1);
     if (B_KMAJOR && (a.epi == EPI_STORE || a.epi == EPI_POLY) && c16 && al && tma_store_enabled()) {
@@ -903,7 +916,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if ((int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + 127) / 128) > (int64_t)1 << 30)
         return cudaErrorInvalidValue;
     // symmetric products default to 128 x 128 tiles, the others to 128 x 256;
-    // 128 x 256 tiles may run as 2-CTA clusters sharing the B tile
+    // 128 x 256 tiles may run as 2-SM products on 2-CTA clusters (each CTA
+    // loads its own operand tiles)
     const int bn = a.symmetric ? (a.tile_n == 256 ? 256 : 128) : (a.tile_n == 128 ? 128 : 256);
     const bool pair = (bn == 256) && a.pair != 0;
     if (tf32) {

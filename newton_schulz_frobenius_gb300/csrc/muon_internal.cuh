@@ -76,6 +76,7 @@ struct GemmArgs {
     int tma_c;              // set by the launcher: 16-bit workspace output written by tile stores
     int* status;            // device status word
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd
+    int stall;              // test hook: k + 1 = CTA 0 leaves k-block k of its first tile unfilled; 0 = off
 };
 
 // Launchers (return the CUDA error of the launch).
@@ -141,6 +142,7 @@ struct SmallArgs {
     float a, b, c;
     int* status;
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}
+    int stall;              // test hook: k + 1 = CTA 0 issues no copy for its prologue piece k; 0 = off
 };
 bool small_ns_fits(int m, int n, int nseg, const int* segs);
 cudaError_t launch_small_ns(const SmallArgs& a, int num_sms, cudaStream_t s);
@@ -234,5 +236,11 @@ enum KernelClass : int {
 };
 void note_launch_begin(int kclass, cudaStream_t s);
 void note_launch_end(int kclass, double work, cudaStream_t s);
+
+// Test hook of the bounded waits (muon_debug_arm_stall): the stage to leave
+// unfilled (+1) in the next launch of the given kernel kind, consumed by that
+// launch; 0 when nothing is armed.
+enum StallKind : int { STALL_NONE = 0, STALL_PRODUCT = 1, STALL_SMALL = 2 };
+int take_stall(int kind);
 
 }  // namespace muon

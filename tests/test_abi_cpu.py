@@ -202,3 +202,14 @@ def test_kernel_timing_read_empty(mg):
     mg.muon_set_kernel_timing(False)
     assert mg.muon_kernel_timing_read() == {}
     assert mg.muon_launch_count() >= 0
+
+
+def test_arm_stall_validation(mg):
+    """The bounded-wait test hook is host state only: bad kernels or stages
+    are refused, and disarming always succeeds."""
+    for kernel, stage in ((3, 0), (1, -1), (2, 1 << 21)):
+        with pytest.raises(mg.MuonError) as ei:
+            mg.muon_debug_arm_stall(kernel, stage)
+        assert ei.value.status == mg.MUON_EINVAL
+    mg.muon_debug_arm_stall(mg.STALL_PRODUCT, 2)
+    mg.muon_debug_arm_stall(0)

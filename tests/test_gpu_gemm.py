@@ -167,9 +167,9 @@ def test_poly_tf32(mg):
     ("mn", 200, 304, 136, 2), ("mn", 640, 1000, 512, 1), ("mn", 384, 256, 256, 3),
     ("tf32", 384, 384, 520, 2), ("tf32sym", 896, 896, 136, 1)])
 def test_paired_products(mg, monkeypatch, kind, M, N, K, batch):
-    """128 x 256 tiles run as 2-CTA clusters whose CTAs share the B tile by
-    multicast (row blocks 2p and 2p+1; an odd last block reads zeros and stores
-    nothing).  Same tiles and K order as the unpaired kernel, so the results
+    """128 x 256 tiles run as 2-SM products on 2-CTA clusters (row blocks 2p
+    and 2p+1; each CTA loads its own A rows and its half of the B tile; an odd
+    last block reads zeros and stores nothing).  Same tiles and K order as the unpaired kernel, so the results
     are bitwise equal to it, and they match the fp64 product."""
     tf32 = kind.startswith("tf32")
     dtype = torch.float32 if tf32 else torch.bfloat16
