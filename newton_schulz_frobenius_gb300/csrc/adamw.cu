@@ -11,7 +11,7 @@
 // bracket is formed first and subtracted once: a factor (1 - lr wd) rounded to
 // fp32 would carry an error of the same sign into every element, comparable
 // to the update itself at small lr.
-#include "muon_internal.cuh"
+#include "host.h"
 #include "epilogue.cuh"
 
 namespace muon {
@@ -82,3 +82,81 @@ cudaError_t launch_adamw(const AdamArgs& a, int nchunks, cudaStream_t s) {
 }
 
 }  // namespace muon
+
+// ---------------------------------------------------------------------------
+// host entry point
+// ---------------------------------------------------------------------------
+
+using namespace muon;
+
+// ---------------------------------------------------------------------------
+// AdamW for the non-matrix parameters ("MuonX" page, section 2)
+// ---------------------------------------------------------------------------
+
+extern "C" int muon_adamw_step(void* const* params, const void* const* grads, void* const* exp_avg,
+                               void* const* exp_avg_sq, const int64_t* numels, int64_t count, int param_dtype,
+                               int state_dtype, float lr, float beta1, float beta2, float eps, float wd,
+                               int64_t step, void* stream) try {
+    if (count < 0) return fail(MUON_EINVAL, "count < 0");
+    if (count == 0) return MUON_OK;
+    if (!params || !grads || !exp_avg || !exp_avg_sq || !numels) return fail(MUON_EINVAL, "NULL array argument");
+    if (!valid_dtype(param_dtype) || !(state_dtype == MUON_F32 || state_dtype == MUON_BF16))
+        return fail(MUON_EDTYPE, "dtypes %d / %d (moments: fp32 or bf16)", param_dtype, state_dtype);
+    if (step < 1) return fail(MUON_EINVAL, "step counts from 1");
+    if (!std::isfinite(lr) || !std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(eps) ||
+        !std::isfinite(wd) || beta1 < 0.f || beta1 >= 1.f || beta2 < 0.f || beta2 >= 1.f || eps < 0.f)
+        return fail(MUON_EINVAL, "bad hyper-parameter");
+    if (count > INT32_MAX) return fail(MUON_EINVAL, "more than 2^31 - 1 tensors");
+    int64_t nchunks = 0;                        // checked before any table is built
+    for (int64_t i = 0; i < count; ++i) {
+        if (!params[i] || !grads[i] || !exp_avg[i] || !exp_avg_sq[i])
+            return fail(MUON_EINVAL, "NULL tensor pointer at %lld", (long long)i);
+        if (numels[i] < 0 || numels[i] > INT64_MAX / 16) return fail(MUON_EINVAL, "bad size at %lld", (long long)i);
+        nchunks += (numels[i] + ADAM_CHUNK_ELEMS - 1) / ADAM_CHUNK_ELEMS;
+        if (nchunks > INT32_MAX) return fail(MUON_EINVAL, "too many elements");
+    }
+    std::vector<AdamTensor> tens((size_t)count);
+    std::vector<AdamChunk> chunks;
+    chunks.reserve((size_t)nchunks);
+    for (int64_t i = 0; i < count; ++i) {
+        auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+        tens[(size_t)i] = AdamTensor{params[i], grads[i], exp_avg[i], exp_avg_sq[i],
+                                     (a16(params[i]) && a16(grads[i]) && a16(exp_avg[i]) && a16(exp_avg_sq[i])) ? 1 : 0, 0};
+        for (int64_t s0 = 0; s0 < numels[i]; s0 += ADAM_CHUNK_ELEMS)
+            chunks.push_back(AdamChunk{s0, (int)i, (int)std::min<int64_t>(ADAM_CHUNK_ELEMS, numels[i] - s0)});
+    }
+    if (chunks.empty()) return MUON_OK;
+    int r;
+    DevCtx dc;
+    if ((r = get_dev(dc))) return r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tb = align_up(sizeof(AdamTensor) * tens.size(), 256);
+    const size_t cb = align_up(sizeof(AdamChunk) * chunks.size(), 256);
+    Workspace* w = nullptr;
+    if ((r = ws_get(dc.device, s, tb + cb, &w))) return r;
+    // both tables through the pinned staging ring, as one byte block (tb and cb
+    // are multiples of 256, so the block is a whole number of ring rows)
+    static_assert(256 % sizeof(MatEntry) == 0, "ring rows tile 256 bytes");
+    std::vector<MatEntry> rows((tb + cb) / sizeof(MatEntry));
+    std::memcpy(rows.data(), tens.data(), sizeof(AdamTensor) * tens.size());
+    std::memcpy(reinterpret_cast<char*>(rows.data()) + tb, chunks.data(), sizeof(AdamChunk) * chunks.size());
+    if ((r = upload_table(*w, rows, reinterpret_cast<MatEntry*>(w->base), s))) return r;
+    AdamArgs a;
+    a.tensors = reinterpret_cast<const AdamTensor*>(w->base);
+    a.chunks = reinterpret_cast<const AdamChunk*>(w->base + tb);
+    a.param_dtype = param_dtype;
+    a.state_dtype = state_dtype;
+    a.beta1 = beta1; a.beta2 = beta2; a.eps = eps;
+    const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
+    const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
+    a.lr_wd = (float)((double)lr * (double)wd);
+    a.step_size = (float)((double)lr / bc1);
+    a.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    double bytes = 0;
+    for (int64_t i = 0; i < count; ++i) bytes += (double)numels[i] * (3.0 * esize(param_dtype) + 4.0 * esize(state_dtype));
+    note_launch_begin(KC_ADAMW, s);
+    cudaError_t e = launch_adamw(a, (int)chunks.size(), s);
+    note_launch_end(KC_ADAMW, bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "adamw launch");
+    return MUON_OK;
+} MUON_CATCH_ALL

@@ -18,6 +18,8 @@
 #include "muon_internal.cuh"
 #include "epilogue.cuh"
 
+#include <cstdlib>
+
 namespace muon {
 
 namespace {
@@ -249,9 +251,13 @@ __global__ void fill_synthetic_kernel(void* X, int64_t count, int dtype, float s
 int prep_num_parts(int m, int n) { return prep_tiles(m, n); }
 
 int prep_grid_parts(int m, int n, int batch) {
+    const int t = prep_tiles(m, n);
+    if (const char* e = std::getenv("MUON_PREP_TPC")) {     // tiles per CTA (measurement knob)
+        const int tpc = std::atoi(e);
+        if (tpc > 0) return (t + tpc - 1) / tpc;
+    }
     // about 2048 CTAs per launch: a few tiles each, so that the per-matrix
     // partial sums (and the finalising count) stay short
-    const int t = prep_tiles(m, n);
     const int want = (2048 + batch - 1) / batch;
     return t < want ? t : (want < 1 ? 1 : want);
 }
