@@ -176,6 +176,31 @@ int muon_group_step(muon_group* group, float lr, float beta, float wd, int neste
 int muon_group_destroy(muon_group* group);
 
 /*
+ * Host-resident gradients and parameters for a group (a training loop that
+ * keeps them in host memory, e.g. an offloaded optimizer, or that reads the
+ * updated parameters back every step).  After this call every
+ * muon_group_step also copies each gradient in from host_grads[i] and each
+ * updated parameter out to host_params[i], on two copy streams of the group:
+ * all gradient copies are issued at the start of the step in the order the
+ * step processes its chunks of same-shape matrices, each chunk's update waits
+ * only for its own gradients, and each chunk's parameters leave as soon as it
+ * is updated, so the transfers overlap the tensor-core work of the other
+ * chunks.  The whole step, copies included, is ordered on `stream` as before.
+ *   host_grads   NULL, or `count` pointers (the group's matrix order) to
+ *                pinned host memory (cudaMallocHost, cudaHostAlloc or
+ *                cudaHostRegister) holding ms[i] x ns[i] elements of
+ *                param_dtype; read every step into grads[i]
+ *   host_params  NULL, or `count` pointers to pinned host memory that receive
+ *                params[i] after its update every step
+ * NULL for both turns the copies off again.  MUON_EINVAL for a NULL entry or
+ * memory that is not pinned host memory; the previous setting is kept then.
+ * The call synchronises the device (steps already enqueued with the previous
+ * buffers finish first); the buffers must stay valid while the group steps
+ * with them.
+ */
+int muon_group_set_host_io(muon_group* group, const void* const* host_grads, void* const* host_params);
+
+/*
  * NS configuration used by muon_step (process-wide, mutex-guarded).
  * coeffs/steps as above; segments/num_segments give the Gram segmentation
  * (default 2+2+1: "MuonX" page, section 3.2); path is a muon_path.

@@ -40,7 +40,8 @@ EXPORTS = (
     "muon_tune_save", "muon_tune_load", "muon_last_path", "muon_sync_status",
     "muon_status_str", "muon_last_error_message", "muon_ns_flops", "muon_launch_count",
     "muon_set_kernel_timing", "muon_kernel_timing_read", "muon_debug_gemm", "muon_debug_arm_stall",
-    "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_owner_plan", "muon_adamw_step",
+    "muon_group_create", "muon_group_step", "muon_group_destroy", "muon_group_set_host_io",
+    "muon_owner_plan", "muon_adamw_step",
     "muon_pack_plan", "muon_pack",
 )
 
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
                                     i32, i32, ctypes.POINTER(vp)]),
         "muon_group_step": (i32, [vp, f32, f32, f32, i32, vp]),
         "muon_group_destroy": (i32, [vp]),
+        "muon_group_set_host_io": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]),
         "muon_owner_plan": (i32, [i64p, i64p, i64, i32, i32, ip, dp, dp, ip]),
         "muon_adamw_step": (i32, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   i64p, i64, i32, i32, f32, f32, f32, f32, f32, i64, vp]),
@@ -253,6 +255,27 @@ class MuonGroup:
 
     def step(self, lr: float, beta: float = 0.95, wd: float = 0.0, nesterov: bool = True, stream=None):
         muon_group_step(self.handle, lr, beta, wd, nesterov, stream)
+
+    def set_host_io(self, host_grads=None, host_params=None):
+        """Pinned CPU tensors (same shapes and dtypes as the group's gradients
+        and parameters) that every step copies the gradients from and the
+        updated parameters to, overlapped with the update; None turns a
+        direction off."""
+        k = len(self._refs[0])
+        arrs = []
+        for lst, nm in ((host_grads, "host_grads"), (host_params, "host_params")):
+            if lst is None:
+                arrs.append(None)
+                continue
+            lst = list(lst)
+            if len(lst) != k:
+                raise ValueError(f"{nm} must hold {k} tensors")
+            for t, ref in zip(lst, self._refs[1] if nm == "host_grads" else self._refs[0]):
+                if t.device.type != "cpu" or not t.is_contiguous() or t.shape != ref.shape or t.dtype != ref.dtype:
+                    raise ValueError(f"{nm}: contiguous CPU tensors of the group's shapes and dtypes required")
+            arrs.append((ctypes.c_void_p * k)(*[t.data_ptr() for t in lst]))
+        self._host_refs = (host_grads, host_params)     # kept alive while the group uses them
+        _check(lib().muon_group_set_host_io(self.handle, arrs[0], arrs[1]), "muon_group_set_host_io")
 
     def close(self):
         if self.handle:

@@ -18,8 +18,6 @@
 #include "muon_internal.cuh"
 #include "epilogue.cuh"
 
-#include <cstdlib>
-
 namespace muon {
 
 namespace {
@@ -251,15 +249,15 @@ __global__ void fill_synthetic_kernel(void* X, int64_t count, int dtype, float s
 int prep_num_parts(int m, int n) { return prep_tiles(m, n); }
 
 int prep_grid_parts(int m, int n, int batch) {
+    // 8 tiles per CTA, 16 when that still gives at least eight waves of five
+    // CTAs per SM (152 SMs): long enough to amortise a CTA's set-up and its partial sum,
+    // short enough that the last wave of a launch stays small.  Measured
+    // against the earlier rule of about 2048 CTAs per launch: the 2560x9728
+    // prologue 0.57 -> 0.60 of the HBM copy rate, the 7B stack's 0.76 -> 0.79.
     const int t = prep_tiles(m, n);
-    if (const char* e = std::getenv("MUON_PREP_TPC")) {     // tiles per CTA (measurement knob)
-        const int tpc = std::atoi(e);
-        if (tpc > 0) return (t + tpc - 1) / tpc;
-    }
-    // about 2048 CTAs per launch: a few tiles each, so that the per-matrix
-    // partial sums (and the finalising count) stay short
-    const int want = (2048 + batch - 1) / batch;
-    return t < want ? t : (want < 1 ? 1 : want);
+    const int64_t total = (int64_t)t * batch;
+    const int tpc = total >= (int64_t)16 * 760 * 8 ? 16 : 8;
+    return (t + tpc - 1) / tpc;
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {

@@ -41,35 +41,132 @@ struct muon_group {
     bool graph_failed = false;
     bool direct_done = false;                       // a direct step ran since the last (re)plan
     uint64_t version = 0;                           // g_cfg_version the plans were made for
+    // host I/O (muon_group_set_host_io), per entry in bucket order
+    std::vector<size_t> entry_bytes;                // parameter bytes of the entry
+    std::vector<int64_t> caller_index;              // the entry's index in the caller's arrays
+    std::vector<const void*> host_g;                // pinned host gradients (empty: no copy in)
+    std::vector<void*> host_p;                      // pinned host parameters (empty: no copy out)
+    cudaStream_t io_in = nullptr, io_out = nullptr; // copy streams
+    std::vector<cudaEvent_t> io_ev;                 // fork, join and two per unit of work
 };
 
 namespace muon {
 
-static int group_enqueue(muon_group* g, cudaStream_t s) {
-    NvtxRange nvr("muon_group_step");
+// The step's units of work in launch order: each fused small-matrix launch
+// (all matrices of its buckets), then every chunk of every other bucket.
+// A unit is a list of entry ranges [first, first + count).
+struct GroupUnit {
+    int fused = -1;                                 // index into g->fused, or -1: bucket k, chunk at c0
+    size_t k = 0;
+    int64_t c0 = 0;
+    int B = 0;
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+};
+
+static std::vector<GroupUnit> group_units(const muon_group* g) {
+    std::vector<GroupUnit> units;
+    for (size_t f = 0; f < g->fused.size(); ++f) {
+        GroupUnit u;
+        u.fused = (int)f;
+        for (int k : g->fused[f].bks) u.ranges.push_back({g->bucket_first[(size_t)k], g->bucket_size[(size_t)k]});
+        units.push_back(u);
+    }
+    for (size_t k = 0; k < g->keys.size(); ++k) {
+        if (g->plans[k].fused) continue;
+        const int64_t cnt = g->bucket_size[k];
+        for (int64_t c0 = 0; c0 < cnt; c0 += g->chunks[k]) {
+            GroupUnit u;
+            u.k = k;
+            u.c0 = c0;
+            u.B = (int)std::min<int64_t>(g->chunks[k], cnt - c0);
+            u.ranges.push_back({g->bucket_first[k] + c0, u.B});
+            units.push_back(u);
+        }
+    }
+    return units;
+}
+
+static int group_run_unit(muon_group* g, const GroupUnit& u, cudaStream_t s) {
     int r;
-    for (const auto& f : g->fused) {
+    if (u.fused >= 0) {
+        const FusedLaunch& f = g->fused[(size_t)u.fused];
         const SmallArgs sa = fused_args(f, g->d_work, g->plans, g->keys, g->bucket_size, g->vec_ok,
                                         [&](int k) { return g->d_table + g->bucket_first[(size_t)k]; }, 0,
                                         g->param_dtype, g->mom_dtype, 0, 0.f, 0.f, 0.f, g->dc.status, g->d_hyper);
-        if ((r = run_small(g->dc, s, sa, fused_flops(f, g->plans, g->keys, g->bucket_size)))) return r;
+        return run_small(g->dc, s, sa, fused_flops(f, g->plans, g->keys, g->bucket_size));
     }
-    for (size_t k = 0; k < g->keys.size(); ++k) {
-        const int m = g->keys[k].first, n = g->keys[k].second;
-        const int64_t first = g->bucket_first[k], cnt = g->bucket_size[k];
-        const NsPlan& plan = g->plans[k];
-        if (plan.fused) continue;
-        const float scale = 0.2f * std::sqrt((float)n);
-        for (int64_t c0 = 0; c0 < cnt; c0 += g->chunks[k]) {
-            const int B = (int)std::min<int64_t>(g->chunks[k], cnt - c0);
-            const ChunkLayout L = chunk_layout(m, n, B, g->ns_dtype);
-            const MatEntry* dm = g->d_table + first + c0;
-            if ((r = run_prep(g->dc, s, g->cbase, L, m, n, B, dm, g->param_dtype, g->mom_dtype, g->ns_dtype, true,
-                              0, 0.f, g->vec_ok[k] != 0, g->pcnt, g->d_hyper)))
-                return r;
-            FinalEpi fin{EPI_UPDATE, dm, g->param_dtype, 0.f, 0.f, scale, g->d_hyper};
-            if ((r = run_ns(g->dc, s, g->cbase, L, m, n, B, g->ns_dtype, plan, x_holds_u(g->ns_dtype), fin))) return r;
+    const int m = g->keys[u.k].first, n = g->keys[u.k].second;
+    const NsPlan& plan = g->plans[u.k];
+    const float scale = 0.2f * std::sqrt((float)n);
+    const ChunkLayout L = chunk_layout(m, n, u.B, g->ns_dtype);
+    const MatEntry* dm = g->d_table + g->bucket_first[u.k] + u.c0;
+    if ((r = run_prep(g->dc, s, g->cbase, L, m, n, u.B, dm, g->param_dtype, g->mom_dtype, g->ns_dtype, true, 0, 0.f,
+                      g->vec_ok[u.k] != 0, g->pcnt, g->d_hyper)))
+        return r;
+    FinalEpi fin{EPI_UPDATE, dm, g->param_dtype, 0.f, 0.f, scale, g->d_hyper};
+    return run_ns(g->dc, s, g->cbase, L, m, n, u.B, g->ns_dtype, plan, x_holds_u(g->ns_dtype), fin);
+}
+
+// Events the host I/O of a step needs (fork, join, two per unit), created
+// outside any capture.
+static int group_io_events(muon_group* g) {
+    if (g->host_g.empty() && g->host_p.empty()) return MUON_OK;
+    const size_t need = 2 + 2 * group_units(g).size();
+    while (g->io_ev.size() < need) {
+        cudaEvent_t e = nullptr;
+        MUON_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        g->io_ev.push_back(e);
+    }
+    return MUON_OK;
+}
+
+static int group_enqueue(muon_group* g, cudaStream_t s) {
+    NvtxRange nvr("muon_group_step");
+    int r;
+    const std::vector<GroupUnit> units = group_units(g);
+    const bool cin = !g->host_g.empty(), cout = !g->host_p.empty();
+    if (!cin && !cout) {
+        for (const GroupUnit& u : units)
+            if ((r = group_run_unit(g, u, s))) return r;
+        return MUON_OK;
+    }
+    // host I/O: fork both copy streams off s; every gradient copy in launch
+    // order on io_in (one event per unit); each unit waits for its own
+    // gradients, and its parameters leave on io_out once it is done; both
+    // streams join s at the end
+    if (g->io_ev.size() < 2 + 2 * units.size()) return fail(MUON_EINVAL, "host I/O events missing");
+    cudaEvent_t fork = g->io_ev[0], join = g->io_ev[1];
+    MUON_CUDA(cudaEventRecord(fork, s));
+    MUON_CUDA(cudaStreamWaitEvent(g->io_in, fork, 0));
+    MUON_CUDA(cudaStreamWaitEvent(g->io_out, fork, 0));
+    if (cin) {
+        for (size_t i = 0; i < units.size(); ++i) {
+            for (const auto& rg : units[i].ranges)
+                for (int64_t e = rg.first; e < rg.first + rg.second; ++e)
+                    MUON_CUDA(cudaMemcpyAsync(const_cast<void*>(g->entries[(size_t)e].grad), g->host_g[(size_t)e],
+                                              g->entry_bytes[(size_t)e], cudaMemcpyHostToDevice, g->io_in));
+            MUON_CUDA(cudaEventRecord(g->io_ev[2 + 2 * i], g->io_in));
         }
+    }
+    for (size_t i = 0; i < units.size(); ++i) {
+        if (cin) MUON_CUDA(cudaStreamWaitEvent(s, g->io_ev[2 + 2 * i], 0));
+        if ((r = group_run_unit(g, units[i], s))) return r;
+        if (cout) {
+            MUON_CUDA(cudaEventRecord(g->io_ev[3 + 2 * i], s));
+            MUON_CUDA(cudaStreamWaitEvent(g->io_out, g->io_ev[3 + 2 * i], 0));
+            for (const auto& rg : units[i].ranges)
+                for (int64_t e = rg.first; e < rg.first + rg.second; ++e)
+                    MUON_CUDA(cudaMemcpyAsync(g->host_p[(size_t)e], g->entries[(size_t)e].w, g->entry_bytes[(size_t)e],
+                                              cudaMemcpyDeviceToHost, g->io_out));
+        }
+    }
+    // join: io_in ended with the last unit's gradients (waited on by s when
+    // copying in); io_out ends with the last unit's parameters
+    MUON_CUDA(cudaEventRecord(join, g->io_out));
+    MUON_CUDA(cudaStreamWaitEvent(s, join, 0));
+    if (!cin) {
+        MUON_CUDA(cudaEventRecord(g->io_ev[2], g->io_in));
+        MUON_CUDA(cudaStreamWaitEvent(s, g->io_ev[2], 0));
     }
     return MUON_OK;
 }
@@ -190,6 +287,8 @@ int muon_group_create(void* const* params, const void* const* grads, void* const
         bool vec = (k.first % 8 == 0) && (k.second % 8 == 0);
         for (int64_t i : idx) {
             g->entries.push_back(MatEntry{grads[i], moms[i], params[i], ms[i] > ns[i] ? 1 : 0, 0});
+            g->entry_bytes.push_back((size_t)ms[i] * (size_t)ns[i] * esize(param_dtype));
+            g->caller_index.push_back(i);
             vec = vec && (reinterpret_cast<uintptr_t>(grads[i]) % 16 == 0) &&
                   (reinterpret_cast<uintptr_t>(moms[i]) % 16 == 0);
         }
@@ -216,6 +315,7 @@ int muon_group_step(muon_group* g, float lr, float beta, float wd, int nesterov,
     int r;
     if (g->version != g_cfg_version.load() || !g->ws)
         if ((r = group_plan(g, s))) return r;
+    if ((r = group_io_events(g))) return r;
 
     // this step's hyper-parameters -> device block (ordered before the step on s)
     const int slot = g->hslot;
@@ -283,9 +383,53 @@ int muon_group_destroy(muon_group* g) {
         if (g->h_hyper[i]) cudaFreeHost(g->h_hyper[i]);
         if (g->hev[i]) cudaEventDestroy(g->hev[i]);
     }
+    for (cudaEvent_t e : g->io_ev) cudaEventDestroy(e);
+    if (g->io_in) cudaStreamDestroy(g->io_in);
+    if (g->io_out) cudaStreamDestroy(g->io_out);
     if (g->cap) cudaStreamDestroy(g->cap);
     delete g;
     return MUON_OK;
 }
+
+int muon_group_set_host_io(muon_group* g, const void* const* host_grads, void* const* host_params) try {
+    if (!g) return fail(MUON_EINVAL, "group is NULL");
+    int dev = -1;
+    MUON_CUDA(cudaGetDevice(&dev));
+    if (dev != g->device) return fail(MUON_EINVAL, "group belongs to device %d, current device is %d", g->device, dev);
+    auto pinned = [](const void* p) {
+        cudaPointerAttributes a;
+        if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        return a.type == cudaMemoryTypeHost;
+    };
+    std::vector<const void*> hg;
+    std::vector<void*> hp;
+    for (size_t e = 0; e < g->entries.size(); ++e) {
+        const int64_t i = g->caller_index[e];
+        if (host_grads) {
+            if (!pinned(host_grads[i]))
+                return fail(MUON_EINVAL, "host_grads[%lld] is NULL or not pinned host memory", (long long)i);
+            hg.push_back(host_grads[i]);
+        }
+        if (host_params) {
+            if (!pinned(host_params[i]))
+                return fail(MUON_EINVAL, "host_params[%lld] is NULL or not pinned host memory", (long long)i);
+            hp.push_back(host_params[i]);
+        }
+    }
+    if ((host_grads || host_params) && !g->io_in) {
+        MUON_CUDA(cudaStreamCreateWithFlags(&g->io_in, cudaStreamNonBlocking));
+        MUON_CUDA(cudaStreamCreateWithFlags(&g->io_out, cudaStreamNonBlocking));
+    }
+    // steps already enqueued with the old buffers (on whatever streams the
+    // caller stepped on) finish first
+    MUON_CUDA(cudaDeviceSynchronize());
+    g->host_g.swap(hg);
+    g->host_p.swap(hp);
+    group_drop_graph(g);        // the step's structure changed: capture it again
+    return MUON_OK;
+} MUON_CATCH_ALL
 
 }  // extern "C"

@@ -104,3 +104,59 @@ def test_group_fused_buckets_match_step(mg, monkeypatch):
             assert torch.equal(a, b)
     finally:
         group.close()
+
+
+@pytest.mark.parametrize("graph", ["1", "0"])
+def test_group_host_io_overlapped(mg, monkeypatch, graph):
+    """Host-resident gradients and parameters (muon_group_set_host_io): every
+    step copies the gradients in from pinned host memory and the updated
+    parameters out, chunk by chunk on the group's copy streams.  Over several
+    steps with gradients rewritten on the host, the device weights and momenta
+    equal those of muon_step on device gradients, and the host parameters
+    equal the device weights after every step."""
+    monkeypatch.setenv("MUON_GRAPH", graph)
+    monkeypatch.setenv("MUON_WORKSPACE_MB", "2")      # several chunks per bucket
+    shapes = [(256, 640), (640, 256), (256, 640), (128, 512), (512, 128), (96, 96)] * 2
+    Wa, Ga, Ma = _make(shapes, torch.bfloat16, torch.float32, 71)
+    Wb, Mb = [w.clone() for w in Wa], [m.clone() for m in Ma]
+    Gb = [torch.zeros_like(g) for g in Ga]             # filled from the host every step
+    host_g = [g.cpu().pin_memory() for g in Ga]
+    host_w = [torch.empty_like(w, device="cpu").pin_memory() for w in Wb]
+    group = mg.MuonGroup(Wb, Gb, Mb)
+    try:
+        group.set_host_io(host_g, host_w)
+        for i, (lr, beta, wd, nest) in enumerate(SCHEDULE):
+            for ga, hg in zip(Ga, host_g):
+                ga.mul_(-0.7).add_(0.001 * (i + 1))
+                hg.copy_(ga)                          # the host holds this step's gradients
+            torch.cuda.synchronize()
+            mg.muon_step(Wa, Ga, Ma, lr=lr, beta=beta, wd=wd, nesterov=nest)
+            group.step(lr=lr, beta=beta, wd=wd, nesterov=nest)
+            torch.cuda.synchronize()
+            assert mg.muon_sync_status() == mg.MUON_OK
+            for x, y in zip(Wa + Ma, Wb + Mb):
+                assert torch.equal(x, y), i
+            for hw, w in zip(host_w, Wb):
+                assert torch.equal(hw, w.cpu()), i
+        # copies off again: the group steps on its device gradients
+        group.set_host_io(None, None)
+        group.step(lr=0.02)
+        mg.muon_step(Wa, Gb, Ma, lr=0.02, beta=0.95, wd=0.0, nesterov=True)
+        torch.cuda.synchronize()
+        for x, y in zip(Wa + Ma, Wb + Mb):
+            assert torch.equal(x, y)
+    finally:
+        group.close()
+
+
+def test_group_host_io_rejects_pageable_memory(mg):
+    W, G, M = _make([(64, 128)], torch.bfloat16, torch.bfloat16, 9)
+    group = mg.MuonGroup(W, G, M)
+    try:
+        with pytest.raises(mg.MuonError) as ei:
+            group.set_host_io([G[0].cpu()], None)        # pageable
+        assert ei.value.status == mg.MUON_EINVAL
+        with pytest.raises(ValueError):
+            group.set_host_io([G[0].cpu().pin_memory()] * 2, None)
+    finally:
+        group.close()
