@@ -158,6 +158,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Load delivered to the same shared-memory offset, and signalled on the
+// mbarrier at the same offset, in every CTA of the cluster set in `mask`.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                               int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+
 // Tile store shared -> global on the copy engine (bulk group of this thread).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
@@ -354,11 +365,43 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 // one per CTA of a cluster (rank selects the row block); tiles_m then counts
 // row-block pairs, and in sym 2 pair p holds tn = 0 .. p.
 struct TileSched {
-    int tiles_m, tiles_n, per_batch, total, sym, pair;
+    int tiles_m, tiles_n, per_batch, total, sym, pair, mc;
 
-    __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn, int rank = 0) const {
+    // Units before pair row p of a symmetric multicast schedule: row i holds
+    // floor(i / 2) + 1 units of two tiles (tn = 2j and 2j + 1, up to i).
+    __host__ __device__ static int mc_sym_units(int p) { return p + (p / 2) * ((p - 1) / 2); }
+
+    // rank: the CTA's rank in its cluster.  valid (multicast schedules only):
+    // false when this pair's tile of the unit lies outside the matrix (odd
+    // tile counts); the pair then repeats its partner's tile and stores nothing.
+    __device__ __forceinline__ void decode(int t, int& b, int& tm, int& tn, int rank = 0, bool* valid = nullptr) const {
         b = t / per_batch;
         const int l = t - b * per_batch;
+        if (mc) {
+            // a unit is two pair tiles sharing pair row p (the same A rows):
+            // pair c = rank >> 1 takes column tile 2j + c
+            const int c = rank >> 1;
+            int p, j, lim;
+            if (sym) {
+                p = (int)(2.0f * (sqrtf((float)l + 1.0f) - 1.0f));
+                if (p < 0) p = 0;
+                while (p > 0 && mc_sym_units(p) > l) --p;
+                while (mc_sym_units(p + 1) <= l) ++p;
+                j = l - mc_sym_units(p);
+                lim = p;                       // tn <= p
+            } else {
+                p = l % tiles_m;
+                j = l / tiles_m;
+                lim = tiles_n - 1;
+            }
+            tn = 2 * j + c;
+            const bool ok = tn <= lim;
+            if (!ok) tn = 2 * j;
+            if (valid) *valid = ok;
+            tm = 2 * p + (rank & 1);
+            return;
+        }
+        if (valid) *valid = true;
         if (pair) {
             int p;
             if (sym) {
@@ -447,7 +490,7 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args, const TileSched sched) {
@@ -455,6 +498,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     constexpr int S = C::STAGES;
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
     static_assert(!PAIR || BN == 256, "paired products use 128 x 256 tiles per CTA");
+    static_assert(!MC || PAIR, "multicast clusters are made of 2-SM pairs");
     constexpr int MM = PAIR ? 2 * BM : BM;      // rows of one product instruction
     const uint32_t IDESC = TF32 ? idesc_tf32(MM, BN) : idesc_f16kind(MM, BN, !B_KMAJOR, args.dtype == MUON_F16);
     constexpr int KE = TF32 ? 32 : 64;    // elements per 128-byte k-block
@@ -476,19 +520,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Paired launches (2-SM products): the two CTAs of a cluster take the two
+    // Paired launches (2-SM products): the two CTAs of a pair take the two
     // row blocks of a 256 x BN tile.  Each loads its own A rows and its half
     // of B; the odd CTA relays "stage full" to the even CTA, which issues the
     // M = 256 products and commits to both; both epilogues report to the even
     // CTA's accumulator barrier.
+    // Multicast launches (MC): a cluster of two pairs takes two tiles that
+    // share their A rows (pair row p, column tiles 2j and 2j + 1).  CTA
+    // (pair c, half h) loads rows c * 64 .. + 64 of its 128 A rows and
+    // multicasts them to itself and to CTA (1 - c, h), so each A row leaves L2
+    // once per cluster; a stage is refilled only after both pairs' products
+    // have released it (the empty barriers count both pairs' commits).
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int lead = rank & ~1;             // the even CTA of this CTA's pair
     const int unit0 = PAIR ? (int)cluster_idx() : (int)blockIdx.x;
     const int ustep = PAIR ? (int)cluster_count() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, (PAIR && rank == 0) ? 2 : 1);   // own copies (+ the peer's relay)
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, (PAIR && (rank & 1) == 0) ? 2 : 1);   // own copies (+ the peer's relay)
+            mbar_init(empty0 + 8 * s, MC ? 2 : 1);                        // one commit per pair
         }
         mbar_init(accf0, 1);
         mbar_init(accf0 + 8, 1);
@@ -549,17 +600,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, C::STAGE_BYTES);
-                    tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
+                    if (MC) {
+                        // half of the A rows, to this CTA and its counterpart in the other pair
+                        const int c = rank >> 1, h = rank & 1;
+                        tma_load_3d_mc(smem_u32(sA + stage * C::A_BYTES + c * (C::A_BYTES / 2)), &tmA, fb, kb * KE,
+                                       tm * BM + c * (BM / 2), b, (uint16_t)((1u << h) | (1u << (2 + h))));
+                    } else {
+                        tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, fb, kb * KE, tm * BM, b);
+                    }
                     if (PAIR) {
-                        // this CTA's half of B: rows (K-major) or columns (MN-major) rank * BN / 2 ..
+                        // this CTA's half of B: rows (K-major) or columns (MN-major) (rank & 1) * BN / 2 ..
+                        const int hb = (rank & 1) * (BN / 2);
                         if (B_KMAJOR) {
-                            tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN + rank * (BN / 2),
-                                        b);
+                            tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN + hb, b);
                         } else {
 #pragma unroll
                             for (int q = 0; q < BN / 128; ++q)
                                 tma_load_3d(smem_u32(sB + stage * C::B_BYTES + q * (BK * 128)), &tmB, fb,
-                                            tn * BN + rank * (BN / 2) + q * 64, kb * BK, b);
+                                            tn * BN + hb + q * 64, kb * BK, b);
                         }
                     } else if (B_KMAJOR) {
                         tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, fb, kb * KE, tn * BN, b);
@@ -586,7 +644,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (issued[s] >= 0) wait_drain(full0 + 8 * s, (uint32_t)issued[s]);
         }
         __syncwarp();
-    } else if (warp == 1 && PAIR && rank == 1) {
+    } else if (warp == 1 && PAIR && (rank & 1) == 1) {
         // ---------------- relay (odd CTA of a pair) ----------------
         // every completed stage of this CTA is reported to the even CTA's full
         // barrier; this CTA refills it only after the even CTA's commit
@@ -600,7 +658,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ok = false;
                         break;
                     }
-                    mbar_arrive_remote_relaxed(full0 + 8 * stage, 0);
+                    mbar_arrive_remote_relaxed(full0 + 8 * stage, (uint32_t)lead);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -647,7 +705,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             else tc_mma_bf16(d, ad, bd, IDESC, accum);
                         }
                     }
-                    if (PAIR) tc_commit2(empty0 + 8 * stage, (uint16_t)0x3);
+                    // release the stage in both CTAs of the pair (MC: of both pairs)
+                    if (PAIR) tc_commit2(empty0 + 8 * stage, (uint16_t)(MC ? 0xF : (0x3u << lead)));
                     else tc_commit(empty0 + 8 * stage);
                     if (++stage == S) {
                         stage = 0;
@@ -655,14 +714,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 if (!ok) break;
-                if (PAIR) tc_commit2(accf0 + 8 * acc, (uint16_t)0x3);
+                if (PAIR) tc_commit2(accf0 + 8 * acc, (uint16_t)(0x3u << lead));
                 else tc_commit(accf0 + 8 * acc);
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
             }
             if (!ok) {
                 // wait (bounded) for the products this thread issued
-                if (PAIR) tc_commit2(drain_bar, (uint16_t)0x1);
+                if (PAIR) tc_commit2(drain_bar, (uint16_t)(0x1u << lead));
                 else tc_commit(drain_bar);
                 wait_drain(drain_bar, 0);
             }
@@ -679,8 +738,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t aphase = 0;
         for (int t = unit0; t < sched.total; t += ustep) {
             int b, tm, tn;
-            sched.decode(t, b, tm, tn, rank);
-            if (args.epi == EPI_UPDATE) {
+            bool vtile = true;
+            sched.decode(t, b, tm, tn, rank, &vtile);
+            const bool valid = MC ? vtile : true;  // MC: a repeated tile is computed, not stored
+            if (valid && args.epi == EPI_UPDATE) {
                 // the update reads the caller's W: start pulling this tile's
                 // part into L2 while the products are still accumulating
                 const MatEntry e = args.mats[b];
@@ -704,8 +765,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (args.epi == EPI_UPDATE || args.epi == EPI_OUT) ent = args.mats[b];
             const int row0 = tm * BM + q * 32;
             const int warp_row_max = row0 + 31;
-            const int ch_beg = half * (HALF_COLS / 32), ch_end = (half + 1) * (HALF_COLS / 32);
-            const bool loads = (args.epi == EPI_POLY || args.epi == EPI_UPDATE);
+            const int ch_beg = half * (HALF_COLS / 32), ch_end = valid ? (half + 1) * (HALF_COLS / 32) : ch_beg;
+            const bool loads = valid && (args.epi == EPI_POLY || args.epi == EPI_UPDATE);
             float gcur[32], gnxt[32];
             if (loads) epi_load_chunk<32>(args, ent, b, row0 + lane, tn * BN + ch_beg * 32, gcur);
             // every lane observes the barrier itself; the warp proceeds only together
@@ -739,7 +800,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (PAIR && rank == 1) mbar_arrive_remote(acce0 + 8 * acc, 0);
+                if (PAIR && (rank & 1)) mbar_arrive_remote(acce0 + 8 * acc, (uint32_t)lead);
                 else mbar_arrive(acce0 + 8 * acc);
             }
             acc ^= 1;
@@ -808,24 +869,25 @@ bool tma_store_enabled() {
     return !(e && e[0] == '0');
 }
 
-template <int BN, bool B_KMAJOR, bool TF32, bool PAIR>
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
-    auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR>;
+    auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR, MC>;
+    constexpr int CL = MC ? 4 : 2;           // CTAs per cluster of a paired launch
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
     std::call_once(attr_once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (attr_err == cudaSuccess && PAIR) {
-            // how many 2-CTA clusters of this kernel fit on the device at once
+            // how many clusters of this kernel fit on the device at once
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * (num_sms / 2));
+            cfg.gridDim = dim3(CL * (num_sms / CL));
             cfg.blockDim = dim3(NTHREADS);
             cfg.dynamicSmemBytes = C::SMEM_BYTES;
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.x = CL;
             at[0].val.clusterDim.y = 1;
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
@@ -838,8 +900,9 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
 
     CUtensorMap mA, mB;
     constexpr uint32_t KE = TF32 ? 32 : 64;   // elements per 128-byte k-block
+    // multicast launches load A in halves of BM / 2 rows
     if (!make_map(&mA, a.A, a.dtype, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch, (uint64_t)a.lda,
-                  (uint64_t)a.strideA, KE, BM))
+                  (uint64_t)a.strideA, KE, MC ? BM / 2 : BM))
         return cudaErrorInvalidValue;
     // a paired K-major B tile arrives as two halves of BN / 2 rows
     bool okB = B_KMAJOR ? make_map(&mB, a.B, a.dtype, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.batch,
@@ -866,10 +929,12 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     sc.tiles_n = (a.N + BN - 1) / BN;
     sc.sym = a.symmetric ? (BN == 256 ? 2 : 1) : 0;
     sc.pair = PAIR ? 1 : 0;
+    sc.mc = MC ? 1 : 0;
     if (PAIR) {
         const int pm = (sc.tiles_m + 1) / 2;
         sc.tiles_m = pm;
-        sc.per_batch = sc.sym ? pm * (pm + 1) / 2 : pm * sc.tiles_n;
+        if (MC) sc.per_batch = sc.sym ? TileSched::mc_sym_units(pm) : pm * ((sc.tiles_n + 1) / 2);
+        else sc.per_batch = sc.sym ? pm * (pm + 1) / 2 : pm * sc.tiles_n;
     } else if (sc.sym == 2) {
         sc.per_batch = 0;
         for (int tm = 0; tm < sc.tiles_m; ++tm) sc.per_batch += tm / 2 + 1;
@@ -881,16 +946,16 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
         const int grid = sc.total < num_sms ? sc.total : num_sms;
         return launch_pdl(kern, dim3(grid), dim3(NTHREADS), (size_t)C::SMEM_BYTES, s, mA, mB, mC, ga, sc);
     }
-    int clusters = std::min(num_sms / 2, max_clusters);
+    int clusters = std::min(num_sms / CL, max_clusters);
     if (sc.total < clusters) clusters = sc.total;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters);
+    cfg.gridDim = dim3(CL * clusters);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.x = CL;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -920,21 +985,26 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     // loads its own operand tiles)
     const int bn = a.symmetric ? (a.tile_n == 256 ? 256 : 128) : (a.tile_n == 128 ? 128 : 256);
     const bool pair = (bn == 256) && a.pair != 0;
+    const bool mc = pair && a.mc != 0;
     if (tf32) {
-        if (bn == 128) return tc::launch_impl<128, true, true, false>(a, num_sms, s);
-        return pair ? tc::launch_impl<256, true, true, true>(a, num_sms, s)
-                    : tc::launch_impl<256, true, true, false>(a, num_sms, s);
+        if (bn == 128) return tc::launch_impl<128, true, true, false, false>(a, num_sms, s);
+        if (!pair) return tc::launch_impl<256, true, true, false, false>(a, num_sms, s);
+        return mc ? tc::launch_impl<256, true, true, true, true>(a, num_sms, s)
+                  : tc::launch_impl<256, true, true, true, false>(a, num_sms, s);
     }
     if (bn == 128) {
-        return a.b_kmajor ? tc::launch_impl<128, true, false, false>(a, num_sms, s)
-                          : tc::launch_impl<128, false, false, false>(a, num_sms, s);
+        return a.b_kmajor ? tc::launch_impl<128, true, false, false, false>(a, num_sms, s)
+                          : tc::launch_impl<128, false, false, false, false>(a, num_sms, s);
     }
     if (pair) {
-        return a.b_kmajor ? tc::launch_impl<256, true, false, true>(a, num_sms, s)
-                          : tc::launch_impl<256, false, false, true>(a, num_sms, s);
+        if (mc)
+            return a.b_kmajor ? tc::launch_impl<256, true, false, true, true>(a, num_sms, s)
+                              : tc::launch_impl<256, false, false, true, true>(a, num_sms, s);
+        return a.b_kmajor ? tc::launch_impl<256, true, false, true, false>(a, num_sms, s)
+                          : tc::launch_impl<256, false, false, true, false>(a, num_sms, s);
     }
-    return a.b_kmajor ? tc::launch_impl<256, true, false, false>(a, num_sms, s)
-                      : tc::launch_impl<256, false, false, false>(a, num_sms, s);
+    return a.b_kmajor ? tc::launch_impl<256, true, false, false, false>(a, num_sms, s)
+                      : tc::launch_impl<256, false, false, false, false>(a, num_sms, s);
 }
 
 }  // namespace muon

@@ -73,6 +73,7 @@ struct GemmArgs {
     float lr, wd, scale;
     int tile_n;             // tensor-core tile N extent (128 or 256)
     int pair;               // tile_n 256 as 2-SM products on 2-CTA clusters: 0 off, otherwise on
+    int mc;                 // paired launches as 4-CTA clusters of two pairs sharing A by TMA multicast
     int tma_c;              // set by the launcher: 16-bit workspace output written by tile stores
     int* status;            // device status word
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd

@@ -67,6 +67,10 @@ GemmArgs gemm_base(int dtype, int* status) {
     // slower); MUON_PAIR=0 turns them off
     if (const char* f = std::getenv("MUON_PAIR")) a.pair = (f[0] == '1') ? 1 : 0;
     else a.pair = -1;
+    // paired products as 4-CTA clusters sharing the A rows by multicast;
+    // MUON_MC=0/1 overrides
+    if (const char* f = std::getenv("MUON_MC")) a.mc = (f[0] == '1') ? 1 : 0;
+    else a.mc = 0;
     a.status = status;
     a.b_kmajor = 1;
     return a;

@@ -169,8 +169,12 @@ def test_poly_tf32(mg):
 def test_paired_products(mg, monkeypatch, kind, M, N, K, batch):
     """128 x 256 tiles run as 2-SM products on 2-CTA clusters (row blocks 2p
     and 2p+1; each CTA loads its own A rows and its half of the B tile; an odd
-    last block reads zeros and stores nothing).  Same tiles and K order as the unpaired kernel, so the results
-    are bitwise equal to it, and they match the fp64 product."""
+    last block reads zeros and stores nothing), and, with MUON_MC=1, as 4-CTA
+    clusters of two pairs on tiles that share their A rows, each A row loaded
+    once per cluster by TMA multicast (an odd tile count leaves one pair
+    repeating its partner's tile without storing it).  Same tiles and K order
+    as the unpaired kernel, so all three results are bitwise equal, and they
+    match the fp64 product."""
     tf32 = kind.startswith("tf32")
     dtype = torch.float32 if tf32 else torch.bfloat16
     sym = kind in ("sym", "tf32sym")
@@ -178,14 +182,16 @@ def test_paired_products(mg, monkeypatch, kind, M, N, K, batch):
     A = _rand((batch, M, K), dtype, 21, scale=1.0 / np.sqrt(K))
     B = A if sym else (_rand((batch, N, K), dtype, 22) if kmajor else _rand((batch, K, N), dtype, 23))
     out = []
-    for pair in ("0", "1"):
+    for pair, mc in (("0", "0"), ("1", "0"), ("1", "1")):
         monkeypatch.setenv("MUON_PAIR", pair)
+        monkeypatch.setenv("MUON_MC", mc)
         C = torch.full((batch, M, N), float("nan"), dtype=dtype, device="cuda")
         mg.muon_debug_gemm(A, B, C, b_kmajor=kmajor, symmetric=sym, tile_n=256, tf32=tf32)
         torch.cuda.synchronize()
         assert mg.muon_sync_status() == mg.MUON_OK
         out.append(C)
     assert torch.equal(out[0], out[1])
+    assert torch.equal(out[0], out[2])
     Bt = B.double().transpose(1, 2) if kmajor else B.double()
     ref = torch.matmul(A.double(), Bt)
     if tf32:
