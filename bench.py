@@ -730,6 +730,18 @@ def bench_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     # the optimizer object of a training loop: registered once, stepped many times
     group = mg.MuonGroup(params, grads, moms)
+    # pinned host buffers of the end-to-end pass, allocated now and cycled
+    # through untimed copies: freshly pinned buffers are read more slowly over
+    # NVLink-C2C on their first passes (7B stack, 14 GB of gradients: 180,
+    # then 122, then a steady 67 ms), and a training loop reuses its buffers
+    host_g = [g.cpu().pin_memory() for g in grads]
+    host_w = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
+    for _ in range(3):
+        for dg, hg in zip(grads, host_g):
+            dg.copy_(hg, non_blocking=True)
+        for hw, p in zip(host_w, params):
+            hw.copy_(p, non_blocking=True)
+    torch.cuda.synchronize()
     dtype_code = {"bf16": mg.MUON_BF16, "f16": mg.MUON_F16, "f32": mg.MUON_F32}[wl.param_dtype]
 
     # warm-up (the first step autotunes every distinct shape)
@@ -791,14 +803,8 @@ def bench_gpu(args):
     # from pinned host memory and every updated weight out to pinned host
     # memory inside each step (muon_group_set_host_io), chunk by chunk on its
     # copy streams, overlapping the update of the other chunks
-    host_g = [g.cpu().pin_memory() for g in grads]
-    host_w = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
     group.set_host_io(host_g, host_w)
-    # untimed: the first step captures the step with its copies; the host
-    # buffers' first passes over NVLink-C2C are slower (measured on the 7B
-    # stack: 14 GB of gradients in 180, 122, then a steady 67 ms), so the
-    # warm-up reaches the steady state a training loop runs in
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, args.warmup)):  # untimed: the first captures the step with its copies
         group.step(**hp)
     e2e_steps = max(3, min(args.steps, 20))
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]

@@ -120,11 +120,35 @@ static int group_io_events(muon_group* g) {
     return MUON_OK;
 }
 
+// With host I/O, only the first unit's gradients and the last unit's
+// parameters cross NVLink-C2C while no unit computes: the smallest unit (in
+// parameter bytes) goes first and the next smallest last, the rest keep
+// their order.  Units are independent, so the results do not change.
+static void order_for_io(const muon_group* g, std::vector<GroupUnit>& units) {
+    if (units.size() < 3) return;
+    std::vector<size_t> bytes(units.size(), 0);
+    for (size_t i = 0; i < units.size(); ++i)
+        for (const auto& rg : units[i].ranges)
+            for (int64_t e = rg.first; e < rg.first + rg.second; ++e) bytes[i] += g->entry_bytes[(size_t)e];
+    std::vector<size_t> idx(units.size());
+    for (size_t i = 0; i < idx.size(); ++i) idx[i] = i;
+    std::stable_sort(idx.begin(), idx.end(), [&](size_t x, size_t y) { return bytes[x] < bytes[y]; });
+    const size_t first = idx[0], last = idx[1];
+    std::vector<GroupUnit> out;
+    out.reserve(units.size());
+    out.push_back(units[first]);
+    for (size_t i = 0; i < units.size(); ++i)
+        if (i != first && i != last) out.push_back(units[i]);
+    out.push_back(units[last]);
+    units.swap(out);
+}
+
 static int group_enqueue(muon_group* g, cudaStream_t s) {
     NvtxRange nvr("muon_group_step");
     int r;
-    const std::vector<GroupUnit> units = group_units(g);
+    std::vector<GroupUnit> units = group_units(g);
     const bool cin = !g->host_g.empty(), cout = !g->host_p.empty();
+    if (cin || cout) order_for_io(g, units);
     if (!cin && !cout) {
         for (const GroupUnit& u : units)
             if ((r = group_run_unit(g, u, s))) return r;
