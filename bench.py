@@ -730,18 +730,6 @@ def bench_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     # the optimizer object of a training loop: registered once, stepped many times
     group = mg.MuonGroup(params, grads, moms)
-    # pinned host buffers of the end-to-end pass, allocated now and cycled
-    # through untimed copies: freshly pinned buffers are read more slowly over
-    # NVLink-C2C on their first passes (7B stack, 14 GB of gradients: 180,
-    # then 122, then a steady 67 ms), and a training loop reuses its buffers
-    host_g = [g.cpu().pin_memory() for g in grads]
-    host_w = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
-    for _ in range(3):
-        for dg, hg in zip(grads, host_g):
-            dg.copy_(hg, non_blocking=True)
-        for hw, p in zip(host_w, params):
-            hw.copy_(p, non_blocking=True)
-    torch.cuda.synchronize()
     dtype_code = {"bf16": mg.MUON_BF16, "f16": mg.MUON_F16, "f32": mg.MUON_F32}[wl.param_dtype]
 
     # warm-up (the first step autotunes every distinct shape)
@@ -803,6 +791,8 @@ def bench_gpu(args):
     # from pinned host memory and every updated weight out to pinned host
     # memory inside each step (muon_group_set_host_io), chunk by chunk on its
     # copy streams, overlapping the update of the other chunks
+    host_g = [g.cpu().pin_memory() for g in grads]
+    host_w = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
     group.set_host_io(host_g, host_w)
     for _ in range(max(3, args.warmup)):  # untimed: the first captures the step with its copies
         group.step(**hp)
@@ -814,6 +804,8 @@ def bench_gpu(args):
         eev[i][0].record()
         group.step(**hp)
         eev[i][1].record()
+        # a training loop reads its updated weights before the next step
+        eev[i][1].synchronize()
     torch.cuda.synchronize()
     group.set_host_io(None, None)
     e2e_ms = combine_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / e2e_steps, dist, device)
