@@ -82,7 +82,8 @@ struct GemmArgs {
 
 // Launchers (return the CUDA error of the launch).
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_simt(const GemmArgs& a, int num_sms, cudaStream_t s);
+int simt_split(int64_t tiles, int K, int num_sms);
 
 // Momentum (+Nesterov) or plain copy, orientation and Frobenius partial sums.
 struct PrepArgs {

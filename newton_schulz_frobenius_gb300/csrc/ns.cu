@@ -84,7 +84,7 @@ int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
     GemmArgs ga = a;
     if (tc) ga.stall = take_stall(STALL_PRODUCT);
     note_launch_begin(kc, s);
-    cudaError_t e = tc ? launch_gemm_tc(ga, dc.sms, s) : launch_gemm_simt(a, s);
+    cudaError_t e = tc ? launch_gemm_tc(ga, dc.sms, s) : launch_gemm_simt(a, dc.sms, s);
     note_launch_end(kc, work, s);
     if (e != cudaSuccess) return cuda_fail(e, "product launch");
     return MUON_OK;
