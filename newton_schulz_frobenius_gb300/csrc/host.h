@@ -102,6 +102,8 @@ struct ChunkLayout {
     int64_t ldx, ldm;
     size_t x_bytes, m_bytes;            // one matrix
     size_t off_X, off_X2, off_G, off_S[3], off_inv, off_part, total;
+    size_t off_SA, off_SB;              // fp32 on the TF32 tensor path: split operands
+    int tf32x3;                         // fp32 products as three TF32 passes (else FFMA)
     int nparts;
 };
 
@@ -153,6 +155,7 @@ inline size_t esize(int dtype) { return is_half(dtype) ? 2 : 4; }
 // products) or U already divided by its norm (the fp16 path).
 inline bool x_holds_u(int x_dtype) { return x_dtype != MUON_F16; }
 inline int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
+inline int64_t pad4(int64_t x) { return (x + 3) / 4 * 4; }
 inline bool valid_dtype(int d) { return d == MUON_F32 || d == MUON_BF16 || d == MUON_F16; }
 // Working precision of NS for parameters of this storage type: fp32 stays
 // fp32; 16-bit parameters use the configured 16-bit type, by default their own.
@@ -186,7 +189,8 @@ int gram_space_tf32(int path, int m, int n);
 NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_segs, int path, int tile_n,
                  int m, int n, int sym_tile_n = 128, int sym_dense = 0);
 GemmArgs gemm_base(int dtype, int* status);
-int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass);
+// work_k: the contraction length the recorded work counts (0: a.K)
+int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass, int64_t work_k = 0);
 ChunkLayout chunk_layout(int m, int n, int B, int dtype);
 int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
            int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin);

@@ -85,6 +85,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_simt(const GemmArgs& a, int num_sms, cudaStream_t s);
 int simt_split(int64_t tiles, int K, int num_sms);
 
+// fp32 operand split for three-pass TF32 products (tf32x3.cu): per batch
+// index, dst row r = [hi | hi | lo] (SPLIT_HHL) or [hi | lo | hi] (SPLIT_HLH)
+// of source row r, each third Kp >= K wide (Kp % 4 == 0, zero beyond K).
+// transposed: the source is K x rows with rows contiguous (leading dim ld_src).
+enum SplitOrder : int { SPLIT_HHL = 0, SPLIT_HLH = 1 };
+struct SplitArgs {
+    const void* src; int64_t ld_src; int64_t stride_src;
+    int rows, K;
+    int64_t Kp;
+    int transposed;
+    int order;
+    float* dst; int64_t stride_dst;   // rows x 3 Kp per batch index
+    int batch;
+};
+cudaError_t launch_tf32_split(const SplitArgs& p, int num_sms, cudaStream_t s);
+
 // Momentum (+Nesterov) or plain copy, orientation and Frobenius partial sums.
 struct PrepArgs {
     const MatEntry* mats;   // device table, one entry per batch index

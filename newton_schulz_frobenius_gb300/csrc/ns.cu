@@ -76,8 +76,16 @@ GemmArgs gemm_base(int dtype, int* status) {
     return a;
 }
 
-int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
-    const double mnk = (double)a.M * a.N * a.K * a.batch;
+// fp32 products on the TF32 tensor path as three passes (tf32x3.cu) instead
+// of FFMA: MUON_FP32_TC=1.  Measured slower than the split-K FFMA products at
+// the fp32 workload's sizes, so off by default.
+int fp32_tc_enabled() {
+    const char* f = std::getenv("MUON_FP32_TC");
+    return (f && f[0] == '1') ? 1 : 0;
+}
+
+int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass, int64_t work_k) {
+    const double mnk = (double)a.M * a.N * (double)(work_k > 0 ? work_k : a.K) * a.batch;
     const double work = a.symmetric ? mnk : 2.0 * mnk;
     const bool tc = (is_half(a.dtype) || a.dtype == DT_TF32);
     const int kc = tc ? kclass : KC_SIMT;
@@ -88,6 +96,36 @@ int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass) {
     note_launch_end(kc, work, s);
     if (e != cudaSuccess) return cuda_fail(e, "product launch");
     return MUON_OK;
+}
+
+// An fp32 product as one TF32 tensor-core product over K' = 3 Kp: A' = [hi |
+// hi | lo] of A's rows, B' = [hi | lo | hi] of op(B)'s columns (tf32x3.cu),
+// written to SA and SB; the epilogue is the fp32 product's own.
+int run_gemm_tf32x3(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass, float* SA, float* SB) {
+    const int64_t Kp = pad4(a.K), K3 = 3 * Kp;
+    SplitArgs sa;
+    std::memset(&sa, 0, sizeof sa);
+    sa.src = a.A; sa.ld_src = a.lda; sa.stride_src = a.strideA;
+    sa.rows = a.M; sa.K = a.K; sa.Kp = Kp; sa.transposed = 0; sa.order = SPLIT_HHL;
+    sa.dst = SA; sa.stride_dst = (int64_t)a.M * K3; sa.batch = a.batch;
+    SplitArgs sb = sa;
+    sb.src = a.B; sb.ld_src = a.ldb; sb.stride_src = a.strideB;
+    sb.rows = a.N; sb.transposed = a.b_kmajor ? 0 : 1; sb.order = SPLIT_HLH;
+    sb.dst = SB; sb.stride_dst = (int64_t)a.N * K3;
+    for (const SplitArgs* sp : {&sa, &sb}) {
+        note_launch_begin(KC_OTHER, s);
+        cudaError_t e = launch_tf32_split(*sp, dc.sms, s);
+        note_launch_end(KC_OTHER, 0.0, s);
+        if (e != cudaSuccess) return cuda_fail(e, "operand split launch");
+    }
+    GemmArgs t = a;
+    t.dtype = DT_TF32;
+    t.A = SA; t.lda = K3; t.strideA = (int64_t)a.M * K3;
+    t.B = SB; t.ldb = K3; t.strideB = (int64_t)a.N * K3; t.b_kmajor = 1;
+    t.K = (int)K3;
+    t.c_dtype = MUON_F32;
+    t.round_tf32 = 0;
+    return run_gemm(dc, s, t, kclass, a.K);   // work counted on the fp32 product's K
 }
 
 // X is stored in the path's dtype; the m x m Gram-space matrices are fp32 on
@@ -112,6 +150,17 @@ ChunkLayout chunk_layout(int m, int n, int B, int dtype) {
     for (int i = 0; i < 3; ++i) L.off_S[i] = take(L.m_bytes * B);
     L.off_inv = take(sizeof(float) * B);
     L.off_part = take(sizeof(float) * (size_t)L.nparts * B);
+    L.tf32x3 = (dtype == MUON_F32) ? fp32_tc_enabled() : 0;
+    L.off_SA = L.off_SB = 0;
+    if (L.tf32x3) {
+        // XX^T: m x 3 pad4(n) both; Gram-space products m x 3 pad4(m) both;
+        // QX: A' m x 3 pad4(m), B' n x 3 pad4(m)
+        const size_t pm = (size_t)pad4(m), pn = (size_t)pad4(n);
+        const size_t sa = 3 * sizeof(float) * std::max((size_t)m * pn, (size_t)m * pm);
+        const size_t sb = 3 * sizeof(float) * std::max({(size_t)m * pn, (size_t)m * pm, (size_t)n * pm});
+        L.off_SA = take(sa * B);
+        L.off_SB = take(sb * B);
+    }
     L.total = o;
     return L;
 }
@@ -160,6 +209,15 @@ int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, i
         return g;
     };
 
+    // every product of the iteration; fp32 ones on the three-pass TF32 path
+    // when the layout holds its split operands
+    auto product = [&](const GemmArgs& g, int kclass) {
+        if (L.tf32x3 && g.dtype == MUON_F32)
+            return run_gemm_tf32x3(dc, s, g, kclass, reinterpret_cast<float*>(base + L.off_SA),
+                                   reinterpret_cast<float*>(base + L.off_SB));
+        return run_gemm(dc, s, g, kclass);
+    };
+
     const int nseg = (int)plan.segs.size();
     for (int si = 0; si < nseg; ++si) {
         const int Lseg = plan.segs[si];
@@ -178,7 +236,7 @@ int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, i
             g.tile_n = plan.sym_tile_n;
             gram_out(g, false);
             if (first && use_inv) { g.alpha_vec = inv; g.alpha_sq = 1; }
-            int r = run_gemm(dc, s, g, KC_SYRK);
+            int r = product(g, KC_SYRK);
             if (r) return r;
         }
 
@@ -197,23 +255,23 @@ int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, i
                 g.epi = EPI_POLY;
                 g.Gin = G; g.ldg = L.ldm; g.strideG = strideM;
                 g.pa = plan.a; g.pb = plan.b; g.pc = plan.c;
-                int r = run_gemm(dc, s, g, KC_SQUARE);
+                int r = product(g, KC_SQUARE);
                 if (r) return r;
             }
             if (j == 1) {
                 q = p;
             } else {
                 const int qn = grab();     // Q <- P Q
-                int r = run_gemm(dc, s, sym(S[p], S[q], S[qn], j == Lseg), KC_SQUARE);
+                int r = product(sym(S[p], S[q], S[qn], j == Lseg), KC_SQUARE);
                 if (r) return r;
                 used[q] = false;
                 q = qn;
             }
             if (j < Lseg) {
                 const int t = grab();      // G <- (P G) P
-                int r = run_gemm(dc, s, sym(S[p], G, S[t], false), KC_SQUARE);
+                int r = product(sym(S[p], G, S[t], false), KC_SQUARE);
                 if (r) return r;
-                r = run_gemm(dc, s, sym(S[t], S[p], G, false), KC_SQUARE);
+                r = product(sym(S[t], S[p], G, false), KC_SQUARE);
                 if (r) return r;
                 used[t] = false;
             }
@@ -239,7 +297,7 @@ int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, i
             g.hyper = fin.hyper;
             if (fin.kind == EPI_UPDATE) kc = KC_APPLY_UPDATE;
         }
-        int r = run_gemm(dc, s, g, kc);
+        int r = product(g, kc);
         if (r) return r;
         std::swap(X, Xn);
     }
