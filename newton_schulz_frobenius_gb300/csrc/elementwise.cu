@@ -18,6 +18,8 @@
 #include "muon_internal.cuh"
 #include "epilogue.cuh"
 
+#include <algorithm>
+
 namespace muon {
 
 namespace {
@@ -254,10 +256,14 @@ int prep_grid_parts(int m, int n, int batch) {
     // short enough that the last wave of a launch stays small.  Measured
     // against the earlier rule of about 2048 CTAs per launch: the 2560x9728
     // prologue 0.57 -> 0.60 of the HBM copy rate, the 7B stack's 0.76 -> 0.79.
+    // Launches of fewer than 8 x 760 tiles take fewer tiles per CTA, down to
+    // one, so that they still spread over the SMs: one 256x1024 fp32 matrix
+    // (64 tiles) ran on 8 CTAs in 28 us.
     const int t = prep_tiles(m, n);
     const int64_t total = (int64_t)t * batch;
-    const int tpc = total >= (int64_t)16 * 760 * 8 ? 16 : 8;
-    return (t + tpc - 1) / tpc;
+    int64_t tpc = total >= (int64_t)16 * 760 * 8 ? 16 : 8;
+    if (total < (int64_t)8 * 760) tpc = std::max<int64_t>(1, total / 760);
+    return (int)((t + tpc - 1) / tpc);
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {

@@ -94,6 +94,8 @@ gemm_simt_kernel(const __grid_constant__ GemmArgs a, int tiles_m, int split, int
     __shared__ __align__(16) float As[SK][ST + 4];
     __shared__ __align__(16) float Bs[SK][ST + 4];
 
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     const int q = blockIdx.x % split;         // this CTA's k-range (its rank in the cluster)
     const int tile = blockIdx.x / split;
@@ -206,13 +208,15 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, int num_sms, cudaStream_t s) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = split;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, a, tiles_m, split, kc);
 }
 
