@@ -578,11 +578,14 @@ __device__ bool process(const SmallArgs& a, const SmallBucket& bk, int b, const 
         for (int i = tid; i < nck * (XCH / 16); i += NT) reinterpret_cast<uint4*>(X)[i] = make_uint4(0, 0, 0, 0);
         __syncthreads();
     }
-    if (a.mode == 0) {
+    // W is pulled into L2 as the last segment starts, so that it is still
+    // there when the write-out reads it
+    auto prefetch_w = [&]() {
+        if (a.mode != 0) return;
         const int64_t wbytes = (int64_t)bk.m * bk.n * 2;
         for (int64_t off = (int64_t)tid * 128; off < wbytes; off += (int64_t)NT * 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(e.w) + off));
-    }
+    };
     float ss = prologue<ROWS>(a, bk, e, X, S0, c.stream, ok);
     if (!ok) return false;
     // while this matrix iterates, pull the next one's inputs into L2
@@ -613,6 +616,7 @@ __device__ bool process(const SmallArgs& a, const SmallBucket& bk, int b, const 
             const int L = bk.segs[si];
             const bool first = (si == 0), last = (si == bk.nseg - 1);
             const float gs = first ? inv * inv : 1.0f;
+            if (last) prefetch_w();
             auto square = [&](const uint8_t* A, const uint8_t* B, uint32_t col) {
                 return run([&] {
                     for (int s = 0; s < 8; ++s) tc_mma(tmem + col, ks(A, s), ks(B, s), ID_SQ, s > 0 ? 1u : 0u);
@@ -662,6 +666,7 @@ __device__ bool process(const SmallArgs& a, const SmallBucket& bk, int b, const 
         for (int it = 0; it < bk.nseg && ok; ++it) {
             const bool first = (it == 0), last = (it == bk.nseg - 1);
             const float gs = first ? inv * inv : 1.0f;
+            if (last) prefetch_w();
             // A = X X^T: A00 -> TMEM [0, 128); rows 128.. (A10 | A11) -> [128, 384)
             ok = run([&] {
                 for (int s = 0; s < nck * 4; ++s) {

@@ -286,6 +286,22 @@ def test_fused_many_matrices_per_cta(mg, monkeypatch):
         assert m_ok
 
 
+def test_fused_mixed_orientations_many_per_cta(mg, monkeypatch):
+    """Wide and tall matrices of one oriented shape in the same bucket (the
+    tall ones read and write the caller's transposed layout), both kernel
+    forms and a 384-column shape in one launch, several matrices per CTA;
+    then the ortho output (O written instead of a W update) for 400 matrices
+    on 152 CTAs."""
+    monkeypatch.setenv("MUON_SMALL", "1")
+    shapes = [(128, 512), (512, 128), (256, 256), (128, 384)] * 60
+    for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", "bf16", mg.MUON_PATH_AUTO, False, 8600, 0.0316):
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+    f, s = _ortho_case(mg, 128, 512, 400, "bf16", (2, 2, 1), 8700)
+    assert f <= TOL["bf16"], f
+    assert s <= SIGMA_TOL
+
+
 @pytest.mark.parametrize("mom_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("small", ["0", "1"])
 def test_degenerate_shapes_step(mg, monkeypatch, small, mom_dtype):
