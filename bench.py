@@ -799,6 +799,10 @@ def bench_gpu(args):
     e2e_steps = max(3, min(args.steps, 20))
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     torch.cuda.synchronize()
+    # the host copies draw power too: the clocks of this pass are reported with it
+    e2e_sampler = ClockSampler(local)
+    e2e_sampler.start()
+    time.sleep(0.3)
     for i in range(e2e_steps):
         flush.zero_()
         eev[i][0].record()
@@ -807,6 +811,7 @@ def bench_gpu(args):
         # a training loop reads its updated weights before the next step
         eev[i][1].synchronize()
     torch.cuda.synchronize()
+    e2e_clocks = e2e_sampler.stop()
     group.set_host_io(None, None)
     e2e_ms = combine_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / e2e_steps, dist, device)
     h2d = sum(g.numel() * g.element_size() for g in grads)
@@ -877,7 +882,8 @@ def bench_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "what": "muon_group_step with host I/O: every gradient copied in from pinned host memory and "
                         "every updated weight copied out to pinned host memory inside each step, overlapped "
-                        "chunk by chunk with the update"},
+                        "chunk by chunk with the update",
+                "clocks": e2e_clocks},
         "gpu_launches": launches,
         "clocks": clocks,
     }
