@@ -63,10 +63,14 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;   // paired: this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (PAIR || BN == 128) ? (MIR ? 6 : 7) : 4;
+    static constexpr int STAGES = (PAIR || BN == 128) ? (MIR ? 5 : 7) : 4;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int MIRROR_BYTES = MIR ? NEPI * 32 * 33 * 4 : 0;   // per epilogue warp: one 32 x 33 fp32 chunk
+    // per epilogue warp: one 32 x 33 fp32 chunk (staged stores), or 4 KB
+    // tile-store buffers used in turn, two where they fit
+    static constexpr int STORE_BUFS = (STAGES * STAGE_BYTES + NEPI * 8192 + 2048 <= 232448) ? 2 : 1;
+    static constexpr int MIRROR_WARP_BYTES = STORE_BUFS == 2 ? 8192 : 32 * 33 * 4;
+    static constexpr int MIRROR_BYTES = MIR ? NEPI * MIRROR_WARP_BYTES : 0;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + MIRROR_BYTES + NUM_BARS * 8 + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -179,6 +183,8 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared-memory sources of this thread's stores may be overwritten
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the most recent bulk-store group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // this thread's stores are complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -435,16 +441,18 @@ struct TileSched {
 };
 
 // 16-bit workspace products (EPI_STORE / EPI_POLY): one warp's 32 x 32 chunk
-// (rows r0 + lane, columns c0..) is converted into the warp's staging area
-// (4 KB: the chunk, then its transpose, 64-byte rows) and leaves as tile stores
-// on the copy engine, so the warp issues two instructions instead of sixteen
-// row-piece stores.  Symmetric products: a chunk below the diagonal is stored
+// (rows r0 + lane, columns c0..) is converted into one of the warp's two
+// staging buffers (4 KB each: the chunk, then its transpose, 64-byte rows;
+// chunks alternate between them, so one chunk's stores read shared memory
+// while the next is converted) and leaves as tile stores on the copy engine,
+// so the warp issues two instructions instead of sixteen row-piece stores.  Symmetric products: a chunk below the diagonal is stored
 // at (r0, c0) and transposed at (c0, r0); the diagonal chunk (c0 == r0) is
 // assembled symmetric (rows c <= r from v, the rest mirrored) and stored once,
 // so no element is written twice.  The stores clip at the matrix edge.
+template <int NB>
 __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorMap* tmC, int b, int r0, int c0,
-                                              float (&v)[32], float s, const float (&g)[32], uint8_t* stg,
-                                              bool& pending) {
+                                              float (&v)[32], float s, const float (&g)[32], uint8_t* stg2,
+                                              int& groups) {
     const int lane = threadIdx.x & 31;
     const int r = r0 + lane;
 #pragma unroll
@@ -454,10 +462,14 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
         for (int j = 0; j < 32; ++j) v[j] = a.pc * v[j] + a.pb * g[j] + ((c0 + j) == r ? a.pa : 0.f);
     }
     const bool f16 = (a.c_dtype == MUON_F16);
-    if (pending) {              // the previous chunk's stores have read the staging
-        if (lane == 0) bulk_wait_read0();
+    if (groups >= NB) {         // the stores that last used this buffer have read it
+        if (lane == 0) {
+            if (NB == 2) bulk_wait_read1();
+            else bulk_wait_read0();
+        }
         __syncwarp();
     }
+    uint8_t* stg = stg2 + (groups % NB) * 4096;
     uint8_t* nrm = stg;
     uint8_t* trn = stg + 2048;
 #pragma unroll
@@ -483,7 +495,7 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
         if (below) tma_store_3d(tmC, smem_u32(trn), r0, c0, b);
         bulk_commit();
     }
-    pending = true;
+    ++groups;
 }
 
 // ---------------------------------------------------------------------------
@@ -730,10 +742,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else {
         // ---------------- epilogue (warps 2..9) ----------------
         const int q = warp & 3;                    // TMEM lane quarter this warp may access
-        float (*mstage)[33] = reinterpret_cast<float (*)[33]>(mirror_stage + (warp - 2) * 32 * 33);
+        float (*mstage)[33] =
+            reinterpret_cast<float (*)[33]>(mirror_stage + (warp - 2) * (C::MIRROR_WARP_BYTES / 4));
         const int half = (warp - 2) / 4;           // which half of the tile's columns
         constexpr int HALF_COLS = BN / 2;
-        bool tma_pending = false;                  // this warp's bulk stores may still read its staging
+        int tma_groups = 0;                        // bulk-store groups this warp has issued
         int acc = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < sched.total; t += ustep) {
@@ -784,8 +797,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
                 if (B_KMAJOR && args.tma_c) {
                     // 16-bit workspace products: the chunk (and its mirror) leave on the copy engine
-                    epi_store_tma(args, &tmC, b, row0, col0, v, scale, gcur,
-                                  reinterpret_cast<uint8_t*>(&mstage[0][0]), tma_pending);
+                    epi_store_tma<C::STORE_BUFS>(args, &tmC, b, row0, col0, v, scale, gcur,
+                                  reinterpret_cast<uint8_t*>(&mstage[0][0]), tma_groups);
                 } else if (B_KMAJOR && (args.epi == EPI_STORE || args.epi == EPI_POLY)) {
                     // workspace products: rows and mirrored rows through the staging area
                     epi_store_staged(args, b, row0, col0, v, scale, gcur, mstage);
@@ -806,7 +819,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
-        if (tma_pending && lane == 0) bulk_wait0();    // the stores are complete before the CTA exits
+        if (tma_groups > 0 && lane == 0) bulk_wait0();   // the stores are complete before the CTA exits
         __syncwarp();
     }
 
