@@ -52,13 +52,15 @@ __device__ __forceinline__ float4 ld_cluster_f4(const void* local, uint32_t rank
 }
 
 // Four consecutive fp32 values at p[0..3] of a row with `valid` elements left
-// (zero beyond); one 16-byte load when all four exist and vec allows it.
+// (zero beyond); one 16-byte load when all four exist and vec allows it,
+// else one load per element.
 __device__ __forceinline__ float4 load4(const float* p, int valid, bool vec) {
     if (vec && valid >= 4) return __ldg(reinterpret_cast<const float4*>(p));
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid > 0) v.x = __ldg(p);
     if (valid > 1) v.y = __ldg(p + 1);
     if (valid > 2) v.z = __ldg(p + 2);
+    if (valid > 3) v.w = __ldg(p + 3);
     return v;
 }
 

@@ -63,6 +63,35 @@ def test_product_mn_major(mg, dtype, M, N, K, batch, tile):
     _check(C, ref, dtype)
 
 
+@pytest.mark.parametrize("kmajor", [True, False])
+@pytest.mark.parametrize("M,N,K,batch", [(64, 64, 1000, 1), (128, 192, 520, 1), (100, 70, 776, 2), (256, 1024, 256, 1),
+                                          (72, 90, 1001, 1)])
+def test_fp32_split_k(mg, kmajor, M, N, K, batch):
+    """fp32 products with few output tiles split K over clusters of CTAs
+    (ragged k-ranges, 16-byte and scalar loads); the partial tiles are added
+    in a fixed order, so two runs agree bit for bit."""
+    A = _rand((batch, M, K), torch.float32, 21)
+    B = _rand((batch, N, K) if kmajor else (batch, K, N), torch.float32, 22)
+    C = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    mg.muon_debug_gemm(A, B, C, b_kmajor=kmajor)
+    C2 = torch.zeros_like(C)
+    mg.muon_debug_gemm(A, B, C2, b_kmajor=kmajor)
+    torch.cuda.synchronize()
+    assert mg.muon_sync_status() == mg.MUON_OK
+    assert torch.equal(C, C2)
+    Bd = B.double().transpose(1, 2) if kmajor else B.double()
+    _check(C, torch.matmul(A.double(), Bd), torch.float32)
+
+
+def test_fp32_split_k_symmetric(mg):
+    X = _rand((1, 96, 1000), torch.float32, 23)
+    C = torch.full((1, 96, 96), float("nan"), dtype=torch.float32, device="cuda")
+    mg.muon_debug_gemm(X, X, C, b_kmajor=True, symmetric=True)
+    torch.cuda.synchronize()
+    assert torch.equal(C, C.transpose(1, 2))
+    _check(C, torch.matmul(X.double(), X.double().transpose(1, 2)), torch.float32)
+
+
 @pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("m,k,batch", [(128, 64, 1), (260, 1000, 2), (512, 384, 1), (37, 200, 3), (896, 136, 1)])
