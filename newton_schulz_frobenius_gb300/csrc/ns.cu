@@ -31,8 +31,9 @@ int validate_segments(int steps, const int* segs, int nseg) {
 // for the Gram path with bf16 Gram space, 0.8-1.2% relative error on every
 // shape with m >= 128 and n >= 2m, but 1.5-4% on square and near-square shapes
 // and 2.3% for m = 37; with TF32 Gram space all of them stay at or below 1.5%.
-// The plain path's error is set by the bf16 X (0.8-1.9% either way), so it
-// keeps bf16.  TF32 costs twice the operand bytes and half the tensor rate on
+// The plain path's error is set by the bf16 X (0.8-1.9% either way from 64
+// rows up; below that up to 4%, so the automatic choice takes the Gram path
+// there, see choose_plan), so it keeps bf16 Gram space.  TF32 costs twice the operand bytes and half the tensor rate on
 // the m^3 products, so it is used only where bf16 is not accurate enough.
 int gram_space_tf32(int path, int m, int n) {
     return (path == MUON_PATH_GRAM && (m < 128 || n < 2 * m)) ? 1 : 0;

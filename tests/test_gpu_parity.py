@@ -286,6 +286,17 @@ def test_fused_many_matrices_per_cta(mg, monkeypatch):
         assert m_ok
 
 
+def test_auto_path_few_rows_bf16(mg):
+    """With bf16 X and fewer than 64 rows the automatic path choice takes the
+    Gram path (the plain iteration errs by up to 4 % there), and the update
+    meets the bf16 bar: matrices with 3, 4 and 32 rows in both orientations."""
+    shapes = [(4, 549), (549, 4), (3, 168), (32, 1000), (1000, 32)]
+    for err, q, m_ok, pname in _step_case(mg, shapes, "bf16", "bf16", mg.MUON_PATH_AUTO, True, 9400, 0.02):
+        assert pname == "gram"
+        assert err <= TOL["bf16"] + q, (err, q)
+        assert m_ok
+
+
 def test_fused_mixed_orientations_many_per_cta(mg, monkeypatch):
     """Wide and tall matrices of one oriented shape in the same bucket (the
     tall ones read and write the caller's transposed layout), both kernel

@@ -81,6 +81,16 @@ def test_plain_gains_nothing_from_tf32():
     assert e_b < 0.02 and abs(e_b - e_t) < 0.2 * e_b
 
 
+@pytest.mark.parametrize("shape", [(4, 549), (3, 168), (32, 1000)])
+def test_bf16_plain_with_few_rows_misses_the_bar(shape):
+    """Below 64 rows the bf16 plain iteration can miss the 2% bar (nearly
+    equal singular values make the five bf16 transforms' errors add up),
+    where the Gram path with TF32 Gram space meets it; the automatic path
+    choice takes Gram there."""
+    assert _err(shape, (1, 1, 1, 1, 1), bf16) > 0.02
+    assert _err(shape, (2, 2, 1), tf32) < 0.02
+
+
 def test_polynomial_needs_one_rounded_g():
     assert _err((1, 64), (1, 1, 1, 1, 1), bf16, lin_fp32=True) > 2 * _err((1, 64), (1, 1, 1, 1, 1), bf16)
 
