@@ -7,8 +7,10 @@ import random
 
 import pytest
 
-from tests.gpu_util import TOL
+from oracle import muon_oracle as orc
+from tests.gpu_util import TOL, rel_fro, to_device, to_f64
 from tests.test_gpu_parity import _step_case
+from workloads import gen_matrix
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -34,7 +36,7 @@ def _shapes(rng, k):
     return out
 
 
-@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("seed", range(10))
 def test_random_steps(mg, monkeypatch, seed):
     rng = random.Random(7000 + seed)
     dtype = rng.choice(["bf16", "bf16", "f32"])
@@ -50,3 +52,28 @@ def test_random_steps(mg, monkeypatch, seed):
     for err, q, m_ok, pname in _step_case(mg, shapes, dtype, mom, path, nesterov, 9000 + 100 * seed, 0.02):
         assert err <= TOL[dtype] + q, (seed, shapes, dtype, mom, pname, err, q)
         assert m_ok, (seed, shapes)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_orthogonalize(mg, monkeypatch, seed):
+    """muon_ns_orthogonalize with random shapes, batches, step counts and
+    segment lists (plain NS, 2+2+1, 2+3, 3+2, 2+1+2, one segment of 5) in
+    bf16, fp16 and fp32."""
+    rng = random.Random(8000 + seed)
+    dtype = rng.choice(["bf16", "f16", "f32"])
+    segs = rng.choice([None, (2, 2, 1), (2, 3), (3, 2), (1, 1, 1, 1, 1), (5,), (2, 1, 2)])
+    steps = sum(segs) if segs else rng.choice([4, 5, 6])
+    r, c = rng.randint(1, 600), rng.randint(1, 600)
+    if segs is None and dtype == "bf16":
+        r, c = max(r, 64), max(c, 64)        # forced plain bf16 below 64 rows: outside the bar by design
+    batch = rng.choice([1, 2, 3])
+    monkeypatch.setenv("MUON_SMALL", rng.choice(["0", "1"]))
+    mats = [gen_matrix(8800 + seed * 10 + b, 0, r, c, 1.0, dtype) for b in range(batch)]
+    x = torch.stack([to_device(h, torch) for h in mats]).contiguous()
+    mg.muon_ns_orthogonalize(x, mg.QUINTIC, steps, segs)
+    assert mg.muon_sync_status() == mg.MUON_OK
+    for b, h in enumerate(mats):
+        ref = orc.orthogonalize(orc.to_f64(h.data, dtype), "gram" if segs else "plain", steps=steps,
+                                segments=segs or (2, 2, 1))
+        err = rel_fro(to_f64(x[b]), ref)
+        assert err <= TOL[dtype], (seed, r, c, batch, dtype, segs, steps, err)
