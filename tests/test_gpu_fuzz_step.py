@@ -77,3 +77,60 @@ def test_random_orthogonalize(mg, monkeypatch, seed):
                                 segments=segs or (2, 2, 1))
         err = rel_fro(to_f64(x[b]), ref)
         assert err <= TOL[dtype], (seed, r, c, batch, dtype, segs, steps, err)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_groups(mg, monkeypatch, seed):
+    """Persistent groups on random shape mixes: graph replay or direct
+    launches, the fused kernel on or off, a small workspace budget (several
+    chunks per bucket) or the default, host-resident gradients and weights in
+    one pinned block or none; every step equals muon_step bit for bit."""
+    rng = random.Random(9100 + seed)
+    monkeypatch.setenv("MUON_GRAPH", rng.choice(["0", "1"]))
+    monkeypatch.setenv("MUON_SMALL", rng.choice(["0", "1"]))
+    if rng.random() < 0.5:
+        monkeypatch.setenv("MUON_WORKSPACE_MB", "2")
+    mdt = rng.choice([torch.bfloat16, torch.float32])
+    host_io = rng.random() < 0.5
+    shapes = _shapes(rng, rng.randint(3, 8))
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_AUTO)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    Wa = [(torch.randn(s, generator=g, device="cuda") * 0.02).to(torch.bfloat16) for s in shapes]
+    Ga = [(torch.randn(s, generator=g, device="cuda") * 0.03).to(torch.bfloat16) for s in shapes]
+    Ma = [torch.zeros(s, device="cuda", dtype=mdt) for s in shapes]
+    Wb, Mb = [w.clone() for w in Wa], [m.clone() for m in Ma]
+    Gb = [x.clone() if not host_io else torch.zeros_like(x) for x in Ga]
+    group = mg.MuonGroup(Wb, Gb, Mb)
+    try:
+        if host_io:
+            n = sum(x.numel() for x in Ga)
+            gblock = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+            wblock = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+            host_g, host_w, off = [], [], 0
+            for x in Ga:
+                host_g.append(gblock[off:off + x.numel()].view(x.shape))
+                host_w.append(wblock[off:off + x.numel()].view(x.shape))
+                off += x.numel()
+            for hg, x in zip(host_g, Ga):
+                hg.copy_(x)
+            group.set_host_io(host_g, host_w)
+        for i, (lr, beta, wd, nest) in enumerate([(0.02, 0.95, 0.1, True), (0.01, 0.9, 0.0, False)]):
+            if i:
+                for j, x in enumerate(Ga):
+                    x.mul_(-0.5).add_(0.002)
+                    if host_io:
+                        host_g[j].copy_(x)
+                    else:
+                        Gb[j].copy_(x)
+            torch.cuda.synchronize()
+            mg.muon_step(Wa, Ga, Ma, lr=lr, beta=beta, wd=wd, nesterov=nest)
+            group.step(lr=lr, beta=beta, wd=wd, nesterov=nest)
+            torch.cuda.synchronize()
+            assert mg.muon_sync_status() == mg.MUON_OK
+            for x, y in zip(Wa + Ma, Wb + Mb):
+                assert torch.equal(x, y), (seed, i, shapes)
+            if host_io:
+                for hw, w in zip(host_w, Wb):
+                    assert torch.equal(hw, w.cpu()), (seed, i)
+    finally:
+        group.close()
