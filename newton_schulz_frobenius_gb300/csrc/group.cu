@@ -98,7 +98,7 @@ static int group_run_unit(muon_group* g, const GroupUnit& u, cudaStream_t s) {
     const int m = g->keys[u.k].first, n = g->keys[u.k].second;
     const NsPlan& plan = g->plans[u.k];
     const float scale = 0.2f * std::sqrt((float)n);
-    const ChunkLayout L = chunk_layout(m, n, u.B, g->ns_dtype);
+    const ChunkLayout L = chunk_layout(m, n, u.B, g->ns_dtype, plan.fp32_tc);
     const MatEntry* dm = g->d_table + g->bucket_first[u.k] + u.c0;
     if ((r = run_prep(g->dc, s, g->cbase, L, m, n, u.B, dm, g->param_dtype, g->mom_dtype, g->ns_dtype, true, 0, 0.f,
                       g->vec_ok[u.k] != 0, g->pcnt, g->d_hyper)))
@@ -225,8 +225,8 @@ static int group_plan(muon_group* g, cudaStream_t s) {
             g->chunks[k] = cnt;
             continue;
         }
-        g->chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, g->ns_dtype).total, cnt);
-        chunk_need = std::max(chunk_need, chunk_layout(m, n, g->chunks[k], g->ns_dtype).total);
+        g->chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, g->ns_dtype, g->plans[k].fp32_tc).total, cnt);
+        chunk_need = std::max(chunk_need, chunk_layout(m, n, g->chunks[k], g->ns_dtype, g->plans[k].fp32_tc).total);
     }
     size_t work_bytes = 0;
     g->fused = plan_fused(g->dc, g->plans, g->keys, g->bucket_size, g->ns_dtype, &work_bytes);

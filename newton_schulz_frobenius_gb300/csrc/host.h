@@ -95,6 +95,7 @@ struct NsPlan {
     int sym_dense;  // compute all tiles of the symmetric products (no mirroring)
     int gram_tf32;  // bf16 path: Gram-space matrices kept in TF32 (else bf16)
     int fused;      // run the whole update of each matrix in one CTA (small_ns.cu)
+    int fp32_tc;    // fp32 path: products as three TF32 tensor-core passes (else FFMA)
 };
 
 // Workspace of one chunk of B matrices of oriented shape m x n.
@@ -191,7 +192,12 @@ NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_
 GemmArgs gemm_base(int dtype, int* status);
 // work_k: the contraction length the recorded work counts (0: a.K)
 int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass, int64_t work_k = 0);
-ChunkLayout chunk_layout(int m, int n, int B, int dtype);
+// fp32_tc: the fp32 path's products as three TF32 passes (the layout then
+// holds their split operands); ignored for 16-bit dtypes
+ChunkLayout chunk_layout(int m, int n, int B, int dtype, int fp32_tc = 0);
+// Whether fp32 products of `count` oriented m x n matrices run as three TF32
+// passes (MUON_FP32_TC=1; else FFMA).
+int fp32_tc_choice(int dtype, int m, int n, int64_t count);
 int run_ns(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,
            int dtype, const NsPlan& plan, bool use_inv, const FinalEpi& fin);
 int run_prep(const DevCtx& dc, cudaStream_t s, char* base, const ChunkLayout& L, int m, int n, int B,

@@ -46,6 +46,7 @@ NsPlan make_plan(const float coeffs[3], int steps, const std::vector<int>& gram_
     p.sym_dense = sym_dense;
     p.gram_tf32 = gram_space_tf32(path, m, n);
     p.fused = 0;
+    p.fp32_tc = 0;
     p.a = coeffs[0];
     p.b = coeffs[1];
     p.c = coeffs[2];
@@ -77,10 +78,17 @@ GemmArgs gemm_base(int dtype, int* status) {
     return a;
 }
 
-// fp32 products on the TF32 tensor path as three passes (tf32x3.cu) instead
-// of FFMA: MUON_FP32_TC=1.  Measured slower than the split-K FFMA products at
-// the fp32 workload's sizes, so off by default.
-int fp32_tc_enabled() {
+// fp32 products on the TF32 tensor path as three passes (tf32x3.cu) or on
+// FFMA; MUON_FP32_TC=1 asks for the former.  Measured (muon_ns_orthogonalize,
+// best of plain and Gram): the tensor path is faster from about 1e9
+// multiply-adds of X X^T per bucket (1024x4096 1.28 against 2.11 ms,
+// 4096² 9.3 against 48.2 ms) but its error against the fp64 oracle grows
+// with K (3.6e-5 at 256x1024, 1.0e-4 at 768x3072, 1.4e-4 at 2048x8192,
+// against 1-6e-6 on FFMA), as an accumulation that does not round to
+// nearest would (its error adding up along K).  It stays opt-in.
+int fp32_tc_choice(int dtype, int m, int n, int64_t count) {
+    (void)m; (void)n; (void)count;
+    if (dtype != MUON_F32) return 0;
     const char* f = std::getenv("MUON_FP32_TC");
     return (f && f[0] == '1') ? 1 : 0;
 }
@@ -131,7 +139,7 @@ int run_gemm_tf32x3(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kcl
 
 // X is stored in the path's dtype; the m x m Gram-space matrices are fp32 on
 // both paths (TF32-rounded on the bf16 path).
-ChunkLayout chunk_layout(int m, int n, int B, int dtype) {
+ChunkLayout chunk_layout(int m, int n, int B, int dtype, int fp32_tc) {
     ChunkLayout L;
     const size_t es = esize(dtype);
     L.ldx = pad8(n);
@@ -151,7 +159,7 @@ ChunkLayout chunk_layout(int m, int n, int B, int dtype) {
     for (int i = 0; i < 3; ++i) L.off_S[i] = take(L.m_bytes * B);
     L.off_inv = take(sizeof(float) * B);
     L.off_part = take(sizeof(float) * (size_t)L.nparts * B);
-    L.tf32x3 = (dtype == MUON_F32) ? fp32_tc_enabled() : 0;
+    L.tf32x3 = (dtype == MUON_F32 && fp32_tc) ? 1 : 0;
     L.off_SA = L.off_SB = 0;
     if (L.tf32x3) {
         // XX^T: m x 3 pad4(n) both; Gram-space products m x 3 pad4(m) both;
@@ -451,10 +459,11 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
         g_last_path[{om, on, dtype}] = path;
         return MUON_OK;
     }
-    const size_t per = chunk_layout(om, on, 1, nsd).total;
+    plan.fp32_tc = fp32_tc_choice(nsd, om, on, batch);
+    const size_t per = chunk_layout(om, on, 1, nsd, plan.fp32_tc).total;
     const int chunk = budget_bytes_chunk(per, (int)std::min<int64_t>(batch, 65535));
     const size_t table_bytes = align_up(sizeof(MatEntry) * (size_t)batch, 256);
-    const ChunkLayout L = chunk_layout(om, on, chunk, nsd);
+    const ChunkLayout L = chunk_layout(om, on, chunk, nsd, plan.fp32_tc);
     Workspace* w = nullptr;
     if ((r = ws_get(dc.device, s, table_bytes + L.total, &w))) return r;
 
@@ -469,7 +478,7 @@ int muon_ns_orthogonalize(void* ptr, int64_t m, int64_t n, int64_t batch, int dt
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && (m % 8 == 0) && (n % 8 == 0);
     for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
         const int B = (int)std::min<int64_t>(chunk, batch - b0);
-        const ChunkLayout LB = chunk_layout(om, on, B, nsd);
+        const ChunkLayout LB = chunk_layout(om, on, B, nsd, plan.fp32_tc);
         int* pc = nullptr;
         if ((r = prep_counters(dc.device, s, B, &pc))) return r;
         if ((r = run_prep(dc, s, cbase, LB, om, on, B, d_table + b0, dtype, dtype, nsd, false, 0, 0.f, vec_ok, pc)))
@@ -538,8 +547,8 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
             chunks[k] = cnt;            // one launch, no workspace beyond the table
             continue;
         }
-        chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, nsd).total, cnt);
-        chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], nsd).total);
+        chunks[k] = budget_bytes_chunk(chunk_layout(m, n, 1, nsd, plans[k].fp32_tc).total, cnt);
+        chunk_need = std::max(chunk_need, chunk_layout(m, n, chunks[k], nsd, plans[k].fp32_tc).total);
     }
     // per bucket: matrix count, first table row, 16-byte access
     std::vector<int64_t> counts(keys.size()), firsts(keys.size());
@@ -600,7 +609,7 @@ int muon_step(void* const* params, const void* const* grads, void* const* moms, 
         }
         for (size_t c0 = 0; c0 < idx.size(); c0 += chunks[k]) {
             const int B = (int)std::min<size_t>(chunks[k], idx.size() - c0);
-            const ChunkLayout L = chunk_layout(m, n, B, nsd);
+            const ChunkLayout L = chunk_layout(m, n, B, nsd, plans[k].fp32_tc);
             const MatEntry* dm = d_table + first + c0;
             int* pc = nullptr;
             if ((r = prep_counters(dc.device, s, B, &pc))) return r;

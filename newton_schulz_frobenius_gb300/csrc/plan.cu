@@ -232,7 +232,8 @@ double fused_flops(const FusedLaunch& f, const std::vector<NsPlan>& plans,
 
 int autotune_shape(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int B, const NsConfig& cfg,
                           TuneEntry* out) {
-    const ChunkLayout L = chunk_layout(m, n, B, dtype);
+    const int ftc = fp32_tc_choice(dtype, m, n, B);
+    const ChunkLayout L = chunk_layout(m, n, B, dtype, ftc);
     const size_t table_off = align_up(L.total, 256);
     Workspace* w = nullptr;
     int r = ws_get(dc.device, s, table_off + align_up(sizeof(MatEntry) * (size_t)B, 256), &w);
@@ -379,6 +380,7 @@ int choose_plan(const DevCtx& dc, cudaStream_t s, int m, int n, int dtype, int b
     // the fused small-matrix kernel: as measured, else whenever it applies
     const bool measured = have && ent.path == path;
     plan->fused = small_eligible(*plan, m, n, dtype) && (measured ? ent.fused != 0 : true);
+    plan->fp32_tc = fp32_tc_choice(dtype, m, n, bucket_count);
     return MUON_OK;
 }
 

@@ -3,7 +3,9 @@
 over a tripled K) against the fp64 CPU oracle on identical seeded bytes, at the
 fp32 bar (1e-4 relative Frobenius error).  Shapes cover several tiles, K not a
 multiple of 4 (padded thirds) and both operand layouts of the apply (QX reads
-X transposed through the split)."""
+X transposed through the split).  The bar holds at these sizes (3.6e-5 at
+256x1024); the error grows with K (1.0e-4 at 768x3072, 1.4e-4 at 2048x8192),
+which is why the path is opt-in."""
 import pytest
 
 from tests.gpu_util import SIGMA_TOL, TOL
