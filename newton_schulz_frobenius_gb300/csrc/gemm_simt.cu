@@ -17,6 +17,13 @@
 // each output sums its terms in order, one fused multiply-add at a time; each
 // thread holds the next k-step's operands in registers (16-byte loads where
 // the rows allow) while the current one is multiplied out of shared memory.
+//
+// Products with at least one 128 x 128 tile per SM take a second kernel:
+// tiles of 128 x 128, k-steps of 16, 8 x 8 outputs per thread (four 16-byte
+// shared-memory reads per 64 multiply-adds instead of two per 16), the
+// operand tiles double-buffered in shared memory with the next k-step held
+// in registers, one block barrier per k-step, two CTAs per SM (128
+// registers a thread).
 #include "muon_internal.cuh"
 #include "epilogue.cuh"
 
@@ -187,6 +194,119 @@ gemm_simt_kernel(const __grid_constant__ GemmArgs a, int tiles_m, int split, int
     cluster_barrier();
 }
 
+
+// ---- large products: 128 x 128 tiles, 8 x 8 outputs per thread ----
+
+constexpr int BT = 128;
+constexpr int BKS = 16;
+constexpr int BIG_LOADS = BT * BKS / 4 / 256;                        // 16-byte pieces per thread per operand
+constexpr int BIG_SMEM = 2 * 2 * BKS * (BT + 4) * (int)sizeof(float);  // two buffers of A and B
+
+template <bool B_KMAJOR>
+__device__ __forceinline__ void big_load(const GemmArgs& a, const float* A, const float* B, int row0, int col0,
+                                         int k0, bool vecA, bool vecB, float4 (&ra)[BIG_LOADS],
+                                         float4 (&rb)[BIG_LOADS]) {
+    constexpr int KQ = BKS / 4;                 // 16-byte pieces along K per row
+#pragma unroll
+    for (int i = 0; i < BIG_LOADS; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        const int r = idx / KQ, k = k0 + 4 * (idx % KQ);
+        ra[i] = (row0 + r < a.M) ? load4(A + (int64_t)(row0 + r) * a.lda + k, a.K - k, vecA)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (B_KMAJOR) {
+            rb[i] = (col0 + r < a.N) ? load4(B + (int64_t)(col0 + r) * a.ldb + k, a.K - k, vecB)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            const int kk = k0 + (idx >> 5), c = col0 + 4 * (idx & 31);
+            rb[i] = (kk < a.K) ? load4(B + (int64_t)kk * a.ldb + c, a.N - c, vecB) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+template <bool B_KMAJOR>
+__device__ __forceinline__ void big_store(float (*As)[BT + 4], float (*Bs)[BT + 4], const float4 (&ra)[BIG_LOADS],
+                                          const float4 (&rb)[BIG_LOADS]) {
+    constexpr int KQ = BKS / 4;
+#pragma unroll
+    for (int i = 0; i < BIG_LOADS; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        const int r = idx / KQ, k = 4 * (idx % KQ);
+        As[k][r] = ra[i].x; As[k + 1][r] = ra[i].y; As[k + 2][r] = ra[i].z; As[k + 3][r] = ra[i].w;
+        if (B_KMAJOR) {
+            Bs[k][r] = rb[i].x; Bs[k + 1][r] = rb[i].y; Bs[k + 2][r] = rb[i].z; Bs[k + 3][r] = rb[i].w;
+        } else {
+            *reinterpret_cast<float4*>(&Bs[idx >> 5][4 * (idx & 31)]) = rb[i];
+        }
+    }
+}
+
+template <bool B_KMAJOR>
+__global__ void __launch_bounds__(256, 2)
+gemm_simt_big_kernel(const __grid_constant__ GemmArgs a, int tiles_m) {
+    extern __shared__ __align__(16) float big_smem[];
+    auto As = reinterpret_cast<float (*)[BKS][BT + 4]>(big_smem);
+    auto Bs = reinterpret_cast<float (*)[BKS][BT + 4]>(big_smem + 2 * BKS * (BT + 4));
+
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.y;
+    int tm, tn;
+    if (a.symmetric) tri_decode(blockIdx.x, tm, tn);
+    else { tm = blockIdx.x % tiles_m; tn = blockIdx.x / tiles_m; }
+    const float* A = reinterpret_cast<const float*>(a.A) + (int64_t)b * a.strideA;
+    const float* B = reinterpret_cast<const float*>(a.B) + (int64_t)b * a.strideB;
+    const bool vecA = (a.lda % 4 == 0) && (a.strideA % 4 == 0 || a.batch == 1) &&
+                      (reinterpret_cast<uintptr_t>(a.A) & 15) == 0;
+    const bool vecB = (a.ldb % 4 == 0) && (a.strideB % 4 == 0 || a.batch == 1) &&
+                      (reinterpret_cast<uintptr_t>(a.B) & 15) == 0;
+    const int row0 = tm * BT, col0 = tn * BT;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    float4 ra[BIG_LOADS], rb[BIG_LOADS];
+    big_load<B_KMAJOR>(a, A, B, row0, col0, 0, vecA, vecB, ra, rb);
+    big_store<B_KMAJOR>(As[0], Bs[0], ra, rb);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < a.K; k0 += BKS) {
+        const bool more = k0 + BKS < a.K;
+        if (more) big_load<B_KMAJOR>(a, A, B, row0, col0, k0 + BKS, vecA, vecB, ra, rb);
+#pragma unroll
+        for (int kk = 0; kk < BKS; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+            const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
+        if (more) {
+            // the other buffer was last read one k-step ago, before the barrier below it
+            big_store<B_KMAJOR>(As[buf ^ 1], Bs[buf ^ 1], ra, rb);
+            __syncthreads();
+            buf ^= 1;
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = row0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+        float v0[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
+        float v1[4] = {acc[i][4], acc[i][5], acc[i][6], acc[i][7]};
+        epi_row_chunk_once<4>(a, b, r, col0 + tx * 4, v0);
+        epi_row_chunk_once<4>(a, b, r, col0 + 64 + tx * 4, v1);
+    }
+}
+
 }  // namespace
 
 // Split of K for a launch of `tiles` output tiles: doubled while the CTAs fit
@@ -199,6 +319,23 @@ int simt_split(int64_t tiles, int K, int num_sms) {
 }
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, int num_sms, cudaStream_t s) {
+    {
+        const int bm = (a.M + BT - 1) / BT, bn = (a.N + BT - 1) / BT;
+        const int per = a.symmetric ? bm * (bm + 1) / 2 : bm * bn;
+        if ((int64_t)per * a.batch >= num_sms) {
+            static const cudaError_t attr =
+                (cudaFuncSetAttribute(gemm_simt_big_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      BIG_SMEM) == cudaSuccess)
+                    ? cudaFuncSetAttribute(gemm_simt_big_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           BIG_SMEM)
+                    : cudaErrorInvalidValue;
+            if (attr != cudaSuccess) return attr;
+            dim3 grid(per, a.batch);
+            if (a.b_kmajor) launch_pdl(gemm_simt_big_kernel<true>, grid, dim3(256), (size_t)BIG_SMEM, s, a, bm);
+            else launch_pdl(gemm_simt_big_kernel<false>, grid, dim3(256), (size_t)BIG_SMEM, s, a, bm);
+            return cudaGetLastError();
+        }
+    }
     const int tiles_m = (a.M + ST - 1) / ST;
     const int tiles_n = (a.N + ST - 1) / ST;
     const int per_batch = a.symmetric ? tiles_m * (tiles_m + 1) / 2 : tiles_m * tiles_n;

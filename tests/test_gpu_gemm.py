@@ -83,6 +83,30 @@ def test_fp32_split_k(mg, kmajor, M, N, K, batch):
     _check(C, torch.matmul(A.double(), Bd), torch.float32)
 
 
+@pytest.mark.parametrize("kmajor", [True, False])
+@pytest.mark.parametrize("M,N,K,batch", [(1536, 1664, 200, 1), (1500, 1701, 77, 1), (700, 900, 130, 4)])
+def test_fp32_large_tiles(mg, kmajor, M, N, K, batch):
+    """fp32 products with at least one 128 x 128 tile per SM run on the
+    large-tile FFMA kernel: ragged edges, odd K and pitches, batches."""
+    A = _rand((batch, M, K), torch.float32, 31)
+    B = _rand((batch, N, K) if kmajor else (batch, K, N), torch.float32, 32)
+    C = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    mg.muon_debug_gemm(A, B, C, b_kmajor=kmajor, alpha=0.5)
+    torch.cuda.synchronize()
+    assert mg.muon_sync_status() == mg.MUON_OK
+    Bd = B.double().transpose(1, 2) if kmajor else B.double()
+    _check(C, 0.5 * torch.matmul(A.double(), Bd), torch.float32)
+
+
+def test_fp32_large_tiles_symmetric(mg):
+    X = _rand((1, 2304, 136), torch.float32, 33)
+    C = torch.full((1, 2304, 2304), float("nan"), dtype=torch.float32, device="cuda")
+    mg.muon_debug_gemm(X, X, C, b_kmajor=True, symmetric=True)
+    torch.cuda.synchronize()
+    assert torch.equal(C, C.transpose(1, 2))
+    _check(C, torch.matmul(X.double(), X.double().transpose(1, 2)), torch.float32)
+
+
 def test_fp32_split_k_symmetric(mg):
     X = _rand((1, 96, 1000), torch.float32, 23)
     C = torch.full((1, 96, 96), float("nan"), dtype=torch.float32, device="cuda")
