@@ -70,3 +70,44 @@ def test_random_products(mg, seed):
             assert torch.equal(C, C.transpose(1, 2)), case
         err = ((C.double() - ref).norm() / ref.norm().clamp_min(1e-30)).item()
         assert err < TOL[kind], (case, err)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_fp32_large_products(mg, seed):
+    """fp32 products with at least one 128x128 tile per SM (the large-tile
+    FFMA kernel): ragged M, N and K, both B layouts, symmetric and
+    polynomial products, one or two matrices."""
+    rng = random.Random(2000 + seed)
+    g = torch.Generator(device="cuda").manual_seed(50 + seed)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for _ in range(3):
+        sym = rng.random() < 0.4
+        poly = sym and rng.random() < 0.5
+        batch = rng.choice([1, 2])
+        M = rng.randint(1700, 2400) if not sym else rng.randint(2050, 2500)
+        K = M if poly else rng.randint(1, 600)
+        N = M if sym else rng.randint(1700, 2400)
+        kmajor = True if sym else rng.random() < 0.5
+        bm, bn = -(-M // 128), -(-N // 128)
+        assert (bm * (bm + 1) // 2 if sym else bm * bn) * batch >= sms
+        A = torch.randn((batch, M, K), generator=g, device="cuda") / K ** 0.5
+        if poly:
+            A = ((A + A.transpose(1, 2)) * 0.5).contiguous()
+        B = A if sym else torch.randn((batch, N, K) if kmajor else (batch, K, N), generator=g,
+                                      device="cuda") / K ** 0.5
+        C = torch.full((batch, M, N), float("nan"), device="cuda")
+        coeffs = (3.4445, -4.7750, 2.0315) if poly else None
+        mg.muon_debug_gemm(A, B, C, b_kmajor=kmajor, symmetric=sym, poly=coeffs)
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+        Ad = A.double()
+        ref = torch.matmul(Ad, B.double().transpose(1, 2) if kmajor else B.double())
+        if poly:
+            a, b, c = coeffs
+            ref = a * torch.eye(M, device="cuda", dtype=torch.float64) + b * Ad + c * ref
+        case = (M, N, K, batch, sym, poly, kmajor)
+        assert not torch.isnan(C).any(), case
+        if sym:
+            assert torch.equal(C, C.transpose(1, 2)), case
+        err = ((C.double() - ref).norm() / ref.norm()).item()
+        assert err < TOL["f32"], (case, err)

@@ -53,6 +53,16 @@ def test_orthogonalize_fp32(mg, rows, cols, batch, segments):
     assert s <= SIGMA_TOL
 
 
+@pytest.mark.parametrize("rows,cols", [(1100, 2200), (2200, 1100)])
+@pytest.mark.parametrize("segments", [None, (2, 2, 1)])
+def test_orthogonalize_fp32_large_tiles(mg, rows, cols, segments):
+    """fp32 NS whose long products have more 128x128 tiles than SMs (the
+    large-tile FFMA kernel) while the m x m products keep the split-K one."""
+    f, s = _ortho_case(mg, rows, cols, 1, "f32", segments, 140)
+    assert f <= TOL["f32"], f
+    assert s <= SIGMA_TOL
+
+
 @pytest.mark.parametrize("small", ["1", "0"])
 @pytest.mark.parametrize("rows,cols,batch", [
     (256, 1024, 1), (128, 512, 4), (256, 256, 2), (300, 1000, 1), (1000, 296, 1), (8, 16, 2),
