@@ -351,3 +351,15 @@ def test_degenerate_shapes_step(mg, monkeypatch, small, mom_dtype):
     for err, q, m_ok, _ in _step_case(mg, shapes, "bf16", mom_dtype, mg.MUON_PATH_AUTO, True, 9900, 0.02, steps=2):
         assert err <= TOL["bf16"] + q, (err, q)
         assert m_ok
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_maximum_side_step(mg, dtype):
+    """Matrices at the largest accepted side (2^20): a row and a column
+    vector and a few-row matrix, two steps against the oracle (one long
+    k-loop in XX^T, thousands of tiles in the apply)."""
+    side = 1 << 20
+    shapes = [(1, side), (side, 1), (8, side)] if dtype == "bf16" else [(2, side), (side, 3)]
+    for err, q, m_ok, _ in _step_case(mg, shapes, dtype, dtype, mg.MUON_PATH_AUTO, False, 9950, 0.02, steps=2):
+        assert err <= TOL[dtype] + q, (err, q)
+        assert m_ok
