@@ -76,7 +76,10 @@ typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muo
  *              Each matrix is normalised on its own.  A matrix with m > n is
  *              processed as its transpose; the result is written back untransposed.
  *   dtype      storage type of the matrices: MUON_F32 (fp32 path: fp32 FFMA
- *              products), MUON_BF16 or MUON_F16 (16-bit tensor-core products,
+ *              products; three TF32 tensor-core passes per product instead when
+ *              the environment sets MUON_FP32_TC=1, faster on large matrices
+ *              but with an error that grows with K past 1e-4 there),
+ *              MUON_BF16 or MUON_F16 (16-bit tensor-core products,
  *              fp32 accumulation, 16-bit intermediates of the NS precision:
  *              the storage type unless muon_set_ns_precision chose the other).
  *   coeffs     (a, b, c) of one NS step X <- aX + (bA + cA^2)X, A = XX^T.
