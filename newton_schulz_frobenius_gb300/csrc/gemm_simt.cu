@@ -200,7 +200,9 @@ gemm_simt_kernel(const __grid_constant__ GemmArgs a, int tiles_m, int split, int
 constexpr int BT = 128;
 constexpr int BKS = 16;
 constexpr int BIG_LOADS = BT * BKS / 4 / 256;                        // 16-byte pieces per thread per operand
-constexpr int BIG_SMEM = 2 * 2 * BKS * (BT + 4) * (int)sizeof(float);  // two buffers of A and B
+// two buffers of A and B, as dynamic shared memory (the form ptxas allocates
+// registers best for)
+constexpr int BIG_SMEM = 2 * 2 * BKS * (BT + 4) * (int)sizeof(float);
 
 template <bool B_KMAJOR>
 __device__ __forceinline__ void big_load(const GemmArgs& a, const float* A, const float* B, int row0, int col0,
@@ -323,13 +325,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, int num_sms, cudaStream_t s) {
         const int bm = (a.M + BT - 1) / BT, bn = (a.N + BT - 1) / BT;
         const int per = a.symmetric ? bm * (bm + 1) / 2 : bm * bn;
         if ((int64_t)per * a.batch >= num_sms) {
-            static const cudaError_t attr =
-                (cudaFuncSetAttribute(gemm_simt_big_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      BIG_SMEM) == cudaSuccess)
-                    ? cudaFuncSetAttribute(gemm_simt_big_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           BIG_SMEM)
-                    : cudaErrorInvalidValue;
-            if (attr != cudaSuccess) return attr;
+            static_assert(BIG_SMEM <= 48 * 1024, "dynamic shared memory above the default limit");
             dim3 grid(per, a.batch);
             if (a.b_kmajor) launch_pdl(gemm_simt_big_kernel<true>, grid, dim3(256), (size_t)BIG_SMEM, s, a, bm);
             else launch_pdl(gemm_simt_big_kernel<false>, grid, dim3(256), (size_t)BIG_SMEM, s, a, bm);
