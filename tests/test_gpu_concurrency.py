@@ -35,7 +35,7 @@ JOBS = [
 def _inputs(seed):
     g = torch.Generator(device="cuda").manual_seed(seed)
     out = []
-    for j, (shapes, pdt, mdt, xs) in enumerate(JOBS):
+    for shapes, pdt, mdt, xs in JOBS:
         W = [(torch.randn(s, generator=g, device="cuda") * 0.02).to(pdt) for s in shapes]
         M = [(torch.randn(s, generator=g, device="cuda") * 0.01).to(mdt) for s in shapes]
         G = [[(torch.randn(s, generator=g, device="cuda") * 0.03).to(pdt) for s in shapes] for _ in range(STEPS)]
