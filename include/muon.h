@@ -76,9 +76,10 @@ typedef enum { MUON_PATH_AUTO = 0, MUON_PATH_PLAIN = 1, MUON_PATH_GRAM = 2 } muo
  *              Each matrix is normalised on its own.  A matrix with m > n is
  *              processed as its transpose; the result is written back untransposed.
  *   dtype      storage type of the matrices: MUON_F32 (fp32 path: fp32 FFMA
- *              products; three TF32 tensor-core passes per product instead when
- *              the environment sets MUON_FP32_TC=1, faster on large matrices
- *              but with an error that grows with K past 1e-4 there),
+ *              products, or, from 2^30 multiply-adds of X X^T per call (m^2 n
+ *              times batch), three TF32 tensor-core passes per product with K
+ *              accumulated in chunks added in round-to-nearest fp32; the
+ *              environment's MUON_FP32_TC=1 or 0 forces one),
  *              MUON_BF16 or MUON_F16 (16-bit tensor-core products,
  *              fp32 accumulation, 16-bit intermediates of the NS precision:
  *              the storage type unless muon_set_ns_precision chose the other).
@@ -385,7 +386,10 @@ int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms,
  *   C is M x N.  dtype is the storage type of A, B and C: MUON_BF16 or MUON_F16
  *   (16-bit tensor cores), MUON_F32 (fp32 FFMA), or 3 = fp32 storage
  *   multiplied on the TF32 tensor path (the kind the bf16 NS path uses for
- *   some Gram-space products; B must be K-major).  tile_n selects the N extent of the
+ *   some Gram-space products; B must be K-major), or 4 = as 3 with the
+ *   K-blocks accumulated in chunks of 16 (512 elements), each chunk from zero,
+ *   the chunk sums added in round-to-nearest fp32 (the fp32 path's three-pass
+ *   products; 128 x 128 tiles whatever tile_n asks).  tile_n selects the N extent of the
  *   tensor-core tile (0 = default, 128 or 256).
  */
 int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

@@ -378,19 +378,22 @@ def muon_kernel_timing_read():
 
 
 MUON_DEBUG_TF32 = 3
+MUON_DEBUG_TF32_CHUNKED = 4
 
 
 def muon_debug_gemm(A, B, C, b_kmajor=True, symmetric=False, poly=None, alpha=1.0, tile_n=0, stream=None,
-                    tf32=False):
+                    tf32=False, tf32_chunked=False):
     """C[b] = alpha * A[b] op(B[b]) (or the fused polynomial when poly=(a, b, c)).
-    tf32=True multiplies fp32 tensors on the TF32 tensor-core path."""
+    tf32=True multiplies fp32 tensors on the TF32 tensor-core path;
+    tf32_chunked=True does too, accumulating K in chunks summed in
+    round-to-nearest fp32."""
     for t, nm in ((A, "A"), (B, "B"), (C, "C")):
         _cuda_contig(t, nm)
     batch = A.shape[0] if A.dim() == 3 else 1
     M, K = A.shape[-2], A.shape[-1]
     N = B.shape[-2] if b_kmajor else B.shape[-1]
     pa, pb, pc = poly if poly is not None else (0.0, 0.0, 0.0)
-    code = MUON_DEBUG_TF32 if tf32 else _dtype_code(A)
+    code = MUON_DEBUG_TF32_CHUNKED if tf32_chunked else (MUON_DEBUG_TF32 if tf32 else _dtype_code(A))
     _check(lib().muon_debug_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, batch, code,
                                  1 if b_kmajor else 0, 1 if symmetric else 0, 1 if poly is not None else 0,
                                  float(alpha), float(pa), float(pb), float(pc), tile_n, _stream_ptr(stream)),

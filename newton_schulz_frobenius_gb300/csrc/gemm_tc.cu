@@ -22,7 +22,9 @@
 // Operand kinds: bf16 or fp16 (kind::f16, K = 16 per instruction, A and B of
 // the same type) for the long products and the 16-bit Gram-space products,
 // TF32 on fp32 storage (kind::tf32, K = 8) for the Gram-space products that
-// need it; either way one k-block is 128 bytes of every operand row.
+// need it and for the fp32 path's three-pass products; either way one k-block
+// is 128 bytes of every operand row.  The three-pass products accumulate in
+// chunks of k-blocks added in round-to-nearest fp32 (the CH instance, below).
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
 // of tile t overlaps the main loop of tile t+1.
 // Paired launches (PAIR, 128 x 256 tiles per CTA): 2-CTA clusters run 2-SM
@@ -342,6 +344,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 consecutive fp32 columns from this thread's 32 values; the
+// store is complete after tmem_wait_st.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+          "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+          "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+          "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+          "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+          "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+          "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+          "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+          "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+          "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+          "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor: start, leading/stride byte offsets, the
 // fixed descriptor version of this MMA generation (bit 46) and 128-byte swizzle.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -502,13 +527,22 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC>
+// CH (chunked accumulation, TF32 on 128 x 128 tiles): the k-blocks of a tile
+// accumulate in chunks of args.kchunk, each from zero in one of the two TMEM
+// buffers; the epilogue adds every chunk into a third buffer with fp32 adds
+// that round to nearest, and the last chunk's sum goes through the ordinary
+// epilogue.  The tensor core's own fp32 accumulation does not round to
+// nearest, so over a long K its error grows with K; in chunks it is bounded
+// by the chunk length.
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC, bool CH = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args, const TileSched sched) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
     constexpr int S = C::STAGES;
+    constexpr int TCOLS = CH ? 512 : C::TMEM_COLS;     // chunked: two accumulators and the running sum
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
+    static_assert(!CH || (TF32 && BN == 128 && !PAIR && !MC), "chunked accumulation: unpaired TF32 128-wide tiles");
     static_assert(!PAIR || BN == 256, "paired products use 128 x 256 tiles per CTA");
     static_assert(!MC || PAIR, "multicast clusters are made of 2-SM pairs");
     constexpr int MM = PAIR ? 2 * BM : BM;      // rows of one product instruction
@@ -567,10 +601,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     if (warp == 1) {
         if (PAIR) {
-            tmem_alloc2(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_alloc2(smem_u32(tmem_slot), TCOLS);
             tmem_relinquish2();
         } else {
-            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_alloc(smem_u32(tmem_slot), TCOLS);
             tmem_relinquish();
         }
     }
@@ -580,6 +614,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = (args.K + KE - 1) / KE;
+    const int kchunk = CH ? max(1, args.kchunk) : kblocks;     // k-blocks per accumulation chunk
+    const int nchunks = CH ? (kblocks + kchunk - 1) / kchunk : 1;
     pdl_wait();          // operands, G, W and the scale come from earlier kernels
     pdl_trigger();
 
@@ -688,13 +724,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t aphase = 0;
             bool ok = true;
             for (int t = unit0; t < sched.total && ok; t += ustep) {
+              for (int c = 0; c < nchunks && ok; ++c) {
+                const int kb0 = CH ? c * kchunk : 0;
+                const int kb1 = CH ? min(kblocks, kb0 + kchunk) : kblocks;
                 if (!wait_bounded(acce0 + 8 * acc, aphase ^ 1u, abort_flag, args.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, args.status)) {
                         ok = false;
                         break;
@@ -708,7 +747,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint64_t ad = sdesc(a_base + kk * 32, 16, 1024);
                         const uint64_t bd = B_KMAJOR ? sdesc(b_base + kk * 32, 16, 1024)
                                                      : sdesc(b_base + kk * 2048, BK * 128, 1024);
-                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
                         if (PAIR) {
                             if (TF32) tc_mma2_tf32(d, ad, bd, IDESC, accum);
                             else tc_mma2_bf16(d, ad, bd, IDESC, accum);
@@ -730,6 +769,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 else tc_commit(accf0 + 8 * acc);
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
+              }
             }
             if (!ok) {
                 // wait (bounded) for the products this thread issued
@@ -771,6 +811,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         prefetch_l2(wb + ((int64_t)c * args.M + tm * BM + q * 32) * ob);
                 }
             }
+            if (CH && nchunks > 1) {
+                // all chunks but the last: running sum (third TMEM buffer) += chunk,
+                // this warp's 32 lanes x HALF_COLS columns, 32 at a time
+                const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+                bool cok = true;
+                for (int c = 0; c + 1 < nchunks; ++c) {
+                    const bool okw = wait_bounded(accf0 + 8 * acc, aphase, abort_flag, args.status);
+                    if (!__all_sync(0xffffffffu, okw)) { cok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int h = 0; h < HALF_COLS / 32; ++h) {
+                        const uint32_t col = (uint32_t)(half * HALF_COLS + 32 * h);
+                        float v[32];
+                        tmem_ld32(tl + (uint32_t)(acc * BN) + col, v);
+                        if (c > 0) {
+                            float r[32];
+                            tmem_ld32(tl + (uint32_t)(2 * BN) + col, r);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(r[j], v[j]);
+                        }
+                        tmem_st32(tl + (uint32_t)(2 * BN) + col, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+                    acc ^= 1;
+                    if (acc == 0) aphase ^= 1u;
+                }
+                if (!cok) break;
+            }
             // per-tile scalars and the first chunk's G / W loads are issued
             // before the wait, so their latency hides behind the main loop
             const float scale = epi_alpha(args, b);
@@ -795,6 +866,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     epi_load_chunk<32>(args, ent, b, row0 + lane, col0 + 32, gnxt);
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
+                if (CH && nchunks > 1) {
+                    float r[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(2 * BN + ch * 32), r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(r[j], v[j]);
+                }
                 if (B_KMAJOR && args.tma_c) {
                     // 16-bit workspace products: the chunk (and its mirror) leave on the copy engine
                     epi_store_tma<C::STORE_BUFS>(args, &tmC, b, row0, col0, v, scale, gcur,
@@ -828,8 +905,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (PAIR) cluster_sync();     // no product, commit or remote arrive targets this CTA any more
     if (warp == 1) {
         tc_fence_after();
-        if (PAIR) tmem_dealloc2(tmem_base, C::TMEM_COLS);
-        else tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if (PAIR) tmem_dealloc2(tmem_base, TCOLS);
+        else tmem_dealloc(tmem_base, TCOLS);
     }
 }
 
@@ -882,10 +959,10 @@ bool tma_store_enabled() {
     return !(e && e[0] == '0');
 }
 
-template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC>
+template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC, bool CH = false>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
-    auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR, MC>;
+    auto kern = gemm_tc_kernel<BN, B_KMAJOR, TF32, PAIR, MC, CH>;
     constexpr int CL = MC ? 4 : 2;           // CTAs per cluster of a paired launch
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1000,6 +1077,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     const bool pair = (bn == 256) && a.pair != 0;
     const bool mc = pair && a.mc != 0;
     if (tf32) {
+        // chunked accumulation: unpaired 128-wide tiles whatever the tile request
+        if (a.kchunk > 0) return tc::launch_impl<128, true, true, false, false, true>(a, num_sms, s);
         if (bn == 128) return tc::launch_impl<128, true, true, false, false>(a, num_sms, s);
         if (!pair) return tc::launch_impl<256, true, true, false, false>(a, num_sms, s);
         return mc ? tc::launch_impl<256, true, true, true, true>(a, num_sms, s)

@@ -17,6 +17,10 @@ namespace muon {
 // fp32 storage whose values are consumed by the tensor cores as TF32 (10-bit
 // mantissa).  The bf16 path keeps some m x m Gram-space matrices in this form.
 constexpr int DT_TF32 = 3;
+// debug product code: TF32 with chunked accumulation (TF32_KCHUNK k-blocks of
+// 32 elements per chunk, chunk sums added in round-to-nearest fp32)
+constexpr int DT_TF32_CHUNKED = 4;
+constexpr int TF32_KCHUNK = 16;
 
 // 16-bit storage that the kind::f16 tensor-core products take (bf16 or fp16).
 __host__ __device__ constexpr bool is_half(int dtype) { return dtype == MUON_BF16 || dtype == MUON_F16; }
@@ -78,6 +82,7 @@ struct GemmArgs {
     int* status;            // device status word
     const float* hyper;     // optional device block {lr, beta, wd, nesterov}: overrides lr, wd
     int stall;              // test hook: k + 1 = CTA 0 leaves k-block k of its first tile unfilled; 0 = off
+    int kchunk;             // TF32: k-blocks per accumulation chunk (sums added in round-to-nearest fp32); 0 = whole K
 };
 
 // Launchers (return the CUDA error of the launch).

@@ -78,19 +78,22 @@ GemmArgs gemm_base(int dtype, int* status) {
     return a;
 }
 
-// fp32 products on the TF32 tensor path as three passes (tf32x3.cu) or on
-// FFMA; MUON_FP32_TC=1 asks for the former.  Measured (muon_ns_orthogonalize,
-// best of plain and Gram): the tensor path is faster from about 1e9
-// multiply-adds of X X^T per bucket (1024x4096 1.28 against 2.11 ms,
-// 4096² 9.3 against 48.2 ms) but its error against the fp64 oracle grows
-// with K (3.6e-5 at 256x1024, 1.0e-4 at 768x3072, 1.4e-4 at 2048x8192,
-// against 1-6e-6 on FFMA), as an accumulation that does not round to
-// nearest would (its error adding up along K).  It stays opt-in.
+// fp32 products on the TF32 tensor path as three passes (tf32x3.cu, the
+// k-blocks accumulated in chunks added in round-to-nearest fp32) or on FFMA.
+// MUON_FP32_TC=1 or 0 forces one; otherwise the tensor path takes buckets of
+// at least 2^30 multiply-adds of X X^T (m^2 n per matrix, times the count).
+// Measured (muon_ns_orthogonalize, best of plain and Gram, ms, FFMA against
+// the tensor path): 640x2560 0.76 / 0.88, 512x2048 0.44 / 0.73, 256x1024 x 4
+// 0.30 / 0.52 below the mark; 1024^2 0.94 / 0.81, 512^2 x 8 0.97 / 0.65,
+// 256x1024 x 16 0.83 / 0.67, 768x3072 1.27 / 1.00, 2048x8192 12.9 / 3.9,
+// 4096^2 29.6 / 11.5 at or above it.  With whole-K accumulation the tensor
+// path missed the 1e-4 fp32 bar from about 768x3072 (its error grew with K);
+// in chunks it holds at every size tested.
 int fp32_tc_choice(int dtype, int m, int n, int64_t count) {
-    (void)m; (void)n; (void)count;
     if (dtype != MUON_F32) return 0;
     const char* f = std::getenv("MUON_FP32_TC");
-    return (f && f[0] == '1') ? 1 : 0;
+    if (f && (f[0] == '0' || f[0] == '1')) return f[0] == '1' ? 1 : 0;
+    return (double)m * m * (double)n * (double)count >= 1073741824.0 ? 1 : 0;
 }
 
 int run_gemm(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kclass, int64_t work_k) {
@@ -134,6 +137,10 @@ int run_gemm_tf32x3(const DevCtx& dc, cudaStream_t s, const GemmArgs& a, int kcl
     t.K = (int)K3;
     t.c_dtype = MUON_F32;
     t.round_tf32 = 0;
+    // the tensor core's fp32 accumulation does not round to nearest: summed
+    // over the whole tripled K its error grows with K (1.2e-4 relative for
+    // K = 3 x 8192); chunk sums added in round-to-nearest fp32 bound it
+    t.kchunk = TF32_KCHUNK;
     return run_gemm(dc, s, t, kclass, a.K);   // work counted on the fp32 product's K
 }
 
@@ -682,7 +689,9 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
     if (!A || !B || !C) return fail(MUON_EINVAL, "NULL operand");
     if (M < 1 || N < 1 || K < 1 || batch < 1) return fail(MUON_EINVAL, "bad sizes");
     if (M > (1 << 20) || N > (1 << 20) || K > (1 << 20)) return fail(MUON_EINVAL, "size above 2^20");
-    if (!valid_dtype(dtype) && dtype != DT_TF32) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    if (!valid_dtype(dtype) && dtype != DT_TF32 && dtype != DT_TF32_CHUNKED) return fail(MUON_EDTYPE, "dtype %d", dtype);
+    const bool chunked = (dtype == DT_TF32_CHUNKED);
+    if (chunked) dtype = DT_TF32;
     if (dtype == DT_TF32 && !b_kmajor) return fail(MUON_EINVAL, "TF32 products need a K-major B");
     if ((symmetric || poly) && M != N) return fail(MUON_EINVAL, "symmetric product needs M == N");
     if (poly && (!symmetric || K != M)) return fail(MUON_EINVAL, "poly needs a symmetric square product");
@@ -705,6 +714,7 @@ int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
     g.alpha = alpha;
     g.C = C; g.ldc = N; g.strideC = M * N;
     g.tile_n = tile_n;   // 0: the launcher's default for the product kind
+    if (chunked) g.kchunk = TF32_KCHUNK;
     if (poly) {
         g.epi = EPI_POLY;
         g.Gin = A; g.ldg = K; g.strideG = M * K;

@@ -1,11 +1,12 @@
 """fp32 path with its products as three TF32 tensor-core passes
-(MUON_FP32_TC=1: A' = [hi | hi | lo], B' = [hi | lo | hi], one TF32 product
-over a tripled K) against the fp64 CPU oracle on identical seeded bytes, at the
-fp32 bar (1e-4 relative Frobenius error).  Shapes cover several tiles, K not a
-multiple of 4 (padded thirds) and both operand layouts of the apply (QX reads
-X transposed through the split).  The bar holds at these sizes (3.6e-5 at
-256x1024); the error grows with K (1.0e-4 at 768x3072, 1.4e-4 at 2048x8192),
-which is why the path is opt-in."""
+(MUON_FP32_TC=1 forces it; large buckets take it by default: A' = [hi | hi |
+lo], B' = [hi | lo | hi], one TF32 product over a tripled K, accumulated in
+chunks added in round-to-nearest fp32) against the fp64 CPU oracle on
+identical seeded bytes, at the fp32 bar (1e-4 relative Frobenius error).
+Shapes cover several tiles, K not a multiple of 4 (padded thirds), both
+operand layouts of the apply (QX reads X transposed through the split) and
+the long K where whole-K accumulation missed the bar (1.0e-4 at 768x3072,
+1.4e-4 at 2048x8192)."""
 import pytest
 
 from tests.gpu_util import SIGMA_TOL, TOL
@@ -69,3 +70,81 @@ def test_tf32x3_runs_on_the_tensor_path(mg, monkeypatch):
     work0 = recs["0"]["gemm_fp32"][2]
     work1 = sum(v[2] for k, v in recs["1"].items() if k.startswith("gemm_tc"))
     assert abs(work1 - work0) / work0 < 1e-12
+
+
+def _tf32_rn(x):
+    m, e = torch.frexp(x.double())
+    return torch.ldexp(torch.round(torch.ldexp(m, torch.tensor(11, device=x.device))), e - 11).float()
+
+
+@pytest.mark.parametrize("M,N,K,batch,sym", [
+    (256, 256, 8192, 1, True), (200, 328, 5000, 2, False), (384, 384, 384, 1, True),
+    (130, 130, 2500, 3, True), (64, 520, 700, 1, False)])
+def test_chunked_tf32_product(mg, M, N, K, batch, sym):
+    """The TF32 product with chunked accumulation on three-pass operands
+    ([hi|hi|lo] against [hi|lo|hi], as the fp32 path builds them): its error
+    against the exact product of the fp32 values stays at the chunk's level
+    for any K, where whole-K accumulation grows with K (about 1.2e-4 at
+    K = 8192).  Ragged M, N and K, several matrices, symmetric launches."""
+    g = torch.Generator(device="cuda").manual_seed(M + K)
+    X = torch.randn((batch, M, K), generator=g, device="cuda")
+    Y = X if sym else torch.randn((batch, N, K), generator=g, device="cuda")
+    K4 = -(-K // 4) * 4
+
+    def split(Z, order):
+        hi = _tf32_rn(Z)
+        lo = _tf32_rn(Z - hi)
+        pad = torch.zeros(Z.shape[:-1] + (K4 - K,), device="cuda")
+        hi, lo = torch.cat([hi, pad], -1), torch.cat([lo, pad], -1)
+        return torch.cat([hi, hi, lo] if order == "hhl" else [hi, lo, hi], dim=-1).contiguous()
+
+    A3, B3 = split(X, "hhl"), split(Y, "hlh")
+    C = torch.full((batch, M, N), float("nan"), device="cuda")
+    mg.muon_debug_gemm(A3, B3, C, b_kmajor=True, symmetric=sym, tf32_chunked=True)
+    torch.cuda.synchronize()
+    assert mg.muon_sync_status() == mg.MUON_OK
+    ref = torch.matmul(X.double(), Y.double().transpose(1, 2))
+    assert not torch.isnan(C).any()
+    if sym:
+        assert torch.equal(C, C.transpose(1, 2))
+    err = ((C.double() - ref).norm() / ref.norm()).item()
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("rows,cols", [(768, 3072), (1024, 4096), (2048, 8192)])
+@pytest.mark.parametrize("segments", [None, (2, 2, 1)])
+def test_orthogonalize_tf32x3_long_k(mg, monkeypatch, rows, cols, segments):
+    """Three-pass TF32 NS at the sizes where whole-K accumulation missed the
+    fp32 bar (1.0e-4 at 768x3072, 1.4e-4 at 2048x8192): with chunked
+    accumulation it holds."""
+    monkeypatch.setenv("MUON_FP32_TC", "1")
+    f, s = _ortho_case(mg, rows, cols, 1, "f32", segments, 320)
+    assert f <= TOL["f32"], f
+    assert s <= SIGMA_TOL
+
+
+def test_step_fp32_large_auto(mg, monkeypatch):
+    """A large fp32 matrix through muon_step with the automatic choices (the
+    tensor path is taken at this size), two steps against the oracle, and
+    the persistent group giving the same bytes."""
+    monkeypatch.delenv("MUON_FP32_TC", raising=False)
+    mg.muon_set_ns_config(mg.QUINTIC, 5, (2, 2, 1), mg.MUON_PATH_AUTO)
+    for err, q, m_ok, _ in _step_case(mg, [(1024, 4096), (4096, 1024)], "f32", "f32", mg.MUON_PATH_AUTO, True,
+                                      1500, 1.0, steps=2):
+        assert err <= TOL["f32"] + q, (err, q)
+        assert m_ok
+    g = torch.Generator(device="cuda").manual_seed(9)
+    Wa = [torch.randn((1024, 4096), generator=g, device="cuda") * 0.02]
+    Ga = [torch.randn((1024, 4096), generator=g, device="cuda")]
+    Ma = [torch.zeros((1024, 4096), device="cuda")]
+    Wb, Gb, Mb = [Wa[0].clone()], [Ga[0].clone()], [Ma[0].clone()]
+    group = mg.MuonGroup(Wb, Gb, Mb)
+    try:
+        for _ in range(2):
+            mg.muon_step(Wa, Ga, Ma, lr=0.02, beta=0.95, wd=0.1, nesterov=True)
+            group.step(lr=0.02, beta=0.95, wd=0.1, nesterov=True)
+        torch.cuda.synchronize()
+        assert mg.muon_sync_status() == mg.MUON_OK
+        assert torch.equal(Wa[0], Wb[0]) and torch.equal(Ma[0], Mb[0])
+    finally:
+        group.close()

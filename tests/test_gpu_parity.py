@@ -53,11 +53,18 @@ def test_orthogonalize_fp32(mg, rows, cols, batch, segments):
     assert s <= SIGMA_TOL
 
 
+@pytest.mark.parametrize("fp32_tc", ["0", "auto"])
 @pytest.mark.parametrize("rows,cols", [(1100, 2200), (2200, 1100)])
 @pytest.mark.parametrize("segments", [None, (2, 2, 1)])
-def test_orthogonalize_fp32_large_tiles(mg, rows, cols, segments):
-    """fp32 NS whose long products have more 128x128 tiles than SMs (the
-    large-tile FFMA kernel) while the m x m products keep the split-K one."""
+def test_orthogonalize_fp32_large_tiles(mg, monkeypatch, fp32_tc, rows, cols, segments):
+    """fp32 NS whose long products have more 128x128 tiles than SMs: on FFMA
+    (the large-tile kernel for them, the split-K one for the m x m products),
+    and as the automatic choice takes it at this size (three-pass TF32 with
+    chunked accumulation)."""
+    if fp32_tc == "0":
+        monkeypatch.setenv("MUON_FP32_TC", "0")
+    else:
+        monkeypatch.delenv("MUON_FP32_TC", raising=False)
     f, s = _ortho_case(mg, rows, cols, 1, "f32", segments, 140)
     assert f <= TOL["f32"], f
     assert s <= SIGMA_TOL
