@@ -387,9 +387,9 @@ int muon_kernel_timing_read(char* names, int64_t* launches, double* total_ms,
  *   (16-bit tensor cores), MUON_F32 (fp32 FFMA), or 3 = fp32 storage
  *   multiplied on the TF32 tensor path (the kind the bf16 NS path uses for
  *   some Gram-space products; B must be K-major), or 4 = as 3 with the
- *   K-blocks accumulated in chunks of 16 (512 elements), each chunk from zero,
+ *   K-blocks accumulated in chunks of 32 (1024 elements), each chunk from zero,
  *   the chunk sums added in round-to-nearest fp32 (the fp32 path's three-pass
- *   products; 128 x 128 tiles whatever tile_n asks).  tile_n selects the N extent of the
+ *   products; 128 x 128 tiles, or 2-SM pairs when tile_n is 256).  tile_n selects the N extent of the
  *   tensor-core tile (0 = default, 128 or 256).
  */
 int muon_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

@@ -527,22 +527,28 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& a, const CUtensorM
 // the kernel
 // ---------------------------------------------------------------------------
 
-// CH (chunked accumulation, TF32 on 128 x 128 tiles): the k-blocks of a tile
-// accumulate in chunks of args.kchunk, each from zero in one of the two TMEM
-// buffers; the epilogue adds every chunk into a third buffer with fp32 adds
-// that round to nearest, and the last chunk's sum goes through the ordinary
-// epilogue.  The tensor core's own fp32 accumulation does not round to
-// nearest, so over a long K its error grows with K; in chunks it is bounded
-// by the chunk length.
+// CH (chunked accumulation, TF32): the k-blocks of a tile accumulate in
+// chunks of args.kchunk, each from zero; the epilogue adds every chunk into a
+// running-sum TMEM buffer with fp32 adds that round to nearest, and the last
+// chunk's sum goes through the ordinary epilogue.  The tensor core's own fp32
+// accumulation does not round to nearest, so over a long K its error grows
+// with K; in chunks it is bounded by the chunk length.  Unpaired 128 x 128
+// tiles keep two accumulators (a chunk accumulates while the previous one is
+// added); a 2-SM pair's 128 x 256 half-tile leaves room for one accumulator
+// beside the running sum, so its products wait for each chunk's addition.
 template <int BN, bool B_KMAJOR, bool TF32, bool PAIR, bool MC, bool CH = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args, const TileSched sched) {
     using C = Cfg<BN, PAIR, B_KMAJOR>;
     constexpr int S = C::STAGES;
-    constexpr int TCOLS = CH ? 512 : C::TMEM_COLS;     // chunked: two accumulators and the running sum
+    constexpr int TCOLS = CH ? 512 : C::TMEM_COLS;     // chunked: the accumulators and the running sum
+    constexpr int NBUF = (CH && PAIR) ? 1 : 2;         // TMEM accumulators that alternate
+    constexpr int SUM_COL = NBUF * BN;                 // chunked: first column of the running sum
     static_assert(!TF32 || B_KMAJOR, "TF32 products read both operands K-major");
-    static_assert(!CH || (TF32 && BN == 128 && !PAIR && !MC), "chunked accumulation: unpaired TF32 128-wide tiles");
+    static_assert(!CH || (TF32 && !MC && (PAIR ? BN == 256 : BN == 128)),
+                  "chunked accumulation: TF32, unpaired 128-wide or paired 256-wide tiles");
+    static_assert(!CH || SUM_COL + BN <= TCOLS, "running sum inside the TMEM allocation");
     static_assert(!PAIR || BN == 256, "paired products use 128 x 256 tiles per CTA");
     static_assert(!MC || PAIR, "multicast clusters are made of 2-SM pairs");
     constexpr int MM = PAIR ? 2 * BM : BM;      // rows of one product instruction
@@ -767,7 +773,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!ok) break;
                 if (PAIR) tc_commit2(accf0 + 8 * acc, (uint16_t)(0x3u << lead));
                 else tc_commit(accf0 + 8 * acc);
-                acc ^= 1;
+                acc = (acc + 1) % NBUF;
                 if (acc == 0) aphase ^= 1u;
               }
             }
@@ -827,17 +833,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         tmem_ld32(tl + (uint32_t)(acc * BN) + col, v);
                         if (c > 0) {
                             float r[32];
-                            tmem_ld32(tl + (uint32_t)(2 * BN) + col, r);
+                            tmem_ld32(tl + (uint32_t)SUM_COL + col, r);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(r[j], v[j]);
                         }
-                        tmem_st32(tl + (uint32_t)(2 * BN) + col, v);
+                        tmem_st32(tl + (uint32_t)SUM_COL + col, v);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-                    acc ^= 1;
+                    if (lane == 0) {
+                        if (PAIR && (rank & 1)) mbar_arrive_remote(acce0 + 8 * acc, (uint32_t)lead);
+                        else mbar_arrive(acce0 + 8 * acc);
+                    }
+                    acc = (acc + 1) % NBUF;
                     if (acc == 0) aphase ^= 1u;
                 }
                 if (!cok) break;
@@ -868,7 +877,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
                 if (CH && nchunks > 1) {
                     float r[32];
-                    tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(2 * BN + ch * 32), r);
+                    tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(SUM_COL + ch * 32), r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(r[j], v[j]);
                 }
@@ -893,7 +902,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (PAIR && (rank & 1)) mbar_arrive_remote(acce0 + 8 * acc, (uint32_t)lead);
                 else mbar_arrive(acce0 + 8 * acc);
             }
-            acc ^= 1;
+            acc = (acc + 1) % NBUF;
             if (acc == 0) aphase ^= 1u;
         }
         if (tma_groups > 0 && lane == 0) bulk_wait0();   // the stores are complete before the CTA exits
@@ -1077,8 +1086,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t s) {
     const bool pair = (bn == 256) && a.pair != 0;
     const bool mc = pair && a.mc != 0;
     if (tf32) {
-        // chunked accumulation: unpaired 128-wide tiles whatever the tile request
-        if (a.kchunk > 0) return tc::launch_impl<128, true, true, false, false, true>(a, num_sms, s);
+        // chunked accumulation: paired 256-wide tiles when asked for, else unpaired 128-wide
+        if (a.kchunk > 0)
+            return (bn == 256 && pair) ? tc::launch_impl<256, true, true, true, false, true>(a, num_sms, s)
+                                       : tc::launch_impl<128, true, true, false, false, true>(a, num_sms, s);
         if (bn == 128) return tc::launch_impl<128, true, true, false, false>(a, num_sms, s);
         if (!pair) return tc::launch_impl<256, true, true, false, false>(a, num_sms, s);
         return mc ? tc::launch_impl<256, true, true, true, true>(a, num_sms, s)

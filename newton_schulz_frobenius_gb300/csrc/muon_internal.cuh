@@ -20,7 +20,7 @@ constexpr int DT_TF32 = 3;
 // debug product code: TF32 with chunked accumulation (TF32_KCHUNK k-blocks of
 // 32 elements per chunk, chunk sums added in round-to-nearest fp32)
 constexpr int DT_TF32_CHUNKED = 4;
-constexpr int TF32_KCHUNK = 16;
+constexpr int TF32_KCHUNK = 32;
 
 // 16-bit storage that the kind::f16 tensor-core products take (bf16 or fp16).
 __host__ __device__ constexpr bool is_half(int dtype) { return dtype == MUON_BF16 || dtype == MUON_F16; }

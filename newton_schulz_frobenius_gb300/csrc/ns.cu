@@ -84,9 +84,9 @@ GemmArgs gemm_base(int dtype, int* status) {
 // at least 2^30 multiply-adds of X X^T (m^2 n per matrix, times the count).
 // Measured (muon_ns_orthogonalize, best of plain and Gram, ms, FFMA against
 // the tensor path): 640x2560 0.76 / 0.88, 512x2048 0.44 / 0.73, 256x1024 x 4
-// 0.30 / 0.52 below the mark; 1024^2 0.94 / 0.81, 512^2 x 8 0.97 / 0.65,
-// 256x1024 x 16 0.83 / 0.67, 768x3072 1.27 / 1.00, 2048x8192 12.9 / 3.9,
-// 4096^2 29.6 / 11.5 at or above it.  With whole-K accumulation the tensor
+// 0.30 / 0.52 below the mark; 1024^2 0.95 / 0.85, 512^2 x 8 0.96 / 0.71,
+// 256x1024 x 16 0.83 / 0.68, 768x3072 1.26 / 1.03, 2048x8192 12.9 / 3.3,
+// 4096^2 29.5 / 9.8 at or above it.  With whole-K accumulation the tensor
 // path missed the 1e-4 fp32 bar from about 768x3072 (its error grew with K);
 // in chunks it holds at every size tested.
 int fp32_tc_choice(int dtype, int m, int n, int64_t count) {

@@ -77,15 +77,18 @@ def _tf32_rn(x):
     return torch.ldexp(torch.round(torch.ldexp(m, torch.tensor(11, device=x.device))), e - 11).float()
 
 
+@pytest.mark.parametrize("tile_n", [0, 128, 256])
 @pytest.mark.parametrize("M,N,K,batch,sym", [
     (256, 256, 8192, 1, True), (200, 328, 5000, 2, False), (384, 384, 384, 1, True),
-    (130, 130, 2500, 3, True), (64, 520, 700, 1, False)])
-def test_chunked_tf32_product(mg, M, N, K, batch, sym):
+    (130, 130, 2500, 3, True), (64, 520, 700, 1, False), (520, 776, 1500, 1, False)])
+def test_chunked_tf32_product(mg, M, N, K, batch, sym, tile_n):
     """The TF32 product with chunked accumulation on three-pass operands
     ([hi|hi|lo] against [hi|lo|hi], as the fp32 path builds them): its error
     against the exact product of the fp32 values stays at the chunk's level
     for any K, where whole-K accumulation grows with K (about 1.2e-4 at
-    K = 8192).  Ragged M, N and K, several matrices, symmetric launches."""
+    K = 8192).  Ragged M, N and K, several matrices, symmetric launches,
+    unpaired 128-wide tiles and 2-SM pairs (tile_n 256; 0 is the launcher's
+    choice)."""
     g = torch.Generator(device="cuda").manual_seed(M + K)
     X = torch.randn((batch, M, K), generator=g, device="cuda")
     Y = X if sym else torch.randn((batch, N, K), generator=g, device="cuda")
@@ -100,7 +103,7 @@ def test_chunked_tf32_product(mg, M, N, K, batch, sym):
 
     A3, B3 = split(X, "hhl"), split(Y, "hlh")
     C = torch.full((batch, M, N), float("nan"), device="cuda")
-    mg.muon_debug_gemm(A3, B3, C, b_kmajor=True, symmetric=sym, tf32_chunked=True)
+    mg.muon_debug_gemm(A3, B3, C, b_kmajor=True, symmetric=sym, tf32_chunked=True, tile_n=tile_n)
     torch.cuda.synchronize()
     assert mg.muon_sync_status() == mg.MUON_OK
     ref = torch.matmul(X.double(), Y.double().transpose(1, 2))
